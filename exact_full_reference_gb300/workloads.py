@@ -1,0 +1,189 @@
+"""Seeded synthetic luma planes for the parity tests and the benchmark.
+
+This module only draws numbers: it holds none of the statistics' arithmetic, so
+both the CPU oracle's tests and the GPU path's tests can take their inputs from
+it.  The pages measure on fixtures (the Netflix 576x324 pair, Big Buck Bunny at
+3840x2160, full-range noise, a bright 16-bit 1920x1080 pair, checkerboards);
+none of them is available, so each workload below is a synthetic stand-in with
+the shape, bit depth, frame count and value distribution of one such case.
+
+Random numbers: numpy ``PCG64``; frame f of a workload draws from child f of
+``SeedSequence(seed)``, so any frame can be regenerated alone.  Rounding of
+normal noise is ``np.rint`` (half to even); results are clipped to
+``[0, 2^bpc - 1]``.  Planes are returned as arrays of shape (frames, h, w),
+``uint8`` at 8 bits and ``uint16`` otherwise.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    width: int
+    height: int
+    bpc: int
+    n_frames: int
+    seed: int
+    kind: str
+    note: str = ""
+
+    @property
+    def dtype(self):
+        return np.uint8 if self.bpc == 8 else np.uint16
+
+    @property
+    def bytes_per_sample(self):
+        return 1 if self.bpc == 8 else 2
+
+    @property
+    def frame_bytes(self):
+        """Bytes of one plane of one frame (dense rows)."""
+        return self.width * self.height * self.bytes_per_sample
+
+    @property
+    def pair_bytes(self):
+        """Bytes read per frame pair (each plane once)."""
+        return 2 * self.frame_bytes
+
+    def generate(self, frames=None):
+        """Return ``(ref, dist)`` for the frames listed (default: all)."""
+        idx = range(self.n_frames) if frames is None else list(frames)
+        children = np.random.SeedSequence(self.seed).spawn(self.n_frames)
+        ref = np.empty((len(idx), self.height, self.width), self.dtype)
+        dist = np.empty_like(ref)
+        for k, f in enumerate(idx):
+            rng = np.random.Generator(np.random.PCG64(children[f]))
+            ref[k], dist[k] = _FRAME_MAKERS[self.kind](self, rng, f)
+        return ref, dist
+
+
+def _clip(a, bpc, dtype):
+    return np.clip(a, 0, (1 << bpc) - 1).astype(dtype)
+
+
+def _noisy_copy(sigma):
+    """8-bit Netflix-pair stand-in: uniform reference, reference plus rounded
+    N(0, sigma^2) as the distorted plane."""
+
+    def make(wl, _rng, _f):
+        ref = _rng.integers(0, 1 << wl.bpc, (wl.height, wl.width), dtype=np.int64)
+        noise = np.rint(_rng.normal(0.0, sigma, (wl.height, wl.width))).astype(np.int64)
+        return ref.astype(wl.dtype), _clip(ref + noise, wl.bpc, wl.dtype)
+
+    return make
+
+
+def _gradient_texture(wl, rng, _f):
+    """Natural-content stand-in: a smooth diagonal ramp over the full range
+    plus uniform texture of amplitude 64, and a lightly distorted copy
+    (rounded N(0, 4^2))."""
+    top = (1 << wl.bpc) - 1
+    y, x = np.mgrid[0 : wl.height, 0 : wl.width]
+    ramp = np.rint(top * (x + y) / max(wl.width + wl.height - 2, 1)).astype(np.int64)
+    tex = rng.integers(-64, 65, (wl.height, wl.width), dtype=np.int64)
+    ref = np.clip(ramp + tex, 0, top)
+    noise = np.rint(rng.normal(0.0, 4.0, (wl.height, wl.width))).astype(np.int64)
+    return ref.astype(wl.dtype), _clip(ref + noise, wl.bpc, wl.dtype)
+
+
+def _uniform_pair(lo, hi):
+    """Independent uniform planes over [lo, hi] (full-range noise, or the
+    bright 16-bit pair when lo is high)."""
+
+    def make(wl, rng, _f):
+        top = (1 << wl.bpc) - 1
+        a = lo if lo is not None else 0
+        b = hi if hi is not None else top
+        ref = rng.integers(a, b + 1, (wl.height, wl.width), dtype=wl.dtype, endpoint=False)
+        dist = rng.integers(a, b + 1, (wl.height, wl.width), dtype=wl.dtype, endpoint=False)
+        return ref, dist
+
+    return make
+
+
+def checkerboard(width, height, cell, bpc):
+    """Cells of ``cell`` x ``cell`` samples: 0 where (x//cell + y//cell) is
+    even, the top code value elsewhere."""
+    y, x = np.mgrid[0:height, 0:width]
+    top = (1 << bpc) - 1
+    return np.where(((x // cell) + (y // cell)) % 2 == 0, 0, top)
+
+
+def _bright_with_checker(wl, rng, f):
+    """Bright 16-bit 4K stand-in: independent U{60000..65535} planes, except
+    the last frame, a 64x64-cell checkerboard against its inverse."""
+    top = (1 << wl.bpc) - 1
+    if f == wl.n_frames - 1:
+        ref = checkerboard(wl.width, wl.height, 64, wl.bpc)
+        return ref.astype(wl.dtype), (top - ref).astype(wl.dtype)
+    return _uniform_pair(60000, 65535)(wl, rng, f)
+
+
+def _dark_tenth(wl, rng, _f):
+    """Full-range 16-bit noise with a tenth of the samples (same positions in
+    both planes) drawn from U{0..4095} instead."""
+    ref, dist = _uniform_pair(None, None)(wl, rng, _f)
+    mask = rng.random((wl.height, wl.width)) < 0.1
+    ref[mask] = rng.integers(0, 4096, int(mask.sum()), dtype=wl.dtype)
+    dist[mask] = rng.integers(0, 4096, int(mask.sum()), dtype=wl.dtype)
+    return ref, dist
+
+
+def _inverse_pair(wl, rng, _f):
+    """Full-range reference against its inverse: the largest differences."""
+    top = (1 << wl.bpc) - 1
+    ref = rng.integers(0, top + 1, (wl.height, wl.width), dtype=wl.dtype)
+    return ref, (top - ref).astype(wl.dtype)
+
+
+_FRAME_MAKERS = {
+    "noisy_copy_8": _noisy_copy(8.0),
+    "gradient_texture": _gradient_texture,
+    "uniform_full": _uniform_pair(None, None),
+    "uniform_bright": _uniform_pair(56000, 64000),
+    "bright_checker": _bright_with_checker,
+    "dark_tenth": _dark_tenth,
+    "inverse": _inverse_pair,
+}
+
+# The five measured configurations, then the stress frames used only for
+# parity past 2^53 units.
+WORKLOADS = {
+    "576x324_8bit_x1": Workload("576x324_8bit_x1", 576, 324, 8, 1, 1, "noisy_copy_8",
+                                "Netflix 576x324 pair stand-in"),
+    "1920x1080_10bit_x48": Workload("1920x1080_10bit_x48", 1920, 1080, 10, 48, 2,
+                                    "gradient_texture", "natural 10-bit content stand-in"),
+    "3840x2160_12bit_x32": Workload("3840x2160_12bit_x32", 3840, 2160, 12, 32, 3,
+                                    "uniform_full", "full-range 12-bit noise"),
+    "1920x1080_16bit_x64": Workload("1920x1080_16bit_x64", 1920, 1080, 16, 64, 4,
+                                    "uniform_bright", "bright 16-bit 1080p pair stand-in"),
+    "3840x2160_16bit_x32": Workload("3840x2160_16bit_x32", 3840, 2160, 16, 32, 5,
+                                    "bright_checker", "bright 16-bit 4K batch + checkerboard"),
+    "stress_full_range_4k16": Workload("stress_full_range_4k16", 3840, 2160, 16, 2, 11,
+                                       "uniform_full", "full-range 16-bit 4K noise"),
+    "stress_dark_tenth_4k16": Workload("stress_dark_tenth_4k16", 3840, 2160, 16, 2, 12,
+                                       "dark_tenth", "a tenth of the samples below 4096"),
+    "stress_inverse_4k16": Workload("stress_inverse_4k16", 3840, 2160, 16, 2, 13,
+                                    "inverse", "reference against its inverse"),
+}
+
+HEADLINE = "3840x2160_16bit_x32"
+
+
+def with_layout(planes, stride_bytes=None, offset_bytes=0):
+    """Copy dense planes (n, h, w) into a flat byte buffer with row pitch
+    ``stride_bytes`` and ``offset_bytes`` of lead-in, the layout the library
+    takes (frame f at ``offset + f*h*stride``).  Padding bytes are filled with
+    0xA5 so that reading them would show up in the sums."""
+    n, h, w = planes.shape
+    bps = planes.itemsize
+    stride = w * bps if stride_bytes is None else stride_bytes
+    if stride < w * bps:
+        raise ValueError("stride shorter than a row")
+    buf = np.full(offset_bytes + n * h * stride, 0xA5, np.uint8)
+    rows = planes.reshape(n * h, w).view(np.uint8).reshape(n * h, w * bps)
+    view = buf[offset_bytes:].reshape(n * h, stride)
+    view[:, : w * bps] = rows
+    return buf, stride

@@ -1,0 +1,150 @@
+"""CPU oracle for the fused float_psnr noise and float_moment statistics.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The GPU
+library (``exact_full_reference_gb300``) never imports, links or calls it, and
+the two share no code.
+
+The arithmetic lives in ``vqx_oracle.c`` (plain C, strict floating point); this
+module only marshals numpy arrays to it and states the past-2^53 bound of
+"ADR-1447: float_moment_hip adds the float squares the CPU adds ..." (section
+Decision).
+"""
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+SCORES_DTYPE = np.dtype(
+    [
+        ("noise", "<f8"),
+        ("mse", "<f8"),
+        ("psnr", "<f8"),
+        ("psnr_uncapped", "<f8"),
+        ("ref_mean", "<f8"),
+        ("ref_meansq", "<f8"),
+        ("dist_mean", "<f8"),
+        ("dist_meansq", "<f8"),
+    ]
+)
+UNITS_DTYPE = np.dtype(
+    [
+        ("noise_units", "<u8"),
+        ("ref_sum", "<u8"),
+        ("dist_sum", "<u8"),
+        ("ref_sumsq", "<u8"),
+        ("dist_sumsq", "<u8"),
+    ]
+)
+
+
+class Oracle:
+    """ctypes handle on one build of the oracle library (the real one, or a
+    deliberately mutated copy used by the mutation tests)."""
+
+    def __init__(self, lib_path=None):
+        if lib_path is None:
+            lib_path = _build.build_oracle()
+        self.path = lib_path
+        lib = ctypes.CDLL(lib_path)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        lib.vqx_oracle_batch.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
+        lib.vqx_oracle_batch.restype = i
+        lib.vqx_oracle_psnr_cap.argtypes = [i]
+        lib.vqx_oracle_psnr_cap.restype = ctypes.c_double
+        self._lib = lib
+
+    def psnr_cap(self, bpc):
+        return self._lib.vqx_oracle_psnr_cap(bpc)
+
+    def batch(self, ref, dist, width, height, stride, bpc, n_frames, offset=0,
+              scores=True, units=True):
+        """Run the oracle over ``n_frames`` frames.
+
+        ``ref``/``dist`` are numpy arrays holding the planes as raw bytes in the
+        GPU library's layout (frame f at ``offset + f*height*stride`` bytes, row
+        y at ``+ y*stride``).  Returns ``(scores, units)`` structured arrays
+        (either may be ``None`` when not requested)."""
+        ref = np.ascontiguousarray(ref)
+        dist = np.ascontiguousarray(dist)
+        need = offset + (n_frames - 1) * height * stride + (height - 1) * stride + width * (
+            1 if bpc == 8 else 2) if n_frames > 0 else 0
+        if ref.nbytes < need or dist.nbytes < need:
+            raise ValueError("plane buffer smaller than the frame geometry needs")
+        sc = np.zeros(n_frames, SCORES_DTYPE) if scores else None
+        un = np.zeros(n_frames, UNITS_DTYPE) if units else None
+        rc = self._lib.vqx_oracle_batch(
+            ref.ctypes.data + offset,
+            dist.ctypes.data + offset,
+            width,
+            height,
+            stride,
+            bpc,
+            n_frames,
+            sc.ctypes.data if sc is not None else None,
+            un.ctypes.data if un is not None else None,
+        )
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (status %d)" % rc)
+        return sc, un
+
+    def frames(self, ref, dist, bpc, scores=True, units=True):
+        """Convenience form for dense arrays of shape (n, h, w) or (h, w)."""
+        ref = np.asarray(ref)
+        dist = np.asarray(dist)
+        if ref.shape != dist.shape:
+            raise ValueError("ref and dist shapes differ")
+        if ref.ndim == 2:
+            ref = ref[None]
+            dist = dist[None]
+        n, h, w = ref.shape
+        return self.batch(ref, dist, w, h, w * ref.itemsize, bpc, n, scores=scores, units=units)
+
+
+_default = None
+
+
+def load():
+    """The oracle built from ``vqx_oracle.c`` (compiled on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def moment_bound(pixels, e):
+    """Largest distance between the CPU's double running sum and the exact sum
+    rounded once, as a moment, once the sum passes 2^53 units ("ADR-1447 ...",
+    section Decision): at least 2^21 adds are exact (a term is below 2^32
+    units), every later add rounds by at most half an ulp of a sum in binade
+    ``e`` (2^(e-53) units), the exact sum rounded once is within the same, a
+    unit is 2^-16 of a moment divided by the pixel count, and the two final
+    divisions add at most 2^-37."""
+    later = max(pixels - 2 ** 21 + 1, 0)
+    return later / pixels * 2.0 ** (e - 69) + 2.0 ** -37
+
+
+def binade(units):
+    """e with 2^e <= units < 2^(e+1) (units > 0)."""
+    return int(units).bit_length() - 1
+
+
+def mse_bound(pixels, noise_units):
+    """The same bound for the MSE (noise / pixels): its terms are float squares
+    below 2^32 units of 2^-16 too, so the derivation of ``moment_bound`` applies
+    unchanged.  Below 2^53 units the CPU's sum is exact and the bound is 0."""
+    if noise_units < 2 ** 53:
+        return 0.0
+    return moment_bound(pixels, binade(noise_units))
+
+
+def psnr_bound(mse, dmse, psnr):
+    """Bound on |PSNR difference| implied by an MSE difference ``dmse``:
+    d/dmse of 10 log10(c/mse) is -(10/ln 10)/mse; plus a few ulps of the
+    logarithm and the product."""
+    if mse == 0.0 or not math.isfinite(psnr):
+        return 0.0
+    return (10.0 / math.log(10.0)) * dmse / (mse - dmse) + 4.0 * math.ulp(abs(psnr) + 1.0)

@@ -1,0 +1,88 @@
+"""Plant a mistake in a copy of the oracle and show that a pin catches it.
+
+Each mutant is a textual change of ``oracle/vqx_oracle.c`` that a careless
+implementation of the pages could plausibly contain.  The copy is compiled with
+the oracle's own flags into a temporary directory and every pin of
+``oracle_checks`` is run on it: at least one must fail.  (CPU only; the planted
+mistakes live in the oracle copy, never in the GPU path.)
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_checks as oc
+from oracle import build as obuild
+
+MUTANTS = [
+    ("exact integer difference square",
+     "float dsq = diff * diff;\n            noise += (uint64_t)dsq;",
+     "noise += (uint64_t)((long long)(r - d) * (long long)(r - d));"),
+    ("exact integer sample squares",
+     "float rsq = (float)r * (float)r;",
+     "double rsq = (double)r * (double)r;"),
+    ("noise square taken in double",
+     "float sq = e * e;",
+     "double sq = (double)e * (double)e;"),
+    ("noise accumulated in float",
+     "double noise = 0.0;",
+     "float noise = 0.0f;"),
+    ("moment accumulated in float",
+     "double sum = 0.0, sum2 = 0.0;",
+     "float sum = 0.0f, sum2 = 0.0f;"),
+    ("scaler 2^bpc in the noise",
+     "const float scaler = (float)(1u << (bpc - 8));\n    double noise",
+     "const float scaler = (float)(1u << bpc);\n    double noise"),
+    ("scaler 2^bpc in the moments",
+     "const float scaler = (float)(1u << (bpc - 8));\n    double sum",
+     "const float scaler = (float)(1u << bpc);\n    double sum"),
+    ("sum instead of difference",
+     "float e = r - d;",
+     "float e = r + d;"),
+    ("second moment without the square",
+     "const float term = pic * pic;",
+     "const float term = pic;"),
+    ("first moment divided by n - 1",
+     "*mean = sum / n;",
+     "*mean = sum / (n - 1.0);"),
+    ("MSE divided by the width only",
+     "out->mse = out->noise / ((double)w * (double)h);",
+     "out->mse = out->noise / (double)w;"),
+    ("peak 2^bpc - 1 instead of 255",
+     "10.0 * log10(255.0 * 255.0 / out->mse)",
+     "10.0 * log10(1023.0 * 1023.0 / out->mse)"),
+    ("no PSNR cap",
+     "out->psnr = out->psnr_uncapped < cap ? out->psnr_uncapped : cap;",
+     "out->psnr = out->psnr_uncapped;"),
+    ("distorted moments taken from the reference",
+     "plane_moments(d, w, h, stride, bpc, &out->dist_mean, &out->dist_meansq);",
+     "plane_moments(r, w, h, stride, bpc, &out->dist_mean, &out->dist_meansq);"),
+    ("row pitch ignored",
+     "const unsigned char *rrow = ref + (size_t)y * stride;",
+     "const unsigned char *rrow = ref + (size_t)y * (size_t)w * (bpc == 8 ? 1u : 2u);"),
+    ("sample byte order swapped",
+     "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return v;",
+     "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return (uint16_t)((v >> 8) | (v << 8));"),
+]
+
+
+def _build_mutant(tmp_path, old, new):
+    src = open(obuild.SRC).read()
+    assert src.count(old) == 1, "mutation anchor must occur exactly once: %r" % old
+    path = os.path.join(tmp_path, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    return obuild.build_oracle(src=path, out=os.path.join(tmp_path, "libmutant.so"), force=True)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    mut = oracle.Oracle(_build_mutant(str(tmp_path), old, new))
+    caught = None
+    for check in oc.ALL_CHECKS:
+        try:
+            check(mut)
+        except (AssertionError, ValueError, OverflowError, ZeroDivisionError):
+            caught = check.__name__
+            break
+    assert caught, "no pin catches the planted mistake: " + name
