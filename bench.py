@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Throughput of the fused PSNR-noise + moment statistics on GB300.
+
+One step = one ``vqx_plane_stats`` call (the whole hot path: load, per-pixel
+terms, exact integer reduction, per-frame sums, read-back, conclusion in
+double) over one batch of synthetic planes already resident in HBM.  The
+default batch is 32 frame pairs of 3840x2160 16-bit luma (1.06 GB, larger than
+L2, so no flush is needed between steps).
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job frame pairs/s; ``e2e``
+is the same metric through ``vqx_plane_stats_host`` with the planes in pinned
+host memory (copies inside the timed region); ``roofline`` is the fused
+kernel's algorithmic bytes per launch over its CUDA-event launch time against
+the measured HBM copy bandwidth; ``cpu_baseline`` is the CPU oracle on this
+host's cores on a bounded sample.
+
+``--impl reference`` times the CPU oracle itself as the reference arm (there is
+no runnable reference implementation of this path).  Under torchrun (N > 1)
+every rank runs its own batch (frames are independent: weak scaling, no
+collective in the data path); rank 0 prints.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "frame pairs/s and HBM GB/s (fused PSNR+moments), 3840x2160 16-bit, 1 GB300"
+UNIT = "frame pairs/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None, help="workload name (default: the 3840x2160 16-bit batch)")
+    p.add_argument("--e2e-steps", type=int, default=60)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 100 ms, stamped with host time when read."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id is not None:
+            cmd += ["-i", str(gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:  # a short timed region: take the samples nearest to it
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for _, p in near]
+            note = "no sample inside the timed region; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        pw = [num(p[3]) for p in inside if num(p[3]) is not None]
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": num(inside[0][2]),
+            "reasons": reasons,
+            "power_w_max": max(pw) if pw else None,
+            "samples": len(inside),
+            "note": note,
+        }
+
+
+def gpu_smi_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- roofline inputs
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_full_reference_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "fused_dense_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_digest():
+        return None
+    per = rec.get("per_launch_bytes", {}).get(workload_name)
+    return float(per) if per is not None else None
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1):
+    """Run the CPU oracle over frames (or bands of ``rows`` rows) of the batch
+    on ``cores`` threads until ``seconds`` have passed.  Returns (pairs/s,
+    pairs done, elapsed s).  ctypes drops the GIL inside the C calls."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    orc = oracle.load()
+    n, h, w = ref.shape
+    band = h if rows is None else max(1, min(rows, h))
+    stride = w * ref.itemsize
+
+    def one(k):
+        f = k % n
+        y0 = (k * 7919) % (h - band + 1) if band < h else 0
+        orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
+        return band
+
+    done_rows = 0
+    k = 0
+    t0 = time.perf_counter()
+    rounds = 0
+    with ThreadPoolExecutor(cores) as ex:
+        while True:
+            done_rows += sum(ex.map(one, range(k, k + cores)))
+            k += cores
+            rounds += 1
+            if rounds >= min_rounds and time.perf_counter() - t0 >= seconds:
+                break
+    el = time.perf_counter() - t0
+    pairs = done_rows / h
+    return pairs / el, pairs, el
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, wlo):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    frames = list(range(min(wlo.n_frames, max(cores, 1))))
+    ref, dist = wlo.generate(frames)
+    # size one step so that warm-up plus timed steps take about two minutes
+    per_step_s = min(0.5, 120.0 / max(args.steps + args.warmup, 1))
+    rate, _, _ = time_oracle(wlo, ref, dist, 0.0, 1, rows=64)  # one thread, calibration
+    rows_per_s = rate * wlo.height
+    rows = int(max(1, min(wlo.height, rows_per_s * per_step_s)))
+    for _ in range(args.warmup):
+        time_oracle(wlo, ref, dist, 0.0, cores, rows=rows)
+    t0 = time.perf_counter()
+    pairs = 0.0
+    for _ in range(args.steps):
+        _, p, _ = time_oracle(wlo, ref, dist, 0.0, cores, rows=rows)
+        pairs += p
+    el = time.perf_counter() - t0
+    value = pairs / el
+    sample = ("%d bands of %d rows (of %d) of %s frames per step, one band per thread"
+              % (cores, rows, wlo.height, wlo.name))
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / max(args.steps, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 terms, f64 sums",
+        "data": "synthetic",
+        "config": {"workload": wlo.name, "frames": wlo.n_frames, "width": wlo.width,
+                   "height": wlo.height, "bpc": wlo.bpc, "oracle": "plain C, raster-order double sums"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, wlo):
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    __import__("__graft_entry__").build()
+    import exact_full_reference_gb300 as vqx
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+
+    ref, dist_np = wlo.generate()
+    n, h, w = ref.shape
+    stride = w * wlo.bytes_per_sample
+    rbytes = ref.reshape(-1).view(np.uint8)
+    dbytes = dist_np.reshape(-1).view(np.uint8)
+    d_ref = torch.from_numpy(rbytes).to(dev)
+    d_dist = torch.from_numpy(dbytes).to(dev)
+    torch.cuda.synchronize()
+
+    so = vqx.library()
+    out = np.zeros(n, vqx.FRAME_STATS_DTYPE)
+    out_p = out.ctypes.data
+    call_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh, out_p)
+
+    def step():
+        rc = so.vqx_plane_stats(*call_args)
+        if rc != 0:
+            raise RuntimeError("vqx_plane_stats: %s" % vqx.status_string(rc))
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_smi_id(torch, dev))
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    vqx.profile_enable(True)
+    vqx.profile_read(reset=True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    prof = vqx.profile_read(reset=True)
+    vqx.profile_enable(False)
+    time.sleep(0.2)
+    clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if pg is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    value = world * n * args.steps / (elapsed_ms / 1e3)
+
+    # roofline of the fused kernel, from the events recorded inside the calls
+    peak, peak_kind = measured_peak()
+    launches = max(prof["stage1_launches"], 1)
+    avg_ms = prof["stage1_ms"] / launches
+    bytes_per_launch = prof["stage1_bytes"] / launches
+    achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
+    traffic = recorded_traffic(wlo.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                "kernel": "fused_dense<%d>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
+                "bytes_per_launch": bytes_per_launch,
+                "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
+
+    # end to end: planes in pinned host memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h_ref = torch.from_numpy(rbytes).pin_memory()
+        h_dist = torch.from_numpy(dbytes).pin_memory()
+        e2e_out = np.zeros(n, vqx.FRAME_STATS_DTYPE)
+        e2e_args = (h_ref.data_ptr(), h_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh,
+                    e2e_out.ctypes.data)
+        for _ in range(3):
+            rc = so.vqx_plane_stats_host(*e2e_args)
+            if rc != 0:
+                raise RuntimeError("vqx_plane_stats_host: %s" % vqx.status_string(rc))
+        assert e2e_out.tobytes() == out.tobytes(), "host-memory path disagrees with the device path"
+        k = max(1, min(args.e2e_steps, args.steps))
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(k):
+            so.vqx_plane_stats_host(*e2e_args)
+        torch.cuda.synchronize()
+        el = time.perf_counter() - t0
+        if pg is not None:
+            t = torch.tensor([el], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            el = float(t.item())
+        e2e = {"value": world * n * k / el, "unit": UNIT, "steps": k,
+               "h2d_bytes_per_step": int(rbytes.nbytes + dbytes.nbytes),
+               "d2h_bytes_per_step": int(n * ctypes.sizeof(ctypes.c_uint64) * 6),
+               "api": "vqx_plane_stats_host (pinned host planes)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cores = host_cores()
+        sub = list(range(min(n, cores)))
+        rate, pairs, el = time_oracle(wlo, ref[sub], dist_np[sub], args.cpu_seconds, cores)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%.1f frame pairs of %s (whole frames, one per thread) in %.1f s"
+                         % (pairs, wlo.name, el)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "u16 samples, f32 terms, u64 sums",
+            "data": "synthetic",
+            "hbm_gbs": value * wlo.pair_bytes / 1e9 / world,
+            "config": {"workload": wlo.name, "frames_per_gpu": n, "width": w, "height": h,
+                       "bpc": wlo.bpc, "batch_bytes": int(rbytes.nbytes + dbytes.nbytes),
+                       "l2": "inputs 1.06 GB per step, larger than the 129 MB L2; no flush",
+                       "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
+            "e2e": e2e,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "clocks": clocks.summary(t_wall0, t_wall1),
+            "gpu_launches": int(prof["kernel_launches"]),
+        }
+        if wlo.pair_bytes * n < 256 << 20:
+            line["config"]["l2"] = "batch smaller than L2: timings include L2 hits"
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    from exact_full_reference_gb300 import workloads as wl
+
+    wlo = wl.WORKLOADS[args.workload or wl.HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, wlo)
+    return run_ours(args, wlo)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

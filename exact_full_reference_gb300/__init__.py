@@ -1,0 +1,196 @@
+"""Python binding of the vqx C ABI (``include/vqx.h``): argument marshalling only.
+
+Every step of the statistics runs in ``libvqx.so`` (CUDA kernels for sm_103a
+plus the host conclusion in C++).  This module loads that library with ctypes,
+turns tensors / arrays into pointers and sizes, and returns the per-frame
+records as a numpy structured array.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+
+PyTorch is used only as a source of device memory and streams: anything with a
+``data_ptr()`` method (a CUDA tensor) or a plain integer address is accepted.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvqx.so")
+
+VQX_OK = 0
+VQX_EINVAL = -1
+VQX_EBPC = -2
+VQX_ERANGE = -3
+VQX_ECUDA = -4
+VQX_ENOMEM = -5
+VQX_FLAG_RANGE = 1
+VQX_MAX_FRAME_PIXELS = 1 << 25
+
+FRAME_STATS_DTYPE = np.dtype(
+    [
+        ("noise_units", "<u8"),
+        ("ref_sum", "<u8"),
+        ("dist_sum", "<u8"),
+        ("ref_sumsq", "<u8"),
+        ("dist_sumsq", "<u8"),
+        ("flags", "<u4"),
+        ("reserved", "<u4"),
+        ("noise", "<f8"),
+        ("mse", "<f8"),
+        ("psnr", "<f8"),
+        ("psnr_uncapped", "<f8"),
+        ("ref_mean", "<f8"),
+        ("ref_meansq", "<f8"),
+        ("dist_mean", "<f8"),
+        ("dist_meansq", "<f8"),
+    ]
+)
+
+
+class VqxProfile(ctypes.Structure):
+    _fields_ = [
+        ("calls", ctypes.c_uint64),
+        ("kernel_launches", ctypes.c_uint64),
+        ("stage1_launches", ctypes.c_uint64),
+        ("stage1_ms", ctypes.c_double),
+        ("stage2_ms", ctypes.c_double),
+        ("stage1_bytes", ctypes.c_uint64),
+    ]
+
+
+class VqxError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+
+def library():
+    """The loaded ``libvqx.so``; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                "libvqx.so is not built (%s); run exact_full_reference_gb300.build.build_library()"
+                % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        for name in ("vqx_plane_stats", "vqx_plane_stats_host"):
+            fn = getattr(lib, name)
+            fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
+            fn.restype = i
+        lib.vqx_psnr_cap.argtypes = [i]
+        lib.vqx_psnr_cap.restype = ctypes.c_double
+        lib.vqx_status_string.argtypes = [i]
+        lib.vqx_status_string.restype = ctypes.c_char_p
+        lib.vqx_last_cuda_error.argtypes = []
+        lib.vqx_last_cuda_error.restype = i
+        lib.vqx_profile_enable.argtypes = [i]
+        lib.vqx_profile_enable.restype = None
+        lib.vqx_profile_read.argtypes = [ctypes.POINTER(VqxProfile), i]
+        lib.vqx_profile_read.restype = None
+        _lib = lib
+    return _lib
+
+
+def _address(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError("expected a tensor, an ndarray or an integer address, got %r" % type(x))
+
+
+def _stream_handle(stream):
+    if stream is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _geometry(ref, width, height, stride, n_frames, bpc):
+    bps = 1 if bpc == 8 else 2
+    shape = tuple(getattr(ref, "shape", ()))
+    if width is None or height is None:
+        if len(shape) < 2:
+            raise ValueError("width and height are needed for a flat buffer")
+        height, width = int(shape[-2]), int(shape[-1])
+        if n_frames is None:
+            n_frames = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+        if stride is None:
+            stride = width * bps
+    if stride is None:
+        stride = width * bps
+    if n_frames is None:
+        n_frames = 1
+    return width, height, stride, n_frames
+
+
+def status_string(status):
+    return library().vqx_status_string(status).decode()
+
+
+def psnr_cap(bpc):
+    return library().vqx_psnr_cap(bpc)
+
+
+def _call(name, ref, dist, width, height, stride, bpc, n_frames, stream, out, check):
+    width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
+    if out is None:
+        out = np.zeros(max(n_frames, 0), FRAME_STATS_DTYPE)
+    rc = getattr(library(), name)(
+        _address(ref), _address(dist), width, height, stride, bpc, n_frames, stream,
+        out.ctypes.data if out.size else None)
+    if check and rc not in (VQX_OK,):
+        msg = "%s failed: %s (%d)" % (name, status_string(rc), rc)
+        if rc == VQX_ECUDA:
+            msg += ", cudaError %d" % library().vqx_last_cuda_error()
+        raise VqxError(rc, msg)
+    return out, rc
+
+
+def vqx_plane_stats(ref, dist, width=None, height=None, stride=None, bpc=16, n_frames=None,
+                    stream=None, out=None, check=True):
+    """Per-frame statistics of device-resident planes.
+
+    ``ref``/``dist``: CUDA tensors (shape (n, h, w) or (h, w); any dtype whose
+    bytes hold the samples) or device addresses with explicit geometry.
+    ``stride`` is in bytes.  Returns a structured array of ``n_frames``
+    records (``FRAME_STATS_DTYPE``).  With ``check=False`` returns
+    ``(records, status)`` instead of raising on a non-zero status."""
+    out, rc = _call("vqx_plane_stats", ref, dist, width, height, stride, bpc, n_frames,
+                    _stream_handle(stream), out, check)
+    return out if check else (out, rc)
+
+
+def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16,
+                         n_frames=None, stream=None, out=None, check=True):
+    """The same for planes in host memory (numpy arrays, pinned tensors or
+    host addresses): the library copies them to the device in chunks."""
+    out, rc = _call("vqx_plane_stats_host", ref, dist, width, height, stride, bpc, n_frames,
+                    _stream_handle(stream), out, check)
+    return out if check else (out, rc)
+
+
+def profile_enable(on=True):
+    library().vqx_profile_enable(1 if on else 0)
+
+
+def profile_read(reset=False):
+    p = VqxProfile()
+    library().vqx_profile_read(ctypes.byref(p), 1 if reset else 0)
+    return {k: getattr(p, k) for k, _ in VqxProfile._fields_}

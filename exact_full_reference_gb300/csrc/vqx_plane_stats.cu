@@ -1,0 +1,516 @@
+// Host side of the C ABI declared in include/vqx.h.
+//
+// A call validates its arguments, plans the launch (layout path and how many
+// segments each frame is split into, so that the grid is a whole number of
+// resident waves on this GPU), takes a stream-ordered workspace for the
+// per-CTA records from a library-owned memory pool, launches the fused
+// stage-1 kernel and the per-frame stage-2 kernel, waits for the stream and
+// concludes the scores from the exact integer sums in double on the host.
+//
+// The conclusion ("ADR-1440: float_psnr_hip adds its squared differences as
+// integers ...", Decision: the host puts the integer sums together in double
+// and divides by scaler^2; "ADR-1447: float_moment_hip adds the float squares
+// the CPU adds ...", Decision: the two final divisions) is compiled with
+// contraction off, and uses only divisions, one product by 10 and log10.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "vqx.h"
+#include "vqx_kernels.cuh"
+
+namespace {
+
+using vqx::Partial;
+using vqx::u64;
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return e == cudaErrorMemoryAllocation ? VQX_ENOMEM : VQX_ECUDA;
+}
+
+// ------------------------------------------------------------------ paths
+enum Path { kDense = 0, kRowsVec = 1, kRowsScalar = 2, kPaths = 3 };
+
+int bpc_index(int bpc) { return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3; }
+
+template <int BPC>
+const void *stage1_kernel(int path) {
+    switch (path) {
+    case kDense: return (const void *)vqx::fused_dense<BPC>;
+    case kRowsVec: return (const void *)vqx::fused_rows<BPC, true>;
+    default: return (const void *)vqx::fused_rows<BPC, false>;
+    }
+}
+
+const void *stage1_kernel(int path, int bpc) {
+    switch (bpc) {
+    case 8: return stage1_kernel<8>(path);
+    case 10: return stage1_kernel<10>(path);
+    case 12: return stage1_kernel<12>(path);
+    default: return stage1_kernel<16>(path);
+    }
+}
+
+// ------------------------------------------------------------------ device state
+// Per-device state, made once: SM count, resident CTAs per SM of every
+// stage-1 variant, the library's stream-ordered memory pool (memory stays
+// in the pool between calls, so a call allocates nothing from the driver
+// once warm) and a copy stream for the host-memory entry point.
+struct DeviceCtx {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    int resident[kPaths][4] = {};
+    cudaMemPool_t pool = nullptr;
+    cudaStream_t copy_stream = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceCtx g_dev[kMaxDevices];
+
+cudaError_t init_device(DeviceCtx &c, int dev) {
+    cudaError_t e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int bpcs[4] = {8, 10, 12, 16};
+    for (int p = 0; p < kPaths; p++)
+        for (int b = 0; b < 4; b++) {
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stage1_kernel(p, bpcs[b]),
+                                                              vqx::kThreads, 0);
+            if (e != cudaSuccess) return e;
+            c.resident[p][b] = n > 0 ? n : 1;
+        }
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&c.pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;  // never hand memory back between calls
+    e = cudaMemPoolSetAttribute(c.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return e;
+    return cudaStreamCreateWithFlags(&c.copy_stream, cudaStreamNonBlocking);
+}
+
+int device_ctx(DeviceCtx **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return VQX_EINVAL;
+    DeviceCtx &c = g_dev[dev];
+    std::call_once(c.once, [&] { c.err = init_device(c, dev); });
+    if (c.err != cudaSuccess) return cuda_status(c.err);
+    *out = &c;
+    return VQX_OK;
+}
+
+// ------------------------------------------------------------------ pinned records
+// Pinned, device-mapped host buffers that stage 2 writes the per-frame sums
+// into.  A call takes one from the free list and returns it afterwards, so
+// concurrent calls never share one.
+struct PinnedBuf {
+    void *host = nullptr;
+    void *dev = nullptr;
+    size_t cap = 0;
+};
+std::mutex g_pinned_mu;
+std::vector<PinnedBuf> g_pinned_free;
+
+int acquire_pinned(size_t bytes, PinnedBuf *out) {
+    {
+        std::lock_guard<std::mutex> lk(g_pinned_mu);
+        for (size_t i = 0; i < g_pinned_free.size(); i++)
+            if (g_pinned_free[i].cap >= bytes) {
+                *out = g_pinned_free[i];
+                g_pinned_free.erase(g_pinned_free.begin() + (long)i);
+                return VQX_OK;
+            }
+    }
+    size_t cap = 4096;
+    while (cap < bytes) cap *= 2;
+    PinnedBuf b;
+    cudaError_t e = cudaHostAlloc(&b.host, cap, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaHostGetDevicePointer(&b.dev, b.host, 0);
+    if (e != cudaSuccess) {
+        cudaFreeHost(b.host);
+        return cuda_status(e);
+    }
+    b.cap = cap;
+    *out = b;
+    return VQX_OK;
+}
+
+void release_pinned(const PinnedBuf &b) {
+    std::lock_guard<std::mutex> lk(g_pinned_mu);
+    g_pinned_free.push_back(b);
+}
+
+// ------------------------------------------------------------------ profiling
+struct Profiler {
+    bool on = false;
+    bool events_ready = false;
+    cudaEvent_t ev[3] = {};
+    vqx_profile totals = {};
+};
+thread_local Profiler t_prof;
+
+bool profiling_events() {
+    if (!t_prof.on) return false;
+    if (!t_prof.events_ready) {
+        for (auto &e : t_prof.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return false;
+        t_prof.events_ready = true;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ validation
+int bytes_per_sample(int bpc) { return bpc == 8 ? 1 : 2; }
+
+int validate(const void *ref, const void *dist, int width, int height, size_t stride, int bpc,
+             int n_frames, const vqx_frame_stats *out) {
+    if (bpc != 8 && bpc != 10 && bpc != 12 && bpc != 16) return VQX_EBPC;
+    if (n_frames < 0) return VQX_EINVAL;
+    if (n_frames == 0) return VQX_OK;
+    if (!ref || !dist || !out) return VQX_EINVAL;
+    if (width <= 0 || height <= 0) return VQX_EINVAL;
+    if ((uint64_t)width * (uint64_t)height > VQX_MAX_FRAME_PIXELS) return VQX_EINVAL;
+    const size_t bps = (size_t)bytes_per_sample(bpc);
+    if (stride < (size_t)width * bps) return VQX_EINVAL;
+    if (bps == 2 && (((uintptr_t)ref | (uintptr_t)dist | (uintptr_t)stride) & 1u)) return VQX_EINVAL;
+    // the whole batch must be addressable
+    const unsigned __int128 span = (unsigned __int128)n_frames * (unsigned __int128)height * stride;
+    if (span > (unsigned __int128)(SIZE_MAX / 2)) return VQX_EINVAL;
+    return VQX_OK;
+}
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+    int path = kDense;
+    int bpc = 8;
+    int segs = 1;
+    uint32_t work = 0;      // 16-byte vectors (dense) or rows per frame
+    uint32_t seg_work = 0;  // per segment
+    size_t frame_pitch = 0;
+    size_t stride = 0;
+    int width = 0, height = 0;
+};
+
+// Segments per frame: the grid (frames x segments CTAs) should fill whole
+// waves of resident CTAs, so that no SM idles at the end; among equally full
+// grids the one with fewer waves (bigger segments) wins.
+int choose_segs(long long frames, uint32_t work, uint32_t min_unit, long long resident) {
+    long long max_segs = work / min_unit;
+    if (max_segs < 1) max_segs = 1;
+    // More than four waves buys no better fill; it only shrinks the units.
+    const long long four_waves = (4 * resident + frames - 1) / frames;
+    if (max_segs > four_waves) max_segs = four_waves;
+    while (max_segs > 1 && frames * max_segs > (1ll << 30)) max_segs /= 2;
+    int best = 1;
+    double best_eff = -1.0;
+    long long best_waves = 0;
+    for (long long s = 1; s <= max_segs; s++) {
+        const long long units = frames * s;
+        const long long waves = (units + resident - 1) / resident;
+        const double eff = (double)units / (double)(waves * resident);
+        if (eff > best_eff + 1e-9 || (eff > best_eff - 1e-9 && waves < best_waves)) {
+            best = (int)s;
+            best_eff = eff;
+            best_waves = waves;
+        }
+    }
+    return best;
+}
+
+Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width, int height,
+               size_t stride, int bpc, long long frames_per_launch) {
+    Plan p;
+    p.bpc = bpc;
+    p.width = width;
+    p.height = height;
+    p.stride = stride;
+    p.frame_pitch = (size_t)height * stride;
+    const size_t row_bytes = (size_t)width * (size_t)bytes_per_sample(bpc);
+    const bool aligned = (((uintptr_t)ref | (uintptr_t)dist) & 15u) == 0;
+    const size_t frame_bytes = row_bytes * (size_t)height;
+    if (aligned && stride == row_bytes && (frame_bytes & 15u) == 0) {
+        p.path = kDense;
+        p.work = (uint32_t)(frame_bytes >> 4);
+    } else {
+        p.path = (aligned && (stride & 15u) == 0) ? kRowsVec : kRowsScalar;
+        p.work = (uint32_t)height;
+    }
+    const long long resident = (long long)c.sms * c.resident[p.path][bpc_index(bpc)];
+    const uint32_t min_unit = p.path == kDense ? (uint32_t)vqx::kThreads : 8u;
+    p.segs = choose_segs(frames_per_launch, p.work, min_unit, resident);
+    p.seg_work = (p.work + (uint32_t)p.segs - 1) / (uint32_t)p.segs;
+    return p;
+}
+
+template <int BPC>
+cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const unsigned char *dist,
+                              int frame0, int frames, Partial *partials, cudaStream_t st) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((long long)frames * p.segs));
+    cfg.blockDim = dim3(vqx::kThreads);
+    cfg.stream = st;
+    if (p.path == kDense)
+        return cudaLaunchKernelEx(&cfg, vqx::fused_dense<BPC>, ref, dist, p.frame_pitch,
+                                  p.work, p.seg_work, p.segs, frame0, partials);
+    if (p.path == kRowsVec)
+        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, true>, ref, dist, p.frame_pitch,
+                                  p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
+                                  partials);
+    return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false>, ref, dist, p.frame_pitch,
+                              p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
+                              partials);
+}
+
+cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int frame0,
+                          int frames, Partial *partials, cudaStream_t st) {
+    const unsigned char *r = (const unsigned char *)ref;
+    const unsigned char *d = (const unsigned char *)dist;
+    switch (p.bpc) {
+    case 8: return launch_stage1_bpc<8>(p, r, d, frame0, frames, partials, st);
+    case 10: return launch_stage1_bpc<10>(p, r, d, frame0, frames, partials, st);
+    case 12: return launch_stage1_bpc<12>(p, r, d, frame0, frames, partials, st);
+    default: return launch_stage1_bpc<16>(p, r, d, frame0, frames, partials, st);
+    }
+}
+
+cudaError_t launch_stage2(const Plan &p, int n_frames, const Partial *partials, Partial *out,
+                          cudaStream_t st) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)n_frames);
+    cfg.blockDim = dim3(vqx::kSumThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, vqx::frame_sums, partials, p.segs, out);
+}
+
+// ------------------------------------------------------------------ conclusion
+void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats *o) {
+    const double S = (double)(1u << (bpc - 8));
+    const double S2 = S * S;
+    const double n = (double)width * (double)height;
+    o->noise_units = s.v[0];
+    o->ref_sum = s.v[1];
+    o->dist_sum = s.v[2];
+    o->ref_sumsq = s.v[3];
+    o->dist_sumsq = s.v[4];
+    o->flags = (s.v[5] >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
+    o->reserved = 0;
+    o->noise = (double)s.v[0] / S2;
+    o->mse = o->noise / n;
+    o->psnr_uncapped = 10.0 * log10(255.0 * 255.0 / o->mse);
+    const double cap = vqx_psnr_cap(bpc);
+    o->psnr = o->psnr_uncapped < cap ? o->psnr_uncapped : cap;
+    o->ref_mean = ((double)s.v[1] / S) / n;
+    o->ref_meansq = ((double)s.v[3] / S2) / n;
+    o->dist_mean = ((double)s.v[2] / S) / n;
+    o->dist_meansq = ((double)s.v[4] / S2) / n;
+}
+
+int conclude_all(const Partial *sums, int n_frames, int bpc, int width, int height,
+                 vqx_frame_stats *out) {
+    int rc = VQX_OK;
+    for (int f = 0; f < n_frames; f++) {
+        conclude(sums[f], bpc, width, height, &out[f]);
+        if (out[f].flags & VQX_FLAG_RANGE) rc = VQX_ERANGE;
+    }
+    return rc;
+}
+
+// Bytes the fused kernel reads for a batch (both planes, each sample once).
+uint64_t plane_bytes(int width, int height, int bpc, int n_frames) {
+    return 2ull * (uint64_t)width * (uint64_t)height * (uint64_t)bytes_per_sample(bpc) *
+           (uint64_t)n_frames;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+double vqx_psnr_cap(int bpc) {
+    if (bpc != 8 && bpc != 10 && bpc != 12 && bpc != 16) return NAN;
+    return 6.0 * bpc + 12.0;
+}
+
+const char *vqx_status_string(int status) {
+    switch (status) {
+    case VQX_OK: return "ok";
+    case VQX_EINVAL: return "invalid argument";
+    case VQX_EBPC: return "unsupported bit depth (8, 10, 12 or 16)";
+    case VQX_ERANGE: return "a sample is out of range for the bit depth";
+    case VQX_ECUDA: return "CUDA runtime error";
+    case VQX_ENOMEM: return "out of memory";
+    default: return "unknown status";
+    }
+}
+
+int vqx_last_cuda_error(void) { return t_last_cuda_error; }
+
+void vqx_profile_enable(int enable) { t_prof.on = enable != 0; }
+
+void vqx_profile_read(vqx_profile *out, int reset) {
+    if (out) *out = t_prof.totals;
+    if (reset) t_prof.totals = vqx_profile{};
+}
+
+int vqx_plane_stats(const void *ref, const void *dist, int width, int height, size_t stride,
+                    int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Plan plan = make_plan(*ctx, ref, dist, width, height, stride, bpc, n_frames);
+
+    PinnedBuf rec;
+    if ((rc = acquire_pinned((size_t)n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)n_frames * plan.segs * sizeof(Partial),
+                                            ctx->pool, st);
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    Partial *partials = (Partial *)ws;
+    const bool prof = profiling_events();
+    if (prof) cudaEventRecord(t_prof.ev[0], st);
+    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st);
+    if (e == cudaSuccess && prof) cudaEventRecord(t_prof.ev[1], st);
+    if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)rec.dev, st);
+    if (e == cudaSuccess && prof) cudaEventRecord(t_prof.ev[2], st);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    const cudaError_t es = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    t_prof.totals.calls++;
+    t_prof.totals.kernel_launches += 2;
+    t_prof.totals.stage1_launches += 1;
+    t_prof.totals.stage1_bytes += plane_bytes(width, height, bpc, n_frames);
+    if (prof) {
+        float a = 0.f, b = 0.f;
+        cudaEventElapsedTime(&a, t_prof.ev[0], t_prof.ev[1]);
+        cudaEventElapsedTime(&b, t_prof.ev[1], t_prof.ev[2]);
+        t_prof.totals.stage1_ms += a;
+        t_prof.totals.stage2_ms += b;
+    }
+    rc = conclude_all((const Partial *)rec.host, n_frames, bpc, width, height, out);
+    release_pinned(rec);
+    return rc;
+}
+
+int vqx_plane_stats_host(const void *ref, const void *dist, int width, int height,
+                         size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                         vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    // Device copies of the planes keep the host byte layout but start on a
+    // 256-byte boundary.  The last row of the last frame may end before the
+    // frame pitch does: copy only the bytes that exist.
+    const size_t pitch = (size_t)height * stride;
+    const size_t row_bytes = (size_t)width * (size_t)bytes_per_sample(bpc);
+    const size_t batch_bytes = (size_t)(n_frames - 1) * pitch + (size_t)(height - 1) * stride + row_bytes;
+    const size_t plane_alloc = (batch_bytes + 255) & ~(size_t)255;
+
+    // Chunks of frames: copy chunk k+1 while chunk k is reduced.
+    int chunk = n_frames;
+    const size_t target = (size_t)64 << 20;  // about 64 MB of each plane per chunk
+    if (pitch > 0 && (size_t)n_frames * pitch > target) {
+        chunk = (int)(target / pitch);
+        if (chunk < 1) chunk = 1;
+    }
+    const int n_chunks = (n_frames + chunk - 1) / chunk;
+
+    // Plan with the device copies' alignment (256-byte aligned bases).
+    const Plan plan = make_plan(*ctx, (const void *)(uintptr_t)256, (const void *)(uintptr_t)256,
+                                width, height, stride, bpc, chunk);
+
+    PinnedBuf rec;
+    if ((rc = acquire_pinned((size_t)n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
+    void *ws = nullptr;
+    const size_t part_bytes = ((size_t)n_frames * plan.segs * sizeof(Partial) + 255) & ~(size_t)255;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, 2 * plane_alloc + part_bytes + 256, ctx->pool, st);
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    unsigned char *dr = (unsigned char *)(((uintptr_t)ws + 255) & ~(uintptr_t)255);
+    unsigned char *dd = dr + plane_alloc;
+    Partial *partials = (Partial *)(dd + plane_alloc);
+
+    std::vector<cudaEvent_t> evs;
+    cudaEvent_t ready = nullptr;
+    e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ready, st);  // the workspace exists from here
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->copy_stream, ready, 0);
+    for (int k = 0; e == cudaSuccess && k < n_chunks; k++) {
+        const int f0 = k * chunk;
+        const int nf = (f0 + chunk <= n_frames) ? chunk : n_frames - f0;
+        const size_t off = (size_t)f0 * pitch;
+        const size_t bytes = (size_t)(nf - 1) * pitch + (size_t)(height - 1) * stride + row_bytes;
+        e = cudaMemcpyAsync(dr + off, (const unsigned char *)ref + off, bytes,
+                            cudaMemcpyHostToDevice, ctx->copy_stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dd + off, (const unsigned char *)dist + off, bytes,
+                                cudaMemcpyHostToDevice, ctx->copy_stream);
+        cudaEvent_t ev = nullptr;
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e == cudaSuccess) {
+            evs.push_back(ev);
+            e = cudaEventRecord(ev, ctx->copy_stream);
+        }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev, 0);
+        if (e == cudaSuccess) e = launch_stage1(plan, dr, dd, f0, nf, partials, st);
+    }
+    if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)rec.dev, st);
+    // Every copy issued into the workspace must be over before the workspace
+    // is freed, also when the loop stopped early on an error: wait for the
+    // copy stream on the host (all copies are queued by now, so this costs
+    // nothing), then free in the compute stream's order.
+    const cudaError_t ec = cudaStreamSynchronize(ctx->copy_stream);
+    if (e == cudaSuccess) e = ec;
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    const cudaError_t es = cudaStreamSynchronize(st);
+    for (cudaEvent_t ev : evs) cudaEventDestroy(ev);
+    if (ready) cudaEventDestroy(ready);
+    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    t_prof.totals.calls++;
+    t_prof.totals.kernel_launches += (uint64_t)n_chunks + 1;
+    t_prof.totals.stage1_launches += (uint64_t)n_chunks;
+    t_prof.totals.stage1_bytes += plane_bytes(width, height, bpc, n_frames);
+    rc = conclude_all((const Partial *)rec.host, n_frames, bpc, width, height, out);
+    release_pinned(rec);
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+/*
+ * vqx: exact per-frame PSNR-noise and moment statistics of luma plane pairs
+ * on one NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * What is computed, per frame pair (a reference plane r and a distorted plane
+ * d of w x h samples at bpc bits, scaler S = 2^(bpc - 8), N = w * h):
+ *
+ *   float_psnr  ("ADR-1440: float_psnr_hip adds its squared differences as
+ *               integers and returns the CPU's score bit for bit", Context and
+ *               Decision): noise = sum over pixels of the float square of the
+ *               float difference of the scaled samples, mse = noise / N,
+ *               psnr = 10 log10(255^2 / mse), capped.
+ *   float_moment ("ADR-1447: float_moment_hip adds the float squares the CPU
+ *               adds, and is bit-identical while the CPU's own sum is exact",
+ *               Context and Decision): mean = sum(s / S) / N and
+ *               meansq = sum(float(s/S * s/S)) / N for both planes.
+ *
+ * How: every per-pixel term is formed in fp32 exactly as the CPU forms it
+ * (one round-to-nearest-even product, no contraction) and is an integer in
+ * units of 1/S^2 (1/S for the plain samples), so the library adds the terms
+ * as integers, exactly and in any order, on the device, and converts the
+ * integer sums to the scores on the host in double.  The scores are
+ * therefore bit-identical to the CPU's wherever the CPU's double sum is
+ * exact (every frame at 8, 10 and 12 bits, and 16-bit frames of up to 2^21
+ * pixels), and past that point they are the exact sum rounded once, within
+ * the bound ADR-1447 (Decision) states.
+ *
+ * Sample layout (all entry points): bpc 8 = one byte per sample; bpc 10, 12
+ * and 16 = one little-endian uint16 per sample (the low bpc bits; a sample
+ * of 2^bpc or more is an error, VQX_ERANGE).  Row y of frame f starts
+ * f * height * stride + y * stride bytes after the plane's base pointer;
+ * both planes use the same stride and the same frame pitch.  Planes of
+ * uint16 samples must be 2-byte aligned (base and stride).
+ */
+#ifndef VQX_H
+#define VQX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *vqx_stream_t;
+
+/* Status codes: 0 on success, negative on failure. */
+#define VQX_OK 0
+#define VQX_EINVAL (-1)  /* null pointer, size <= 0, stride too short,
+                            misaligned uint16 plane, frame over 2^25 pixels */
+#define VQX_EBPC (-2)    /* bpc not one of 8, 10, 12, 16 */
+#define VQX_ERANGE (-3)  /* a sample >= 2^bpc was read (results are still
+                            written; the frames concerned carry
+                            VQX_FLAG_RANGE) */
+#define VQX_ECUDA (-4)   /* a CUDA runtime call failed; see
+                            vqx_last_cuda_error() */
+#define VQX_ENOMEM (-5)  /* device or pinned host memory could not be had */
+
+/* Largest frame accepted, in pixels (w * h).  Up to 12 bits the exact noise
+ * sum then needs at most 49 bits (ADR-1440, Context: "at most 49 bits at
+ * any frame size the library accepts"; 2^24 * 2^25 = 2^49). */
+#define VQX_MAX_FRAME_PIXELS (1u << 25)
+
+/* vqx_frame_stats.flags */
+#define VQX_FLAG_RANGE 1u /* the frame holds a sample >= 2^bpc */
+
+/* Results for one frame pair.  The integer fields are the exact sums on the
+ * device ("debug" accumulators); the doubles are concluded from them. */
+typedef struct {
+    uint64_t noise_units;     /* sum of float(D * D), D = r - d raw; unit 1/S^2 */
+    uint64_t ref_sum;         /* sum of r; unit 1/S */
+    uint64_t dist_sum;        /* sum of d; unit 1/S */
+    uint64_t ref_sumsq;       /* sum of float(r * r); unit 1/S^2 */
+    uint64_t dist_sumsq;      /* sum of float(d * d); unit 1/S^2 */
+    uint32_t flags;           /* VQX_FLAG_* */
+    uint32_t reserved;
+    double noise;             /* noise_units / S^2 */
+    double mse;               /* noise / N (the 8-bit scale) */
+    double psnr;              /* min(psnr_uncapped, vqx_psnr_cap(bpc)) */
+    double psnr_uncapped;     /* 10 log10(255^2 / mse); +inf when mse == 0 */
+    double ref_mean, ref_meansq;   /* (ref_sum / S) / N, (ref_sumsq / S^2) / N */
+    double dist_mean, dist_meansq; /* the same for the distorted plane */
+} vqx_frame_stats;
+
+/*
+ * vqx_plane_stats: the fused pass over device-resident planes.
+ *
+ *   ref, dist  device pointers (caller-owned, read only, not retained) to
+ *              n_frames frames laid out as above.
+ *   width, height  samples per row, rows per frame (>= 1; w * h at most
+ *              VQX_MAX_FRAME_PIXELS).
+ *   stride     bytes from one row to the next (>= width * bytes per sample).
+ *   bpc        8, 10, 12 or 16.
+ *   n_frames   frames in the batch (0 is an empty batch: returns VQX_OK and
+ *              touches nothing).
+ *   stream     the CUDA stream the work is ordered on; it must belong to the
+ *              current device.  The call waits for the stream before it
+ *              returns (out is filled on return).
+ *   out        host array of n_frames records (caller-owned).
+ *
+ * The library owns only short-lived memory: a stream-ordered device
+ * workspace from its own memory pool and a pinned host record buffer, both
+ * reused across calls.  No device memory is cleared before use: every device
+ * buffer is written before it is read.  Calls on different streams or
+ * threads may run concurrently.  Returns VQX_OK or a negative status; on an
+ * argument error nothing is launched and out is untouched.
+ */
+int vqx_plane_stats(const void *ref, const void *dist, int width, int height, size_t stride,
+                    int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out);
+
+/*
+ * vqx_plane_stats_host: the same results for planes in host memory.  The
+ * frames are copied to the device in chunks on an internal copy stream while
+ * earlier chunks are reduced on `stream` (copy and compute overlap); pinned
+ * host memory (cudaHostAlloc / cudaHostRegister) gives asynchronous copies,
+ * pageable memory works but copies synchronously.  Arguments as for
+ * vqx_plane_stats, with ref and dist host pointers.
+ */
+int vqx_plane_stats_host(const void *ref, const void *dist, int width, int height,
+                         size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                         vqx_frame_stats *out);
+
+/* The PSNR cap in dB for a bit depth (6 * bpc + 12: 60, 72, 84, 108), or a
+ * NaN for an unsupported bpc.  ADR-1440 (Consequences) shows that a cap
+ * exists but does not print its value; this value is a stated choice. */
+double vqx_psnr_cap(int bpc);
+
+/* A static, human-readable description of a status code. */
+const char *vqx_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this thread inside
+ * the library (0 if none). */
+int vqx_last_cuda_error(void);
+
+/* Per-thread counters of the library's work.  Calls, kernel launches and
+ * bytes read are always counted (both entry points).  Device times are
+ * measured only while enabled: each vqx_plane_stats call then records CUDA
+ * events on the caller's stream around its fused kernel and its per-frame
+ * kernel.  vqx_profile_read returns the totals since the last reset. */
+typedef struct {
+    uint64_t calls;            /* successful calls */
+    uint64_t kernel_launches;  /* library kernels launched by those calls */
+    uint64_t stage1_launches;  /* of which fused load/reduce launches */
+    double stage1_ms;          /* device time of the fused launches (enabled only) */
+    double stage2_ms;          /* device time of the per-frame sums (enabled only) */
+    uint64_t stage1_bytes;     /* plane bytes the fused launches read */
+} vqx_profile;
+
+void vqx_profile_enable(int enable);
+void vqx_profile_read(vqx_profile *out, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQX_H */

@@ -1,0 +1,115 @@
+"""The C-ABI library builds, loads and exports what include/vqx.h declares;
+argument checks that need no GPU (CPU only: no compute call is made)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(vqx_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_status_string",
+              "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = lib.library()
+    for name in declared_functions():
+        assert hasattr(so, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert set(declared_functions()) <= exported
+    # the statically linked CUDA runtime stays private
+    assert not any(s.startswith("cuda") for s in exported), sorted(
+        s for s in exported if s.startswith("cuda"))[:5]
+
+
+def test_status_strings_and_caps(lib):
+    assert lib.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5):
+        assert lib.status_string(code) not in ("ok", "unknown status")
+    assert lib.status_string(-99) == "unknown status"
+    assert [lib.psnr_cap(b) for b in (8, 10, 12, 16)] == [60.0, 72.0, 84.0, 108.0]
+    assert math.isnan(lib.psnr_cap(9))
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+@pytest.mark.parametrize(
+    "args,status",
+    [
+        (dict(bpc=9), -2),
+        (dict(bpc=0), -2),
+        (dict(width=0), -1),
+        (dict(height=-3), -1),
+        (dict(n_frames=-1), -1),
+        (dict(stride=2 * 64 - 2), -1),
+        (dict(ref=0), -1),
+        (dict(dist=0), -1),
+        (dict(ref=FAKE + 1), -1),  # odd address, 16-bit samples
+        (dict(stride=2 * 64 + 1), -1),  # odd stride, 16-bit samples
+        (dict(width=8192, height=4097, stride=8192 * 2), -1),  # over 2^25 pixels
+        (dict(bpc=8, width=1 << 13, height=(1 << 12) + 1, stride=1 << 13), -1),
+    ],
+)
+def test_argument_errors_need_no_gpu(lib, args, status):
+    a = dict(ref=FAKE, dist=FAKE, width=64, height=4, stride=128, bpc=16, n_frames=2)
+    a.update(args)
+    out = (ctypes.c_char * (152 * 4))()
+    so = lib.library()
+    for name in ("vqx_plane_stats", "vqx_plane_stats_host"):
+        rc = getattr(so, name)(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
+                               a["stride"], a["bpc"], a["n_frames"], None, out)
+        assert rc == status, (name, args, rc)
+
+
+def test_empty_batch_is_ok_without_gpu(lib):
+    so = lib.library()
+    assert so.vqx_plane_stats(None, None, 0, 0, 0, 16, 0, None, None) == 0
+    assert so.vqx_plane_stats_host(None, None, 0, 0, 0, 8, 0, None, None) == 0
+
+
+def test_null_output_rejected(lib):
+    so = lib.library()
+    assert so.vqx_plane_stats(FAKE, FAKE, 4, 4, 8, 16, 1, None, None) == -1
+
+
+def test_record_layout_matches_header(lib):
+    # 5 uint64 + 2 uint32 + 8 doubles = 112 bytes, no padding
+    assert lib.FRAME_STATS_DTYPE.itemsize == 112
+    assert ctypes.sizeof(lib.VqxProfile) == 48
+
+
+def test_profile_counters_without_gpu(lib):
+    lib.profile_enable(True)
+    p = lib.profile_read(reset=True)
+    assert p["calls"] == 0 and p["stage1_ms"] == 0.0
+    lib.profile_enable(False)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import exact_full_reference_gb300 as vqx
+
+    monkeypatch.setattr(vqx, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(vqx, "_lib", None)
+    with pytest.raises(ImportError):
+        vqx.library()

@@ -1,0 +1,217 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every output of every frame is compared (see ``parity.compare``): the integer
+sums always exactly, the scores bit for bit in the exact range and within the
+stated bound past it.
+"""
+import threading
+
+import numpy as np
+import pytest
+
+import parity
+from exact_full_reference_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_case(lib, orc, ref, dist, bpc, stride=None, offset_ref=0, offset_dist=0):
+    n, h, w = ref.shape
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist, stride, offset_ref, offset_dist)
+    rec = lib.vqx_plane_stats(pr, pd, w, h, stride, bpc, n)
+    torch.cuda.synchronize()
+    sc, un = orc.batch(rb, db, w, h, stride, bpc, n)
+    parity.compare(rec, sc, un, bpc, w * h)
+    return rec, sc, un
+
+
+# ------------------------------------------------------------- full workloads
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workload_parity(lib, orc, name):
+    """The measured configurations at full size (every frame, the launch the
+    benchmark times) and the past-2^53 stress frames."""
+    w = wl.WORKLOADS[name]
+    ref, dist = w.generate()
+    rec, sc, un = run_case(lib, orc, ref, dist, w.bpc)
+    if name.startswith("stress"):
+        # these are chosen to leave the exact range
+        assert parity.exact_count(un) < len(un)
+    elif w.bpc < 16 or w.width * w.height <= 2 ** 21:
+        assert parity.exact_count(un) == len(un)
+
+
+def test_headline_checkerboard_frame(lib, orc):
+    """The checkerboard frame of the 3840x2160 16-bit batch, alone."""
+    w = wl.WORKLOADS["3840x2160_16bit_x32"]
+    ref, dist = w.generate([w.n_frames - 1])
+    rec, sc, un = run_case(lib, orc, ref, dist, 16)
+    assert int(rec[0]["noise_units"]) == 3840 * 2160 * 4294836224
+
+
+# ------------------------------------------------------------- shapes and layouts
+SHAPES = [(1, 1), (1, 7), (7, 1), (3, 5), (17, 13), (64, 1), (1, 300), (33, 31), (130, 9),
+          (576, 2), (1000, 3), (8, 16), (16, 16), (24, 40)]
+
+
+@pytest.mark.parametrize("bpc", [8, 10, 12, 16])
+@pytest.mark.parametrize("w,h", SHAPES)
+def test_small_shapes_dense(lib, orc, bpc, w, h):
+    rng = np.random.Generator(np.random.PCG64(w * 1000 + h * 10 + bpc))
+    dt = np.uint8 if bpc == 8 else np.uint16
+    ref = rng.integers(0, 1 << bpc, (3, h, w)).astype(dt)
+    dist = rng.integers(0, 1 << bpc, (3, h, w)).astype(dt)
+    run_case(lib, orc, ref, dist, bpc)
+
+
+@pytest.mark.parametrize("bpc", [8, 10, 12, 16])
+@pytest.mark.parametrize(
+    "w,h,pad,off_r,off_d",
+    [
+        (100, 7, 16, 0, 0),     # padded, 16-byte aligned rows: vector path with a tail
+        (96, 5, 32, 0, 0),
+        (37, 9, 6, 0, 0),       # padded, unaligned rows: scalar path
+        (64, 4, 0, 2, 2),       # dense but both bases off a 16-byte boundary
+        (64, 4, 0, 0, 6),       # ref aligned, dist not
+        (333, 3, 2, 4, 8),
+        (1921, 3, 14, 0, 0),
+    ],
+)
+def test_layouts(lib, orc, bpc, w, h, pad, off_r, off_d):
+    bps = 1 if bpc == 8 else 2
+    rng = np.random.Generator(np.random.PCG64(7 * w + h + bpc))
+    dt = np.uint8 if bpc == 8 else np.uint16
+    ref = rng.integers(0, 1 << bpc, (4, h, w)).astype(dt)
+    dist = rng.integers(0, 1 << bpc, (4, h, w)).astype(dt)
+    if bps == 2:
+        pad += pad % 2
+    run_case(lib, orc, ref, dist, bpc, stride=w * bps + pad, offset_ref=off_r, offset_dist=off_d)
+
+
+def test_large_frame_at_the_limit(lib, orc):
+    """A single 16-bit frame of exactly 2^25 pixels (8192 x 4096)."""
+    rng = np.random.Generator(np.random.PCG64(99))
+    ref = rng.integers(0, 1 << 16, (1, 4096, 8192), dtype=np.uint16)
+    dist = rng.integers(0, 1 << 16, (1, 4096, 8192), dtype=np.uint16)
+    run_case(lib, orc, ref, dist, 16)
+
+
+def test_many_small_frames(lib, orc):
+    rng = np.random.Generator(np.random.PCG64(5))
+    ref = rng.integers(0, 1024, (3000, 6, 10)).astype(np.uint16)
+    dist = rng.integers(0, 1024, (3000, 6, 10)).astype(np.uint16)
+    run_case(lib, orc, ref, dist, 10)
+
+
+# ------------------------------------------------------------- boundary behaviour
+def test_range_flag(lib, orc):
+    """A 10-bit frame holding 1024 is flagged; the call reports VQX_ERANGE and
+    still fills every record (the integers are the sums of what was read)."""
+    rng = np.random.Generator(np.random.PCG64(3))
+    ref = rng.integers(0, 1024, (3, 8, 24)).astype(np.uint16)
+    dist = rng.integers(0, 1024, (3, 8, 24)).astype(np.uint16)
+    ref[1, 5, 7] = 1024
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    rec, rc = lib.vqx_plane_stats(pr, pd, 24, 8, stride, 10, 3, check=False)
+    assert rc == lib.VQX_ERANGE
+    assert [int(f) for f in rec["flags"]] == [0, 1, 0]
+    _, un = orc.batch(rb, db, 24, 8, stride, 10, 3, scores=False)
+    for k in parity.UNIT_FIELDS:
+        assert [int(x) for x in rec[k]] == [int(x) for x in un[k]]
+
+
+def test_no_stale_state_between_calls(lib, orc):
+    """ADR-1423 (Context, cause 3): a later, larger call must not see an
+    earlier call's sums.  Small call, then a larger one on a new stream."""
+    a = wl.WORKLOADS["576x324_8bit_x1"]
+    ref, dist = a.generate()
+    run_case(lib, orc, ref, dist, 8)
+    s = torch.cuda.Stream()
+    rng = np.random.Generator(np.random.PCG64(17))
+    big_r = rng.integers(0, 65536, (5, 1080, 1920), dtype=np.uint16)
+    big_d = rng.integers(0, 65536, (5, 1080, 1920), dtype=np.uint16)
+    with torch.cuda.stream(s):
+        run_case(lib, orc, big_r, big_d, 16)
+
+
+def test_concurrent_calls_on_two_streams(lib, orc):
+    rng = np.random.Generator(np.random.PCG64(21))
+    cases = []
+    for k in range(2):
+        r = rng.integers(0, 4096, (6, 540, 960)).astype(np.uint16)
+        d = rng.integers(0, 4096, (6, 540, 960)).astype(np.uint16)
+        keep, pr, pd, stride, (rb, db) = parity.place(r, d)
+        sc, un = orc.batch(rb, db, 960, 540, stride, 12, 6)
+        cases.append((keep, pr, pd, stride, sc, un))
+    results = [None, None]
+
+    def worker(k):
+        s = torch.cuda.Stream()
+        keep, pr, pd, stride, _, _ = cases[k]
+        outs = []
+        for _ in range(20):
+            outs.append(lib.vqx_plane_stats(pr, pd, 960, 540, stride, 12, 6, stream=s.cuda_stream))
+        results[k] = outs
+
+    th = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    for k in range(2):
+        for rec in results[k]:
+            parity.compare(rec, cases[k][4], cases[k][5], 12, 960 * 540)
+
+
+def test_repeat_calls_are_identical(lib):
+    w = wl.WORKLOADS["1920x1080_16bit_x64"]
+    ref, dist = w.generate(range(8))
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    a = lib.vqx_plane_stats(pr, pd, 1920, 1080, stride, 16, 8)
+    b = lib.vqx_plane_stats(pr, pd, 1920, 1080, stride, 16, 8)
+    assert a.tobytes() == b.tobytes()
+
+
+def test_empty_batch(lib):
+    rec = lib.vqx_plane_stats(0, 0, 0, 0, 0, 16, 0)
+    assert rec.size == 0
+
+
+def test_host_entry_point_matches(lib, orc):
+    """vqx_plane_stats_host (pageable numpy, pinned tensor, padded rows) gives
+    the device path's records."""
+    w = wl.WORKLOADS["3840x2160_12bit_x32"]
+    ref, dist = w.generate(range(6))
+    rb, stride = wl.with_layout(ref)
+    db, _ = wl.with_layout(dist)
+    host = lib.vqx_plane_stats_host(rb, db, 3840, 2160, stride, 12, 6)
+    sc, un = orc.batch(rb, db, 3840, 2160, stride, 12, 6)
+    parity.compare(host, sc, un, 12, 3840 * 2160)
+    pr = torch.from_numpy(rb).pin_memory()
+    pdd = torch.from_numpy(db).pin_memory()
+    pinned = lib.vqx_plane_stats_host(pr.data_ptr(), pdd.data_ptr(), 3840, 2160, stride, 12, 6)
+    assert pinned.tobytes() == host.tobytes()
+    rp, stride_p = wl.with_layout(ref[:3], 3840 * 2 + 10)
+    dp, _ = wl.with_layout(dist[:3], 3840 * 2 + 10)
+    padded = lib.vqx_plane_stats_host(rp, dp, 3840, 2160, stride_p, 12, 3)
+    assert padded.tobytes() == host[:3].tobytes()
+
+
+def test_profile_counts_launches(lib):
+    w = wl.WORKLOADS["576x324_8bit_x1"]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    lib.profile_enable(True)
+    lib.profile_read(reset=True)
+    for _ in range(3):
+        lib.vqx_plane_stats(pr, pd, 576, 324, stride, 8, 1)
+    p = lib.profile_read(reset=True)
+    lib.profile_enable(False)
+    assert p["calls"] == 3 and p["kernel_launches"] == 6 and p["stage1_launches"] == 3
+    assert p["stage1_ms"] > 0 and p["stage1_bytes"] == 3 * 2 * 576 * 324
