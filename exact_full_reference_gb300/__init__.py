@@ -25,6 +25,7 @@ VQX_ECUDA = -4
 VQX_ENOMEM = -5
 VQX_FLAG_RANGE = 1
 VQX_MAX_FRAME_PIXELS = 1 << 25
+VQX_NOALLOC_MAX_RECORDS = 65536
 
 FRAME_STATS_DTYPE = np.dtype(
     [
@@ -77,7 +78,7 @@ def library():
                 % LIB_PATH)
         lib = ctypes.CDLL(LIB_PATH)
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-        for name in ("vqx_plane_stats", "vqx_plane_stats_host"):
+        for name in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_stats_noalloc"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
@@ -182,6 +183,16 @@ def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16
     """The same for planes in host memory (numpy arrays, pinned tensors or
     host addresses): the library copies them to the device in chunks."""
     out, rc = _call("vqx_plane_stats_host", ref, dist, width, height, stride, bpc, n_frames,
+                    _stream_handle(stream), out, check)
+    return out if check else (out, rc)
+
+
+def vqx_plane_stats_noalloc(ref, dist, width=None, height=None, stride=None, bpc=16,
+                            n_frames=None, stream=None, out=None, check=True):
+    """The allocation-free variant (device planes, at most
+    ``VQX_NOALLOC_MAX_RECORDS // 2`` frames a call; calls must not overlap
+    on the GPU)."""
+    out, rc = _call("vqx_plane_stats_noalloc", ref, dist, width, height, stride, bpc, n_frames,
                     _stream_handle(stream), out, check)
     return out if check else (out, rc)
 

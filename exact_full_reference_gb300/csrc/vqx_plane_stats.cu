@@ -514,3 +514,92 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
 }
 
 }  // extern "C"
+
+// ====================================================================== no-allocation variant
+// vqx_plane_stats_noalloc runs the same two kernels as vqx_plane_stats, but
+// its scratch (the per-CTA records and the per-frame sums) is the file-scope
+// array below instead of memory taken from a pool, and the per-frame sums are
+// copied into the caller's own output array instead of a pinned buffer.  It
+// therefore never allocates: not at set-up, not per call.
+static __device__ __align__(256) vqx::Partial g_noalloc_scratch[VQX_NOALLOC_MAX_RECORDS];
+
+namespace {
+
+// Per-device set-up, done by the first call on each device with that device
+// current: the scratch array's device address (in host code the array's name
+// is only a host-side stand-in, so kernels must be given this address), the
+// SM count and the resident CTAs of each stage-1 variant for planning.
+struct NoAllocCtx {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    Partial *scratch = nullptr;
+    DeviceCtx planning;  // only sms and resident are filled in
+};
+NoAllocCtx g_noalloc[kMaxDevices];
+
+cudaError_t init_noalloc(NoAllocCtx &c, int dev) {
+    cudaError_t e = cudaGetSymbolAddress((void **)&c.scratch, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (c.scratch == nullptr) return cudaErrorInvalidSymbol;
+    e = cudaDeviceGetAttribute(&c.planning.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int bpcs[4] = {8, 10, 12, 16};
+    for (int p = 0; p < kPaths; p++)
+        for (int b = 0; b < 4; b++) {
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stage1_kernel(p, bpcs[b]),
+                                                              vqx::kThreads, 0);
+            if (e != cudaSuccess) return e;
+            c.planning.resident[p][b] = n > 0 ? n : 1;
+        }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int width, int height,
+                                       size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                                       vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    // one record per frame for the sums plus at least one per frame for stage 1
+    if ((long long)n_frames * 2 > (long long)VQX_NOALLOC_MAX_RECORDS) return VQX_EINVAL;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return VQX_EINVAL;
+    NoAllocCtx &c = g_noalloc[dev];
+    std::call_once(c.once, [&] { c.err = init_noalloc(c, dev); });
+    if (c.err != cudaSuccess) return cuda_status(c.err);
+
+    Plan plan = make_plan(c.planning, ref, dist, width, height, stride, bpc, n_frames);
+    const long long room = (long long)VQX_NOALLOC_MAX_RECORDS / n_frames - 1;  // >= 1
+    if (plan.segs > room) {
+        plan.segs = (int)room;
+        plan.seg_work = (plan.work + (uint32_t)plan.segs - 1) / (uint32_t)plan.segs;
+    }
+    Partial *partials = c.scratch;
+    Partial *sums = c.scratch + (size_t)n_frames * plan.segs;
+    cudaStream_t st = (cudaStream_t)stream;
+    // Every record is written before it is read, so the scratch needs no
+    // clearing between calls.
+    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st);
+    if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, sums, st);
+    // The sums (48 bytes a frame) land in the front of the caller's array,
+    // which has 112 bytes a frame; they are concluded in place below.
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(out, sums, (size_t)n_frames * sizeof(Partial), cudaMemcpyDeviceToHost, st);
+    const cudaError_t es = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = es;
+    if (e != cudaSuccess) return cuda_status(e);
+    // Last frame first: record f starts at byte 112 f, at or after the sums of
+    // every frame below f, so no sums are overwritten before they are read.
+    rc = VQX_OK;
+    for (int f = n_frames - 1; f >= 0; f--) {
+        Partial s_f;
+        memcpy(&s_f, (const unsigned char *)out + (size_t)f * sizeof(Partial), sizeof s_f);
+        conclude(s_f, bpc, width, height, &out[f]);
+        if (out[f].flags & VQX_FLAG_RANGE) rc = VQX_ERANGE;
+    }
+    return rc;
+}

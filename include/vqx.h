@@ -150,6 +150,45 @@ typedef struct {
 void vqx_profile_enable(int enable);
 void vqx_profile_read(vqx_profile *out, int reset);
 
+/*
+ * Records held by the static scratch of vqx_plane_stats_noalloc: 65536
+ * records of 48 bytes (3 MiB of device memory on every GPU that loads the
+ * library, held until the process exits).
+ */
+#define VQX_NOALLOC_MAX_RECORDS 65536
+
+/*
+ * vqx_plane_stats_noalloc: vqx_plane_stats for callers that cannot allocate.
+ * (An addition of this library, with no counterpart in the pages it follows.)
+ *
+ * Some callers must not allocate memory once they run: a real-time video
+ * pipeline whose frame deadline cannot absorb a device or pinned allocation
+ * (these can take driver locks or wait for the device), or a host
+ * application that hands all of the GPU's memory to its own allocator and
+ * lets no library take memory behind its back.  This entry point allocates
+ * nothing, in any call, the first one included: its scratch is a
+ * fixed-size array in the library's device memory, and the per-frame sums
+ * are copied straight into `out`.
+ *
+ * Arguments, results and status codes are those of vqx_plane_stats.  The
+ * batch may hold at most VQX_NOALLOC_MAX_RECORDS / 2 frames; a larger
+ * n_frames is rejected with VQX_EINVAL before anything runs.  Large frames
+ * may be split into fewer segments than vqx_plane_stats uses, so a batch of
+ * many frames can run somewhat slower; the results are identical.
+ *
+ * The first call on each device (with that device current) looks up the
+ * scratch array's device address; make that first call before any stream
+ * capture.  Every call uses the same scratch array, which keeps the last
+ * call's contents; nothing in it needs to start at zero, because every
+ * record is written before it is read.  Two calls whose work overlaps on the
+ * GPU (calls on different streams, or from different threads, at the same
+ * time) use the same scratch and race: serialise them, or use
+ * vqx_plane_stats.
+ */
+int vqx_plane_stats_noalloc(const void *ref, const void *dist, int width, int height,
+                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                            vqx_frame_stats *out);
+
 #ifdef __cplusplus
 }
 #endif
