@@ -345,7 +345,7 @@ def run_ours(args, wlo):
     traffic = recorded_traffic(wlo.name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                "kernel": "fused_dense<%d>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
+                "kernel": "fused_dense_tma<%d, 16, 1024, 3>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
                 "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
 

@@ -23,7 +23,9 @@ VQX_EBPC = -2
 VQX_ERANGE = -3
 VQX_ECUDA = -4
 VQX_ENOMEM = -5
+VQX_ETIMEOUT = -6
 VQX_FLAG_RANGE = 1
+VQX_FLAG_TIMEOUT = 2
 VQX_MAX_FRAME_PIXELS = 1 << 25
 VQX_NOALLOC_MAX_RECORDS = 65536
 

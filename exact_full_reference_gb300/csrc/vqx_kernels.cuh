@@ -1,10 +1,13 @@
 // Device side of the fused PSNR-noise + moment reduction (sm_103a).
 //
-// Stage 1 (fused_dense / fused_rows): one pass over both planes.  Each CTA
-// owns one (frame, segment) unit, streams its samples with 16-byte
-// non-allocating loads, forms the per-pixel terms and adds them as integers;
-// warp shuffles and a shared-memory step reduce the CTA to one Partial record,
-// which it *writes* (no atomics, nothing to clear beforehand).
+// Stage 1 (fused_dense_tma / fused_rows): one pass over both planes, in
+// (frame, segment) units.  Dense planes stream through a persistent TMA
+// pipeline (bulk copies into a shared-memory ring, mbarrier hand-off to
+// consumer warps); other layouts are read row by row with 16-byte
+// non-allocating loads.  The per-pixel terms are formed and added as
+// integers; warp shuffles and a shared-memory step reduce each unit to one
+// Partial record, which is *written* (no atomics, nothing to clear
+// beforehand).
 //
 // Stage 2 (frame_sums): one CTA per frame adds the frame's Partial records
 // (integers, so the order is irrelevant and the result deterministic) and
@@ -34,9 +37,18 @@ struct Partial {
     u64 v[6];
 };
 
-constexpr int kThreads = 256;      // stage-1 CTA size
-constexpr int kSumThreads = 128;   // stage-2 CTA size
-constexpr int kUnroll = 2;         // 16-byte vectors per plane in flight per thread
+constexpr int kThreads = 256;     // CTA size of the strided-layout stage-1 kernel
+constexpr int kSumThreads = 128;  // stage-2 CTA size
+
+// Shape of the dense-layout stage-1 pipeline (fused_dense_tma): consumer
+// warps, 16-byte vectors per plane per stage, stages in the ring.  Chosen by
+// measurement on GB300 over 8-, 10-, 12- and 16-bit batches of 3840x2160 and
+// 1920x1080 frames; two CTAs (96 KB of ring each) are resident per SM.
+constexpr int kTmaWarps = 16;
+constexpr int kTmaStageVecs = 1024;
+constexpr int kTmaStages = 3;
+constexpr int kTmaThreads = (kTmaWarps + 1) * 32;
+constexpr size_t kTmaSmem = (size_t)kTmaStages * 2 * kTmaStageVecs * 16;
 
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
@@ -64,6 +76,64 @@ __device__ __forceinline__ void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- TMA + mbarriers
+// Bulk copies (cp.async.bulk, the TMA engine's 1-D form) from global to shared
+// memory, completed on an mbarrier by transaction bytes.  Every wait on an
+// mbarrier is bounded: after about a second (kWaitCycles SM clock cycles) it
+// gives up, and the kernel marks its record with kErrTimeout (the host then
+// reports VQX_ETIMEOUT) instead of spinning forever.
+constexpr long long kWaitCycles = 2000000000ll;
+constexpr u64 kErrTimeout = 1ull << 63;  // in Partial::v[5]
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait until the phase of parity `parity` has completed; false after `limit`
+// SM clock cycles without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+// bytes (a multiple of 16) from 16-byte aligned global src to 16-byte
+// aligned shared dst, completing `bytes` transactions on mbarrier bar.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- terms
 // Per-thread accumulators.  Each forms, for every pixel, exactly the terms
 // listed at the top of this file, and adds them exactly, but without any
@@ -74,12 +144,10 @@ __device__ __forceinline__ void allow_dependent_launch() {
 //
 // vec() takes 16 bytes of each plane, sample() one sample of each; flush()
 // folds the bounded 32-bit / fp32 runs into 64-bit sums and must be called at
-// least once per kFlushVecs vec() or sample() calls; totals() returns
+// least once per TermSums::kFlushVecs vec() or sample() calls; totals() returns
 // {noise, ref sum, dist sum, ref sum of squares, dist sum of squares, OR of
 // samples} in raw units.
 
-// vec() / sample() calls a thread may make between two flush() calls.
-constexpr uint32_t kFlushVecs = 2048;
 
 // An fp32 holding an integer of magnitude below 2^22, as an int, by an add:
 // x + 1.5 * 2^23 lies in [2^23, 2^24), where the ulp is 1, so that sum is
@@ -101,6 +169,7 @@ struct TermSums;
 // 2^31.
 template <>
 struct TermSums<8> {
+    static constexpr uint32_t kFlushVecs = 2048;
     u64 sr = 0, sd = 0, srr = 0, sdd = 0, srd = 0;
     uint32_t r_ = 0, d_ = 0, rr_ = 0, dd_ = 0, rd_ = 0;
 
@@ -152,6 +221,7 @@ struct TermSums<8> {
 template <int BPC>
 struct TermSums {
     static_assert(BPC == 10 || BPC == 12, "8 and 16 bits have their own forms");
+    static constexpr uint32_t kFlushVecs = 2048;
     u64 sr = 0, sd = 0, rr = 0, dd = 0, rd = 0;
     uint32_t r_ = 0, d_ = 0, orv = 0;
 
@@ -195,91 +265,145 @@ struct TermSums {
     }
 };
 
+// Two fp32 lanes in one 64-bit register, lane 0 in the low half.  Blackwell's
+// packed fp32 instructions (add/sub/fma .rn.f32x2) apply the scalar IEEE
+// operation with round to nearest even to each lane, so every lane's result
+// is the one the scalar instruction gives; they halve the issue slots.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_pack(uint32_t lo, uint32_t hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 v, uint32_t &lo, uint32_t &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// fl(a * a) per lane, as one fused multiply-add with a +0 addend: a single
+// round-to-nearest-even of the exact square (+0 adds nothing to a product
+// that is +0 or positive).  Not a plain mul.rn.f32x2: the back end was found
+// to fuse a packed multiply into the packed add or subtract that consumes it
+// (which would add the unrounded square) even with contraction disabled; an
+// fma result has nothing left to fuse, and the +0 addend keeps it from being
+// rewritten as a plain multiply.
+__device__ __forceinline__ f32x2 f2_square(f32x2 a) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(d) : "l"(a), "l"(0ull));
+    return d;
+}
+
+// Exact sum, per lane, of integer-valued fp32 terms in [0, 2^32), in fp32.
+// hi starts at 2^39 (bits 0x53000000); while it stays in [2^39, 2^40) its
+// ulp is 2^16, so h = hi + x is hi plus x rounded to a multiple of 2^16, and
+//   z = h - hi   (both multiples of 2^16 in one binade: exact)
+//   e = x - z    (an integer of magnitude at most 2^15: exact)
+// hold exactly; lo collects the e.  After at most kMaxTerms terms hi is below
+// 2^39 + 127 (2^32 + 2^15) < 2^40 - 2^15, so it never leaves the binade, and
+// |lo| <= 127 * 2^15 < 2^22.  drain() returns the lanes' exact total:
+// (bits(hi) - bits(2^39)) counts the units of 2^16 that hi gained.
+struct ExactSum2 {
+    static constexpr int kMaxTerms = 127;
+    static constexpr uint32_t kSeedBits = 0x53000000u;  // 2^39
+    f32x2 hi = ((f32x2)kSeedBits << 32) | kSeedBits;
+    f32x2 lo = 0;
+
+    __device__ __forceinline__ void add(f32x2 x) {
+        const f32x2 h = f2_add(hi, x);
+        const f32x2 z = f2_sub(h, hi);
+        lo = f2_add(lo, f2_sub(x, z));
+        hi = h;
+    }
+    __device__ __forceinline__ long long drain() {
+        uint32_t h0, h1, l0, l1;
+        f2_unpack(hi, h0, h1);
+        f2_unpack(lo, l0, l1);
+        const long long units = (long long)(h0 - kSeedBits) + (long long)(h1 - kSeedBits);
+        const long long rest = (long long)small_float_to_int(__uint_as_float(l0)) +
+                               (long long)small_float_to_int(__uint_as_float(l1));
+        hi = ((f32x2)kSeedBits << 32) | kSeedBits;
+        lo = 0;
+        return units * 65536 + rest;
+    }
+};
+
 // 16 bits.  Here the float square rounds (D^2 and s^2 reach 2^32), so the
-// terms are the fp32 products, computed as such, and their sum is split as
-//   sum fl(x*x) = sum x^2 - sum e,   e = x*x - fl(x*x),
-// with both parts exact:
+// terms are the fp32 products, computed as such, two pixels at a time:
 // - Floats without conversion: with K = 0x4B000000 (the bits of 2^23), the
 //   bits K | s are the float 2^23 + s exactly (s < 2^16), so
 //   (2^23 + r) - (2^23 + d) = r - d = D and (2^23 + s) - 2^23 = s are exact
-//   fp32 subtractions.  fl(D*D) and fl(s*s) are single round-to-nearest-even
-//   products (__fmul_rn), the CPU's terms.
-// - e = fma(x, x, -fl(x*x)) is exact: the fused operation rounds the exact
-//   x*x - fl(x*x), an integer of magnitude at most 128 (half an ulp below
-//   2^32), which fp32 holds.  Runs of at most 2048 vectors (16384 pixels)
-//   keep the fp32 sums of e below 2^21 in magnitude, hence exact.
-// - sum x^2: the bit patterns K + s are integers, so 32x32->64-bit
-//   multiply-adds give B_rr = sum (K + r)^2, B_dd and B_rd = sum (K + r)(K + d)
-//   modulo 2^64, and
-//     sum r^2 = B_rr - n K^2 - 2 K sum r,   sum r d = B_rd - n K^2 - K (sum r + sum d)
-//   hold modulo 2^64; the true values are below 2^57, so they are exact.
-//   sum D^2 = sum r^2 + sum d^2 - 2 sum r d.
-// The products fl(x*x) are formed with __fmul_rn and the residuals with an
-// explicit __fmaf_rn; nothing else is fused (the file is built with
-// --fmad=false).
+//   fp32 subtractions.
+// - fl(D*D), fl(r*r), fl(d*d): one round-to-nearest-even product each (the
+//   CPU's terms), integers below 2^32 (f2_square).
+// - The reference plane's square stream is added exactly by an ExactSum2
+//   (FMA pipe), drained into a 64-bit integer at least every kFlushVecs
+//   vectors (4 terms per lane each).  The noise and the distorted plane's
+//   square streams are converted (exactly: the values are integers below
+//   2^32) with F2I, which runs on the XU pipe, and added in 64-bit integers on
+//   the ALU pipe.  The FMA pipe is what limits this form, so its work is
+//   spread over three pipes (two conversions a pixel keep the XU pipe, a
+//   quarter as wide, below its own limit at full HBM bandwidth).
+// - Sums of samples: dp2a adds the two 16-bit halves of a word.
 template <>
 struct TermSums<16> {
     static constexpr uint32_t kBias = 0x4B000000u;
-    u64 brr = 0, bdd = 0, brd = 0, sr = 0, sd = 0;
-    long long en = 0, er = 0, ed = 0;
-    uint32_t r_ = 0, d_ = 0, n = 0;
-    float en_ = 0.f, er_ = 0.f, ed_ = 0.f;
+    static constexpr uint32_t kFlushVecs = 24;
+    static_assert(4 * kFlushVecs <= ExactSum2::kMaxTerms, "ExactSum2 run bound");
+    ExactSum2 rsq_;
+    u64 noise = 0, rss = 0, dss = 0, sr = 0, sd = 0;
+    uint32_t r_ = 0, d_ = 0;
 
-    __device__ __forceinline__ void pixel(uint32_t br, uint32_t bd) {
-        const float xr = __uint_as_float(br);
-        const float xd = __uint_as_float(bd);
-        const float diff = __fsub_rn(xr, xd);
-        const float t = __fmul_rn(diff, diff);
-        en_ = __fadd_rn(en_, __fmaf_rn(diff, diff, -t));
-        const float fr = __fsub_rn(xr, 8388608.0f);
-        const float fd = __fsub_rn(xd, 8388608.0f);
-        const float qr = __fmul_rn(fr, fr);
-        const float qd = __fmul_rn(fd, fd);
-        er_ = __fadd_rn(er_, __fmaf_rn(fr, fr, -qr));
-        ed_ = __fadd_rn(ed_, __fmaf_rn(fd, fd, -qd));
-        brr += (u64)br * br;
-        bdd += (u64)bd * bd;
-        brd += (u64)br * bd;
+    __device__ __forceinline__ void pair(f32x2 xr, f32x2 xd) {
+        const f32x2 two23 = ((f32x2)kBias << 32) | kBias;
+        uint32_t t0, t1;
+        f2_unpack(f2_square(f2_sub(xr, xd)), t0, t1);
+        noise += (u64)__float2uint_rn(__uint_as_float(t0)) + __float2uint_rn(__uint_as_float(t1));
+        const f32x2 fr = f2_sub(xr, two23);
+        rsq_.add(f2_square(fr));
+        uint32_t q0, q1;
+        f2_unpack(f2_square(f2_sub(xd, two23)), q0, q1);
+        dss += (u64)__float2uint_rn(__uint_as_float(q0)) + __float2uint_rn(__uint_as_float(q1));
     }
     __device__ __forceinline__ void word(uint32_t a, uint32_t b) {
         r_ = __dp2a_lo(a, 0x01010101u, r_);
         d_ = __dp2a_lo(b, 0x01010101u, d_);
-        pixel((a & 0xffffu) | kBias, (b & 0xffffu) | kBias);
-        pixel(__byte_perm(a, kBias, 0x7632), __byte_perm(b, kBias, 0x7632));
+        pair(f2_pack((a & 0xffffu) | kBias, __byte_perm(a, kBias, 0x7632)),
+             f2_pack((b & 0xffffu) | kBias, __byte_perm(b, kBias, 0x7632)));
     }
     __device__ __forceinline__ void vec(const uint4 &a, const uint4 &b) {
         word(a.x, b.x);
         word(a.y, b.y);
         word(a.z, b.z);
         word(a.w, b.w);
-        n += 8;
     }
+    // One pixel in lane 0; lane 1 holds the sample 0, whose terms are 0.
     __device__ __forceinline__ void sample(uint32_t r, uint32_t d) {
         r_ += r;
         d_ += d;
-        pixel(r | kBias, d | kBias);
-        n += 1;
+        pair(f2_pack(r | kBias, kBias), f2_pack(d | kBias, kBias));
     }
     __device__ __forceinline__ void flush() {
         sr += r_;
         sd += d_;
         r_ = d_ = 0;
-        en += small_float_to_int(en_);
-        er += small_float_to_int(er_);
-        ed += small_float_to_int(ed_);
-        en_ = er_ = ed_ = 0.f;
+        rss += (u64)rsq_.drain();
     }
     __device__ __forceinline__ void totals(u64 (&t)[6]) {
         flush();
-        const u64 K = kBias, K2 = K * K, N = n;
-        const u64 rr = brr - N * K2 - 2 * K * sr;
-        const u64 dd = bdd - N * K2 - 2 * K * sd;
-        const u64 rd = brd - N * K2 - K * (sr + sd);
-        t[0] = rr + dd - 2 * rd - (u64)en;
+        t[0] = noise;
         t[1] = sr;
         t[2] = sd;
-        t[3] = rr - (u64)er;
-        t[4] = dd - (u64)ed;
+        t[3] = rss;
+        t[4] = dss;
         t[5] = 0;
     }
 };
@@ -322,47 +446,6 @@ __device__ __forceinline__ void block_reduce_store(u64 (&t)[6], u64 *dst) {
 }
 
 // ---------------------------------------------------------------- stage 1
-// Dense layout: each frame of each plane is frame_vecs contiguous 16-byte
-// vectors (16-byte aligned, rows packed).  Unit u of the grid is frame
-// frame0 + u / segs, vectors [s * seg_vecs, min((s + 1) * seg_vecs,
-// frame_vecs)) with s = u % segs.
-template <int BPC>
-__global__ void __launch_bounds__(kThreads)
-    fused_dense(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
-                size_t frame_pitch, uint32_t frame_vecs, uint32_t seg_vecs, int segs, int frame0,
-                Partial *__restrict__ partials) {
-    allow_dependent_launch();
-    const int unit = blockIdx.x;
-    const int f = frame0 + unit / segs;
-    const int s = unit - (unit / segs) * segs;
-    const uint32_t v0 = (uint32_t)s * seg_vecs;
-    const uint32_t v1 = min(v0 + seg_vecs, frame_vecs);
-    const uint4 *R = reinterpret_cast<const uint4 *>(ref + (size_t)f * frame_pitch);
-    const uint4 *D = reinterpret_cast<const uint4 *>(dist + (size_t)f * frame_pitch);
-
-    TermSums<BPC> acc;
-    uint32_t v = v0 + threadIdx.x;
-    while (v < v1) {
-        // at most kFlushVecs vectors per thread before the next flush
-        const uint32_t stop = min(v1, v + kFlushVecs * kThreads);
-        for (; v + (kUnroll - 1) * kThreads < stop; v += kUnroll * kThreads) {
-            uint4 a[kUnroll], b[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; u++) {
-                a[u] = ld_stream16(R + v + u * kThreads);
-                b[u] = ld_stream16(D + v + u * kThreads);
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; u++) acc.vec(a[u], b[u]);
-        }
-        for (; v < stop; v += kThreads) acc.vec(ld_stream16(R + v), ld_stream16(D + v));
-        acc.flush();
-    }
-    u64 t[6];
-    acc.totals(t);
-    block_reduce_store<kThreads>(t, partials[(size_t)f * segs + s].v);
-}
-
 // Any layout: unit u is frame frame0 + u / segs, rows [s * seg_rows,
 // min((s + 1) * seg_rows, height)).  A warp walks one row at a time.  With
 // VEC, rows start 16-byte aligned and are read as 16-byte vectors plus a
@@ -391,7 +474,7 @@ __global__ void __launch_bounds__(kThreads)
         if constexpr (VEC) {
             const int nvec = (width * kBps) >> 4;
             for (int c = lane; c < nvec;) {
-                const int stop = min(nvec, c + (int)kFlushVecs * 32);
+                const int stop = min(nvec, c + (int)TermSums<BPC>::kFlushVecs * 32);
                 for (; c < stop; c += 32)
                     acc.vec(ld_stream16(rr + 16 * (size_t)c), ld_stream16(dr + 16 * (size_t)c));
                 acc.flush();
@@ -399,7 +482,7 @@ __global__ void __launch_bounds__(kThreads)
             x0 = nvec * (16 / kBps);
         }
         for (int x = x0 + lane; x < width;) {
-            const int stop = min(width, x + (int)kFlushVecs * 32);
+            const int stop = min(width, x + (int)TermSums<BPC>::kFlushVecs * 32);
             for (; x < stop; x += 32) acc.sample(ld_sample<BPC>(rr, x), ld_sample<BPC>(dr, x));
             acc.flush();
         }
@@ -407,6 +490,170 @@ __global__ void __launch_bounds__(kThreads)
     u64 t[6];
     acc.totals(t);
     block_reduce_store<kThreads>(t, partials[(size_t)f * segs + s].v);
+}
+
+// Named barrier 1 over the consumer warps only (barrier 0 is __syncthreads).
+template <int NCW>
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
+}
+
+// The consumer warps' totals reduced to one record: warp shuffles, one
+// value per warp through shared memory, warp 0.  Only consumer threads take
+// part (named barrier 1), so the producer lane keeps streaming meanwhile.
+template <int NCW>
+__device__ __forceinline__ void consumer_reduce_store(u64 (&t)[6], u64 (*scratch)[6], u64 *dst) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < 5; k++) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
+        t[5] |= __shfl_xor_sync(0xffffffffu, t[5], o);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < 6; k++) scratch[warp][k] = t[k];
+    }
+    consumer_sync<NCW>();
+    if (warp == 0) {
+        u64 y[6];
+#pragma unroll
+        for (int k = 0; k < 6; k++) y[k] = lane < NCW ? scratch[lane][k] : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int k = 0; k < 5; k++) y[k] += __shfl_xor_sync(0xffffffffu, y[k], o);
+            y[5] |= __shfl_xor_sync(0xffffffffu, y[5], o);
+        }
+        u64 mine = 0;
+#pragma unroll
+        for (int k = 0; k < 6; k++)
+            if (lane == k) mine = y[k];
+        if (lane < 6) dst[lane] = mine;
+    }
+    consumer_sync<NCW>();  // scratch is reused by the next unit
+}
+
+// Dense layout (each frame of each plane frame_vecs contiguous, 16-byte
+// aligned 16-byte vectors) through a persistent TMA pipeline.  Unit u is
+// frame frame0 + u / segs, vectors [s * seg_vecs, min((s + 1) * seg_vecs,
+// frame_vecs)) with s = u % segs; CTA b takes units b, b + gridDim.x, ... in
+// order.  One producer lane (warp
+// NCW) streams them, stage by stage (SV vectors of each plane), into a ring
+// of STAGES shared-memory buffers with bulk copies; NCW consumer warps wait
+// for a stage's "full" mbarrier, fold it through TermSums from shared memory
+// and release it on its "empty" mbarrier (one arrive per warp) for the
+// producer to refill.  Loads stay in flight while the consumers compute,
+// without holding registers, and the ring does not drain between units: at
+// the end of a unit only the consumers meet, to reduce and write its record.
+//
+// Ring phases: the CTA's k-th stage (counted across its units) goes to buffer
+// k % STAGES; its full barrier completes phase k / STAGES, and the producer
+// refills the buffer for stage k only after the empty barrier completed
+// phase k / STAGES - 1 (stage k - STAGES released).  A wait that times out
+// sets kErrTimeout in the waiting thread; from then on that warp waits for
+// nothing, still writes (flagged) records for its remaining units, and the
+// producer waits (bounded) for the copies it issued before the CTA exits.
+template <int BPC, int NCW, int SV, int STAGES>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+    fused_dense_tma(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
+                    size_t frame_pitch, uint32_t frame_vecs, uint32_t seg_vecs, int segs,
+                    int frame0, int units, Partial *__restrict__ partials) {
+    constexpr uint32_t kStageBytes = SV * 16;  // per plane
+    constexpr uint32_t kPerThread = SV / (NCW * 32);
+    static_assert(SV % (NCW * 32) == 0, "a full stage gives every consumer thread equal work");
+    static_assert(kPerThread <= TermSums<BPC>::kFlushVecs, "flush at least once per stage");
+    constexpr uint32_t kStagesPerFlush = TermSums<BPC>::kFlushVecs / kPerThread;
+    extern __shared__ __align__(128) unsigned char ring[];  // [STAGES][2][kStageBytes]
+    __shared__ __align__(8) u64 full[STAGES], empty[STAGES];
+    __shared__ u64 red[NCW][6];
+
+    allow_dependent_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring0 = smem_u32(ring);
+    const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, NCW);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        if (lane != 0) return;
+        bool ok = true;
+        uint32_t k = 0;
+        for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int f = frame0 + u / segs;
+            const uint32_t v0 = min((uint32_t)(u % segs) * seg_vecs, frame_vecs);
+            const uint32_t nvec = min(v0 + seg_vecs, frame_vecs) - v0;
+            const unsigned char *R = ref + (size_t)f * frame_pitch + (size_t)v0 * 16;
+            const unsigned char *D = dist + (size_t)f * frame_pitch + (size_t)v0 * 16;
+            for (uint32_t j = 0; j * SV < nvec; j++, k++) {
+                const uint32_t st = k % STAGES;
+                if (k >= STAGES && !mbar_wait(empty0 + 8 * st, ((k / STAGES) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t bytes = min((uint32_t)SV, nvec - j * SV) * 16;
+                mbar_arrive_expect_tx(full0 + 8 * st, 2 * bytes);
+                bulk_g2s(ring0 + (2 * st) * kStageBytes, R + (size_t)j * kStageBytes, bytes,
+                         full0 + 8 * st);
+                bulk_g2s(ring0 + (2 * st + 1) * kStageBytes, D + (size_t)j * kStageBytes, bytes,
+                         full0 + 8 * st);
+            }
+        }
+        // The last copies must have landed before the CTA (and its shared
+        // memory) goes away; stages k - STAGES .. k - 1 were issued last.
+        for (uint32_t q = k > STAGES ? k - STAGES : 0; q < k; q++)
+            mbar_wait(full0 + 8 * (q % STAGES), (q / STAGES) & 1);
+        return;
+    }
+
+    u64 err = 0;
+    uint32_t k = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int f = frame0 + u / segs;
+        const int sg = u % segs;
+        const uint32_t v0 = min((uint32_t)sg * seg_vecs, frame_vecs);
+        const uint32_t nvec = min(v0 + seg_vecs, frame_vecs) - v0;
+        TermSums<BPC> acc;
+        uint32_t since_flush = 0;
+        for (uint32_t j = 0; j * SV < nvec; j++, k++) {
+            if (err) continue;  // a wait of this warp timed out: skip, write flagged records
+            const uint32_t st = k % STAGES;
+            // every lane's wait is bounded; the warp then decides together,
+            // so that no lane leaves while others reach __syncwarp
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * st, (k / STAGES) & 1))) {
+                err = kErrTimeout;
+                continue;
+            }
+            const uint4 *a = reinterpret_cast<const uint4 *>(ring + (2 * st) * kStageBytes);
+            const uint4 *b = reinterpret_cast<const uint4 *>(ring + (2 * st + 1) * kStageBytes);
+            const uint32_t cnt = min((uint32_t)SV, nvec - j * SV);
+            if (cnt == SV) {
+#pragma unroll
+                for (uint32_t q = 0; q < kPerThread; q++) {
+                    const uint32_t i = threadIdx.x + q * NCW * 32;
+                    acc.vec(a[i], b[i]);
+                }
+            } else {
+                for (uint32_t i = threadIdx.x; i < cnt; i += NCW * 32) acc.vec(a[i], b[i]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            if (++since_flush == kStagesPerFlush) {
+                acc.flush();
+                since_flush = 0;
+            }
+        }
+        u64 t[6];
+        acc.totals(t);
+        t[5] |= err;
+        consumer_reduce_store<NCW>(t, red, partials[(size_t)f * segs + sg].v);
+    }
 }
 
 // ---------------------------------------------------------------- stage 2

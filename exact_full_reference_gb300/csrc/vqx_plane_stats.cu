@@ -40,22 +40,52 @@ enum Path { kDense = 0, kRowsVec = 1, kRowsScalar = 2, kPaths = 3 };
 
 int bpc_index(int bpc) { return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3; }
 
+// Kernel, CTA size and dynamic shared memory of each stage-1 variant.
+struct Stage1Shape {
+    const void *fn;
+    int threads;
+    size_t smem;
+};
+
 template <int BPC>
-const void *stage1_kernel(int path) {
+Stage1Shape stage1_shape(int path) {
     switch (path) {
-    case kDense: return (const void *)vqx::fused_dense<BPC>;
-    case kRowsVec: return (const void *)vqx::fused_rows<BPC, true>;
-    default: return (const void *)vqx::fused_rows<BPC, false>;
+    case kDense:
+        return {(const void *)vqx::fused_dense_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs,
+                                                   vqx::kTmaStages>,
+                vqx::kTmaThreads, vqx::kTmaSmem};
+    case kRowsVec: return {(const void *)vqx::fused_rows<BPC, true>, vqx::kThreads, 0};
+    default: return {(const void *)vqx::fused_rows<BPC, false>, vqx::kThreads, 0};
     }
 }
 
-const void *stage1_kernel(int path, int bpc) {
+Stage1Shape stage1_shape(int path, int bpc) {
     switch (bpc) {
-    case 8: return stage1_kernel<8>(path);
-    case 10: return stage1_kernel<10>(path);
-    case 12: return stage1_kernel<12>(path);
-    default: return stage1_kernel<16>(path);
+    case 8: return stage1_shape<8>(path);
+    case 10: return stage1_shape<10>(path);
+    case 12: return stage1_shape<12>(path);
+    default: return stage1_shape<16>(path);
     }
+}
+
+// Per device: allow the dense kernels their shared-memory ring and count
+// the CTAs of each variant that fit on one SM.
+cudaError_t prepare_stage1(int (&resident)[kPaths][4]) {
+    const int bpcs[4] = {8, 10, 12, 16};
+    for (int p = 0; p < kPaths; p++)
+        for (int b = 0; b < 4; b++) {
+            const Stage1Shape sh = stage1_shape(p, bpcs[b]);
+            cudaError_t e = cudaSuccess;
+            if (sh.smem > 48 * 1024)
+                e = cudaFuncSetAttribute(sh.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sh.smem);
+            if (e != cudaSuccess) return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sh.fn, sh.threads, sh.smem);
+            if (e != cudaSuccess) return e;
+            resident[p][b] = n > 0 ? n : 1;
+        }
+    return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ device state
@@ -78,15 +108,7 @@ DeviceCtx g_dev[kMaxDevices];
 cudaError_t init_device(DeviceCtx &c, int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int bpcs[4] = {8, 10, 12, 16};
-    for (int p = 0; p < kPaths; p++)
-        for (int b = 0; b < 4; b++) {
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stage1_kernel(p, bpcs[b]),
-                                                              vqx::kThreads, 0);
-            if (e != cudaSuccess) return e;
-            c.resident[p][b] = n > 0 ? n : 1;
-        }
+    if ((e = prepare_stage1(c.resident)) != cudaSuccess) return e;
     cudaMemPoolProps props;
     memset(&props, 0, sizeof props);
     props.allocType = cudaMemAllocationTypePinned;
@@ -198,6 +220,7 @@ struct Plan {
     int path = kDense;
     int bpc = 8;
     int segs = 1;
+    long long resident = 1;  // CTAs of this variant resident on the whole GPU
     uint32_t work = 0;      // 16-byte vectors (dense) or rows per frame
     uint32_t seg_work = 0;  // per segment
     size_t frame_pitch = 0;
@@ -249,9 +272,10 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
         p.path = (aligned && (stride & 15u) == 0) ? kRowsVec : kRowsScalar;
         p.work = (uint32_t)height;
     }
-    const long long resident = (long long)c.sms * c.resident[p.path][bpc_index(bpc)];
-    const uint32_t min_unit = p.path == kDense ? (uint32_t)vqx::kThreads : 8u;
-    p.segs = choose_segs(frames_per_launch, p.work, min_unit, resident);
+    p.resident = (long long)c.sms * c.resident[p.path][bpc_index(bpc)];
+    // a dense unit is at least one pipeline stage, a row unit one row per warp
+    const uint32_t min_unit = p.path == kDense ? (uint32_t)vqx::kTmaStageVecs : 8u;
+    p.segs = choose_segs(frames_per_launch, p.work, min_unit, p.resident);
     p.seg_work = (p.work + (uint32_t)p.segs - 1) / (uint32_t)p.segs;
     return p;
 }
@@ -261,12 +285,19 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
                               int frame0, int frames, Partial *partials, cudaStream_t st) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)((long long)frames * p.segs));
+    const long long units = (long long)frames * p.segs;
+    cfg.gridDim = dim3((unsigned)units);
     cfg.blockDim = dim3(vqx::kThreads);
     cfg.stream = st;
-    if (p.path == kDense)
-        return cudaLaunchKernelEx(&cfg, vqx::fused_dense<BPC>, ref, dist, p.frame_pitch,
-                                  p.work, p.seg_work, p.segs, frame0, partials);
+    if (p.path == kDense) {
+        // persistent: at most the resident CTAs, each walking several units
+        cfg.gridDim = dim3((unsigned)(units < p.resident ? units : p.resident));
+        cfg.blockDim = dim3(vqx::kTmaThreads);
+        cfg.dynamicSmemBytes = vqx::kTmaSmem;
+        return cudaLaunchKernelEx(
+            &cfg, vqx::fused_dense_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages>,
+            ref, dist, p.frame_pitch, p.work, p.seg_work, p.segs, frame0, (int)units, partials);
+    }
     if (p.path == kRowsVec)
         return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, true>, ref, dist, p.frame_pitch,
                                   p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
@@ -313,7 +344,8 @@ void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats 
     o->dist_sum = s.v[2];
     o->ref_sumsq = s.v[3];
     o->dist_sumsq = s.v[4];
-    o->flags = (s.v[5] >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
+    o->flags = ((s.v[5] & 0xffffffffull) >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
+    if (s.v[5] & vqx::kErrTimeout) o->flags |= VQX_FLAG_TIMEOUT;
     o->reserved = 0;
     o->noise = (double)s.v[0] / S2;
     o->mse = o->noise / n;
@@ -326,12 +358,20 @@ void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats 
     o->dist_meansq = ((double)s.v[4] / S2) / n;
 }
 
+// The call's status from the frames' flags: a timed-out device wait first
+// (its sums are incomplete), then an out-of-range sample.
+int merge_status(int rc, const vqx_frame_stats &f) {
+    if (f.flags & VQX_FLAG_TIMEOUT) return VQX_ETIMEOUT;
+    if ((f.flags & VQX_FLAG_RANGE) && rc == VQX_OK) return VQX_ERANGE;
+    return rc;
+}
+
 int conclude_all(const Partial *sums, int n_frames, int bpc, int width, int height,
                  vqx_frame_stats *out) {
     int rc = VQX_OK;
     for (int f = 0; f < n_frames; f++) {
         conclude(sums[f], bpc, width, height, &out[f]);
-        if (out[f].flags & VQX_FLAG_RANGE) rc = VQX_ERANGE;
+        rc = merge_status(rc, out[f]);
     }
     return rc;
 }
@@ -360,6 +400,7 @@ const char *vqx_status_string(int status) {
     case VQX_ERANGE: return "a sample is out of range for the bit depth";
     case VQX_ECUDA: return "CUDA runtime error";
     case VQX_ENOMEM: return "out of memory";
+    case VQX_ETIMEOUT: return "a device-side wait timed out (results incomplete)";
     default: return "unknown status";
     }
 }
@@ -543,16 +584,7 @@ cudaError_t init_noalloc(NoAllocCtx &c, int dev) {
     if (c.scratch == nullptr) return cudaErrorInvalidSymbol;
     e = cudaDeviceGetAttribute(&c.planning.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int bpcs[4] = {8, 10, 12, 16};
-    for (int p = 0; p < kPaths; p++)
-        for (int b = 0; b < 4; b++) {
-            int n = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stage1_kernel(p, bpcs[b]),
-                                                              vqx::kThreads, 0);
-            if (e != cudaSuccess) return e;
-            c.planning.resident[p][b] = n > 0 ? n : 1;
-        }
-    return cudaSuccess;
+    return prepare_stage1(c.planning.resident);
 }
 
 }  // namespace
@@ -599,7 +631,7 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
         Partial s_f;
         memcpy(&s_f, (const unsigned char *)out + (size_t)f * sizeof(Partial), sizeof s_f);
         conclude(s_f, bpc, width, height, &out[f]);
-        if (out[f].flags & VQX_FLAG_RANGE) rc = VQX_ERANGE;
+        rc = merge_status(rc, out[f]);
     }
     return rc;
 }

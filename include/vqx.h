@@ -56,6 +56,11 @@ typedef struct CUstream_st *vqx_stream_t;
 #define VQX_ECUDA (-4)   /* a CUDA runtime call failed; see
                             vqx_last_cuda_error() */
 #define VQX_ENOMEM (-5)  /* device or pinned host memory could not be had */
+#define VQX_ETIMEOUT (-6) /* a wait inside a kernel gave up after about a
+                             second (a copy that never completed); the
+                             frames concerned carry VQX_FLAG_TIMEOUT and their
+                             sums are incomplete.  The CUDA context stays
+                             usable. */
 
 /* Largest frame accepted, in pixels (w * h).  Up to 12 bits the exact noise
  * sum then needs at most 49 bits (ADR-1440, Context: "at most 49 bits at
@@ -63,7 +68,8 @@ typedef struct CUstream_st *vqx_stream_t;
 #define VQX_MAX_FRAME_PIXELS (1u << 25)
 
 /* vqx_frame_stats.flags */
-#define VQX_FLAG_RANGE 1u /* the frame holds a sample >= 2^bpc */
+#define VQX_FLAG_RANGE 1u   /* the frame holds a sample >= 2^bpc */
+#define VQX_FLAG_TIMEOUT 2u /* a device-side wait for this frame timed out */
 
 /* Results for one frame pair.  The integer fields are the exact sums on the
  * device ("debug" accumulators); the doubles are concluded from them. */
