@@ -59,6 +59,24 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(value, pg=None, device=None):
+    """The maximum of ``value`` over all ranks (the slowest rank's time), or
+    ``value`` itself without a process group."""
+    if pg is None:
+        return value
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, frames_per_rank, steps, seconds):
+    """Whole-job frame pairs per second: every rank's frames over the slowest
+    rank's time (weak scaling: each rank reduces its own batch)."""
+    return world * frames_per_rank * steps / seconds
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -329,12 +347,8 @@ def run_ours(args, wlo):
     vqx.profile_enable(False)
     time.sleep(0.2)
     clocks.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if pg is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    value = world * n * args.steps / (elapsed_ms / 1e3)
+    elapsed_ms = reduce_max(ev0.elapsed_time(ev1), pg, dev)
+    value = job_throughput(world, n, args.steps, elapsed_ms / 1e3)
 
     # roofline of the fused kernel, from the events recorded inside the calls
     peak, peak_kind = measured_peak()
@@ -369,12 +383,8 @@ def run_ours(args, wlo):
         for _ in range(k):
             so.vqx_plane_stats_host(*e2e_args)
         torch.cuda.synchronize()
-        el = time.perf_counter() - t0
-        if pg is not None:
-            t = torch.tensor([el], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            el = float(t.item())
-        e2e = {"value": world * n * k / el, "unit": UNIT, "steps": k,
+        el = reduce_max(time.perf_counter() - t0, pg, dev)
+        e2e = {"value": job_throughput(world, n, k, el), "unit": UNIT, "steps": k,
                "h2d_bytes_per_step": int(rbytes.nbytes + dbytes.nbytes),
                "d2h_bytes_per_step": int(n * ctypes.sizeof(ctypes.c_uint64) * 6),
                "api": "vqx_plane_stats_host (pinned host planes)"}

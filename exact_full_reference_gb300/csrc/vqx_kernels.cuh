@@ -302,37 +302,44 @@ __device__ __forceinline__ f32x2 f2_square(f32x2 a) {
     return d;
 }
 
-// Exact sum, per lane, of integer-valued fp32 terms in [0, 2^32), in fp32.
-// hi starts at 2^39 (bits 0x53000000); while it stays in [2^39, 2^40) its
-// ulp is 2^16, so h = hi + x is hi plus x rounded to a multiple of 2^16, and
-//   z = h - hi   (both multiples of 2^16 in one binade: exact)
-//   e = x - z    (an integer of magnitude at most 2^15: exact)
-// hold exactly; lo collects the e.  After at most kMaxTerms terms hi is below
-// 2^39 + 127 (2^32 + 2^15) < 2^40 - 2^15, so it never leaves the binade, and
-// |lo| <= 127 * 2^15 < 2^22.  drain() returns the lanes' exact total:
-// (bits(hi) - bits(2^39)) counts the units of 2^16 that hi gained.
-struct ExactSum2 {
-    static constexpr int kMaxTerms = 127;
-    static constexpr uint32_t kSeedBits = 0x53000000u;  // 2^39
-    f32x2 hi = ((f32x2)kSeedBits << 32) | kSeedBits;
-    f32x2 lo = 0;
+// Exact integer sum of pairs of integer-valued fp32 terms in [0, 2^32),
+// without a conversion instruction and without accumulating in floating
+// point.  Each term x is split by two exact fp32 additions into
+//   h = x rounded to a multiple of 2^16      (x + 1.5*2^39 lies in
+//       [2^39, 2^40), where the ulp is 2^16, so that sum is x rounded to a
+//       multiple of 2^16, plus 1.5*2^39, and its bits are
+//       bits(1.5*2^39) + h / 2^16)
+//   l = x - h, an integer of magnitude at most 2^15 (exact)
+//                                        (l + 1.5*2^23 lies in [2^23, 2^24),
+//       where the ulp is 1: its bits are bits(1.5*2^23) + l)
+// and the two bit patterns of both lanes are added as 32-bit integers.  Over
+// n terms the sums are n*bits(1.5*2^39) + sum(h)/2^16 and
+// n*bits(1.5*2^23) + sum(l), taken modulo 2^32; with at most kMaxTerms
+// terms between drains, sum(h)/2^16 < 2^32 and |sum(l)| < 2^31, so the
+// true values come back exactly, and sum(x) = 2^16 * sum(h)/2^16 + sum(l).
+struct SplitSum2 {
+    static constexpr uint32_t kMaxTerms = 32768;  // terms (both lanes) per drain
+    static constexpr uint32_t kHiBits = 0x53400000u;  // 1.5 * 2^39
+    static constexpr uint32_t kLoBits = 0x4B400000u;  // 1.5 * 2^23
+    uint32_t hi = 0, lo = 0, n = 0;
 
     __device__ __forceinline__ void add(f32x2 x) {
-        const f32x2 h = f2_add(hi, x);
-        const f32x2 z = f2_sub(h, hi);
-        lo = f2_add(lo, f2_sub(x, z));
-        hi = h;
-    }
-    __device__ __forceinline__ long long drain() {
+        const f32x2 c_hi = ((f32x2)kHiBits << 32) | kHiBits;
+        const f32x2 c_lo = ((f32x2)kLoBits << 32) | kLoBits;
+        const f32x2 hb = f2_add(x, c_hi);                      // bits: kHiBits + h/2^16
+        const f32x2 lb = f2_add(f2_sub(x, f2_sub(hb, c_hi)), c_lo);  // bits: kLoBits + l
         uint32_t h0, h1, l0, l1;
-        f2_unpack(hi, h0, h1);
-        f2_unpack(lo, l0, l1);
-        const long long units = (long long)(h0 - kSeedBits) + (long long)(h1 - kSeedBits);
-        const long long rest = (long long)small_float_to_int(__uint_as_float(l0)) +
-                               (long long)small_float_to_int(__uint_as_float(l1));
-        hi = ((f32x2)kSeedBits << 32) | kSeedBits;
-        lo = 0;
-        return units * 65536 + rest;
+        f2_unpack(hb, h0, h1);
+        f2_unpack(lb, l0, l1);
+        hi += h0 + h1;
+        lo += l0 + l1;
+        n += 2;
+    }
+    __device__ __forceinline__ u64 drain() {
+        const u64 units = (u64)(uint32_t)(hi - n * kHiBits);
+        const long long rest = (long long)(int32_t)(lo - n * kLoBits);
+        hi = lo = n = 0;
+        return units * 65536 + (u64)rest;
     }
 };
 
@@ -344,21 +351,22 @@ struct ExactSum2 {
 //   fp32 subtractions.
 // - fl(D*D), fl(r*r), fl(d*d): one round-to-nearest-even product each (the
 //   CPU's terms), integers below 2^32 (f2_square).
-// - The reference plane's square stream is added exactly by an ExactSum2
-//   (FMA pipe), drained into a 64-bit integer at least every kFlushVecs
-//   vectors (4 terms per lane each).  The noise and the distorted plane's
-//   square streams are converted (exactly: the values are integers below
-//   2^32) with F2I, which runs on the XU pipe, and added in 64-bit integers on
-//   the ALU pipe.  The FMA pipe is what limits this form, so its work is
-//   spread over three pipes (two conversions a pixel keep the XU pipe, a
-//   quarter as wide, below its own limit at full HBM bandwidth).
+// - The reference plane's square stream is split into exact 16-bit parts by
+//   a SplitSum2 (fp32 additions) and added as integers, drained into a 64-bit
+//   integer at least every kFlushVecs vectors (8 terms each).  The noise and
+//   the distorted plane's square streams are converted (exactly: the values
+//   are integers below 2^32) with F2I, which runs on the XU pipe, and added in
+//   64-bit integers on the ALU pipe.  No stream is accumulated in floating
+//   point.  The work is spread over the FMA, ALU and XU pipes so that none of
+//   them limits the pass (two conversions a pixel keep the XU pipe, a quarter
+//   as wide, below its own limit at full HBM bandwidth).
 // - Sums of samples: dp2a adds the two 16-bit halves of a word.
 template <>
 struct TermSums<16> {
     static constexpr uint32_t kBias = 0x4B000000u;
-    static constexpr uint32_t kFlushVecs = 24;
-    static_assert(4 * kFlushVecs <= ExactSum2::kMaxTerms, "ExactSum2 run bound");
-    ExactSum2 rsq_;
+    static constexpr uint32_t kFlushVecs = 2048;
+    static_assert(8 * kFlushVecs <= SplitSum2::kMaxTerms, "SplitSum2 run bound");
+    SplitSum2 rsq_;
     u64 noise = 0, rss = 0, dss = 0, sr = 0, sd = 0;
     uint32_t r_ = 0, d_ = 0;
 
@@ -395,7 +403,7 @@ struct TermSums<16> {
         sr += r_;
         sd += d_;
         r_ = d_ = 0;
-        rss += (u64)rsq_.drain();
+        rss += rsq_.drain();
     }
     __device__ __forceinline__ void totals(u64 (&t)[6]) {
         flush();
