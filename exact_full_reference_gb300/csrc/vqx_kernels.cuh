@@ -214,7 +214,7 @@ struct TermSums<8> {
 
 // 10 and 12 bits.  A valid sample is below 2^12, so |D| and s are below
 // 2^12, their squares below 2^24, and the float squares are the integer
-// squares ("ADR-1440 ...", Decision: up to 12 bits the square is exact).
+// squares ("ADR-1440 ...", Decision: below 13 bits no float square rounds).
 // Squares and products are added with 32x32->64-bit multiply-adds; the sums
 // of samples with dp2a (two 16-bit halves at once).  The OR of all samples
 // flags values of 2^bpc or more, for which the library reports VQX_ERANGE.

@@ -20,10 +20,11 @@
  * units of 1/S^2 (1/S for the plain samples), so the library adds the terms
  * as integers, exactly and in any order, on the device, and converts the
  * integer sums to the scores on the host in double.  The scores are
- * therefore bit-identical to the CPU's wherever the CPU's double sum is
- * exact (every frame at 8, 10 and 12 bits, and 16-bit frames of up to 2^21
- * pixels), and past that point they are the exact sum rounded once, within
- * the bound ADR-1447 (Decision) states.
+ * therefore bit-identical to the CPU's wherever the CPU's double sum stays
+ * under 2^53 units, where a double holds it exactly (always up to 12 bits,
+ * and at 16 bits for frames of at most 2^21 pixels); beyond that they are
+ * the exact sum rounded once, within the bound derived in ADR-1447
+ * (Decision).
  *
  * Sample layout (all entry points): bpc 8 = one byte per sample; bpc 10, 12
  * and 16 = one little-endian uint16 per sample (the low bpc bits; a sample
@@ -62,9 +63,10 @@ typedef struct CUstream_st *vqx_stream_t;
                              sums are incomplete.  The CUDA context stays
                              usable. */
 
-/* Largest frame accepted, in pixels (w * h).  Up to 12 bits the exact noise
- * sum then needs at most 49 bits (ADR-1440, Context: "at most 49 bits at
- * any frame size the library accepts"; 2^24 * 2^25 = 2^49). */
+/* Largest frame accepted, in pixels (w * h).  With terms below 2^24 (bit
+ * depths up to 12) a frame of this size keeps the exact noise sum within
+ * 49 bits, 2^24 * 2^25, the width ADR-1440 (Context) gives for the CPU's
+ * exact sums. */
 #define VQX_MAX_FRAME_PIXELS (1u << 25)
 
 /* vqx_frame_stats.flags */

@@ -116,13 +116,14 @@ def load():
 
 
 def moment_bound(pixels, e):
-    """Largest distance between the CPU's double running sum and the exact sum
-    rounded once, as a moment, once the sum passes 2^53 units ("ADR-1447 ...",
-    section Decision): at least 2^21 adds are exact (a term is below 2^32
-    units), every later add rounds by at most half an ulp of a sum in binade
-    ``e`` (2^(e-53) units), the exact sum rounded once is within the same, a
-    unit is 2^-16 of a moment divided by the pixel count, and the two final
-    divisions add at most 2^-37."""
+    """Bound, as a moment, on the gap between the CPU's sequential double sum
+    and the exact sum rounded once, for sums of at least 2^53 units, after
+    "ADR-1447 ..." (Decision).  Terms stay below 2^32 units, so the first 2^21
+    additions cannot leave the exact range; each of the remaining
+    pixels - 2^21 + 1 additions can round by half an ulp of a sum with
+    2^e <= sum < 2^(e+1), i.e. 2^(e-53) units, as can the single rounding of
+    the exact sum; one unit is 2^-16 / pixels in moment terms (2^(e-69) per
+    addition), and the final two divisions contribute at most 2^-37."""
     later = max(pixels - 2 ** 21 + 1, 0)
     return later / pixels * 2.0 ** (e - 69) + 2.0 ** -37
 

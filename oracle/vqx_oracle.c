@@ -10,16 +10,18 @@
  *
  * What is followed (vmafx ADR pages):
  *  - "ADR-1440: float_psnr_hip adds its squared differences as integers and
- *    returns the CPU's score bit for bit", section Context: float_psnr.c
- *    divides each sample by scaler = 2^(bpc - 8), squares each difference in
- *    float and adds the squares in double, row by row.  The Consequences
- *    section gives the PSNR a cap (the option uncapped=true exists) and puts
- *    an MSE of 16570 at a PSNR below 6 dB, which fixes the peak at 255.
+ *    returns the CPU's score bit for bit", section Context: the CPU extractor
+ *    scales both planes to the 8-bit range (a sample over 2^(bpc - 8)) in
+ *    float, takes the per-pixel difference and its square in float, and
+ *    keeps a double running total over the frame, one row after another.
+ *    Its Consequences section shows that the score is capped (there is an
+ *    option to lift the cap) and places MSE 16570 under 6 dB, which only
+ *    holds with a peak of 255.
  *  - "ADR-1447: float_moment_hip adds the float squares the CPU adds, and is
- *    bit-identical while the CPU's own sum is exact", section Context:
- *    picture_copy() divides each sample by 1, 4, 16 or 256; moment.c adds the
- *    samples, and their float squares (term = pic * pic), into one double per
- *    output and divides by the pixel count.
+ *    bit-identical while the CPU's own sum is exact", section Context: the
+ *    same scaling (scalers 1, 4, 16, 256 for 8, 10, 12, 16 bits), then one
+ *    double total of the scaled samples and one of their float squares per
+ *    plane, each divided by the number of pixels at the end.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - "row by row" is one double accumulator walked in raster order;

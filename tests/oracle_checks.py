@@ -177,8 +177,9 @@ def check_swap_symmetry(orc):
 
 
 def check_units_integer_identity_le12(orc):
-    """Up to 12 bits every square is below 2^24, so the float square is the
-    integer square (ADR-1440 Decision, ADR-1447 Context)."""
+    """Below 13 bits every square is smaller than 2^24, so fp32 holds it and
+    the float square equals the integer one (ADR-1440 Decision, ADR-1447
+    Context)."""
     for bpc in (8, 10, 12):
         for seed in range(3):
             ref, dist = small_random(bpc, 300 + 10 * bpc + seed)
@@ -192,9 +193,10 @@ def check_units_integer_identity_le12(orc):
 
 
 def check_units_rne24_16bit(orc):
-    """At 16 bits the float square is the integer square rounded to 24
-    significant bits, ties to even (ADR-1447 Decision); checked against the
-    pure-integer rounding on full-range, bright and small-difference frames."""
+    """With 16-bit samples a square can need up to 32 bits, and fp32 keeps the
+    24 leading ones, rounding to nearest with ties to even (ADR-1447
+    Decision); checked against the pure-integer rounding on full-range,
+    bright and small-difference frames."""
     cases = [
         small_random(16, 400),
         small_random(16, 401, lo=56000, hi=64000),
@@ -211,9 +213,9 @@ def check_units_rne24_16bit(orc):
 
 
 def check_scores_equal_exact_sums(orc):
-    """While the sums are below 2^53 units the CPU's double sums are exact
-    (ADR-1440 Consequences, ADR-1447 Decision): every score equals the
-    correctly rounded quotient of the independent exact integer sums."""
+    """Below 2^53 units a double holds every partial sum exactly (ADR-1440
+    Consequences, ADR-1447 Decision), so every score must equal the correctly
+    rounded quotient of the independent exact integer sums."""
     cases = [(bpc, None) + small_random(bpc, 500 + bpc) for bpc in (8, 10, 12, 16)]
     cases += [(16, None) + small_random(16, 520, lo=56000, hi=64000)]
     b4 = cached("bright1080p0", lambda: wl.WORKLOADS["1920x1080_16bit_x64"].generate([0]))
@@ -254,9 +256,10 @@ def check_stride_and_batch_layout(orc):
 
 
 def check_past_2_53_page_measurements(orc):
-    """ADR-1447 Consequences: past 2^53 units the CPU's rounded sum differs
-    from the exact one by about 1.2e-7 on full-range 3840x2160 noise and by 0
-    when every sample is above 60000; both within the stated bound."""
+    """ADR-1447 Consequences reports, beyond 2^53 units, a gap of about 1.2e-7
+    between the CPU's rounded total and the exact one on full-range 3840x2160
+    noise, and no gap when all samples exceed 60000; both are reproduced here
+    on synthetic frames, within the bound."""
     import oracle as _o
 
     figs = page_figures()
@@ -282,9 +285,10 @@ def check_past_2_53_page_measurements(orc):
 
 
 def check_noise_limit_2_53(orc):
-    """ADR-1440 Consequences: the CPU's noise is exact below 2^53 units of
-    2^-16; the inverse pair (MSE far above 16570 at 3840x2160) passes it and
-    its double sum rounds, within the analogous bound."""
+    """ADR-1440 Consequences: the CPU's 16-bit noise total stops being exact
+    once it reaches 2^53 units (of 2^-16 each); the inverse pair (MSE far
+    above the 16570 limit at 3840x2160) crosses that point, so its double sum
+    rounds, and stays within the analogous bound."""
     import oracle as _o
 
     inv = cached("inv4k", lambda: wl.WORKLOADS["stress_inverse_4k16"].generate([0]))
