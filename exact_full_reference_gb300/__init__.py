@@ -80,7 +80,8 @@ def library():
                 % LIB_PATH)
         lib = ctypes.CDLL(LIB_PATH)
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-        for name in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_stats_noalloc"):
+        for name in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_stats_noalloc",
+                     "vqx_plane_stats_ordered"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
@@ -185,6 +186,15 @@ def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16
     """The same for planes in host memory (numpy arrays, pinned tensors or
     host addresses): the library copies them to the device in chunks."""
     out, rc = _call("vqx_plane_stats_host", ref, dist, width, height, stride, bpc, n_frames,
+                    _stream_handle(stream), out, check)
+    return out if check else (out, rc)
+
+
+def vqx_plane_stats_ordered(ref, dist, width=None, height=None, stride=None, bpc=16,
+                            n_frames=None, stream=None, out=None, check=True):
+    """Device planes; the doubles equal the CPU's also past 2^53 units (the
+    CPU's sequential roundings are replayed on the device)."""
+    out, rc = _call("vqx_plane_stats_ordered", ref, dist, width, height, stride, bpc, n_frames,
                     _stream_handle(stream), out, check)
     return out if check else (out, rc)
 

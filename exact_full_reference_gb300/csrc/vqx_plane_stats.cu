@@ -22,6 +22,7 @@
 
 #include "vqx.h"
 #include "vqx_kernels.cuh"
+#include "vqx_ordered.cuh"
 
 namespace {
 
@@ -335,7 +336,11 @@ cudaError_t launch_stage2(const Plan &p, int n_frames, const Partial *partials, 
 }
 
 // ------------------------------------------------------------------ conclusion
-void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats *o) {
+// cpu, when given, holds the CPU's sequential double sums (noise, reference
+// squares, distorted squares) in units, replayed on the device; otherwise
+// the exact integer sums are rounded once.
+void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats *o,
+              const u64 *cpu = nullptr) {
     const double S = (double)(1u << (bpc - 8));
     const double S2 = S * S;
     const double n = (double)width * (double)height;
@@ -347,15 +352,15 @@ void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats 
     o->flags = ((s.v[5] & 0xffffffffull) >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
     if (s.v[5] & vqx::kErrTimeout) o->flags |= VQX_FLAG_TIMEOUT;
     o->reserved = 0;
-    o->noise = (double)s.v[0] / S2;
+    o->noise = (double)(cpu ? cpu[0] : s.v[0]) / S2;
     o->mse = o->noise / n;
     o->psnr_uncapped = 10.0 * log10(255.0 * 255.0 / o->mse);
     const double cap = vqx_psnr_cap(bpc);
     o->psnr = o->psnr_uncapped < cap ? o->psnr_uncapped : cap;
     o->ref_mean = ((double)s.v[1] / S) / n;
-    o->ref_meansq = ((double)s.v[3] / S2) / n;
+    o->ref_meansq = ((double)(cpu ? cpu[1] : s.v[3]) / S2) / n;
     o->dist_mean = ((double)s.v[2] / S) / n;
-    o->dist_meansq = ((double)s.v[4] / S2) / n;
+    o->dist_meansq = ((double)(cpu ? cpu[2] : s.v[4]) / S2) / n;
 }
 
 // The call's status from the frames' flags: a timed-out device wait first
@@ -555,6 +560,88 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
 }
 
 }  // extern "C"
+
+// ====================================================================== CPU-order replay
+extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
+                                       size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                                       vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    const uint64_t pixels = (uint64_t)width * (uint64_t)height;
+    // Below 16 bits, or up to 2^21 pixels, no CPU sum can reach 2^53 units:
+    // the exact sums are the CPU's sums.
+    if (bpc != 16 || pixels <= (1u << 21))
+        return vqx_plane_stats(ref, dist, width, height, stride, bpc, n_frames, stream, out);
+    if (n_frames > 65535) return VQX_EINVAL;
+    rc = vqx_plane_stats(ref, dist, width, height, stride, bpc, n_frames, stream, out);
+    if (rc != VQX_OK) return rc;
+    bool any = false;
+    for (int f = 0; f < n_frames; f++)
+        any |= out[f].noise_units >= vqx::kTwo53 || out[f].ref_sumsq >= vqx::kTwo53 ||
+               out[f].dist_sumsq >= vqx::kTwo53;
+    if (!any) return VQX_OK;
+
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int nb = (int)((pixels + vqx::kOrdBlock - 1) / vqx::kOrdBlock);
+    const size_t cells = (size_t)n_frames * vqx::kOrdSeqs * nb;
+    const size_t sums_b = cells * sizeof(u64), cls_b = cells * sizeof(int),
+                 tab_b = cells * sizeof(vqx::OrdTable), ors_b = cells * sizeof(uint32_t);
+    PinnedBuf res;
+    if ((rc = acquire_pinned((size_t)n_frames * vqx::kOrdSeqs * sizeof(u64), &res)) != VQX_OK) return rc;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, sums_b + cls_b + tab_b + ors_b + 256, ctx->pool, st);
+    if (e != cudaSuccess) {
+        release_pinned(res);
+        return cuda_status(e);
+    }
+    u64 *sums = (u64 *)ws;
+    vqx::OrdTable *tables = (vqx::OrdTable *)((unsigned char *)ws + sums_b);
+    int *cls = (int *)((unsigned char *)ws + sums_b + tab_b);
+    uint32_t *ors = (uint32_t *)((unsigned char *)ws + sums_b + tab_b + cls_b);
+    const unsigned char *r = (const unsigned char *)ref, *d = (const unsigned char *)dist;
+    const size_t pitch = (size_t)height * stride;
+    const uint32_t px = (uint32_t)pixels;
+    vqx::ordered_block_sums<<<dim3(nb, n_frames), 128, 0, st>>>(r, d, pitch, stride, width, px, nb,
+                                                                 sums, ors);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(sums, ors, nb, cls);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        vqx::ordered_tables<<<dim3(nb, n_frames, vqx::kOrdSeqs), 32, 0, st>>>(r, d, pitch, stride, width,
+                                                                            px, nb, cls, tables);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        vqx::ordered_walk<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(
+            r, d, pitch, stride, width, px, nb, sums, ors, cls, tables, (u64 *)res.dev);
+        e = cudaGetLastError();
+    }
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    const cudaError_t es = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e != cudaSuccess) {
+        release_pinned(res);
+        return cuda_status(e);
+    }
+    t_prof.totals.kernel_launches += 4;
+    const u64 *cpu = (const u64 *)res.host;
+    for (int f = 0; f < n_frames; f++) {
+        Partial s_f;
+        s_f.v[0] = out[f].noise_units;
+        s_f.v[1] = out[f].ref_sum;
+        s_f.v[2] = out[f].dist_sum;
+        s_f.v[3] = out[f].ref_sumsq;
+        s_f.v[4] = out[f].dist_sumsq;
+        s_f.v[5] = 0;  // 16-bit: no range flag; a timeout would have returned above
+        conclude(s_f, bpc, width, height, &out[f], cpu + (size_t)f * vqx::kOrdSeqs);
+    }
+    release_pinned(res);
+    return VQX_OK;
+}
 
 // ====================================================================== no-allocation variant
 // vqx_plane_stats_noalloc runs the same two kernels as vqx_plane_stats, but

@@ -129,6 +129,28 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
                          size_t stride, int bpc, int n_frames, vqx_stream_t stream,
                          vqx_frame_stats *out);
 
+/*
+ * vqx_plane_stats_ordered: vqx_plane_stats, bit-identical to the CPU
+ * extractors also where their double sums pass 2^53 units.
+ *
+ * Past 2^53 units the CPU's running double sum rounds at every add, so its
+ * value depends on the order of the terms; vqx_plane_stats returns the exact
+ * sum rounded once, within the bound of "ADR-1447: float_moment_hip adds the
+ * float squares the CPU adds ..." (Decision).  This entry point replays the
+ * CPU's raster-order sequence of roundings on the device (ADR-1447,
+ * Alternatives, names that replay as the way to be bit-identical for every
+ * frame), so noise, mse, psnr, psnr_uncapped, ref_meansq and dist_meansq
+ * equal the CPU's doubles for every frame.  The integer fields stay the exact
+ * sums.  Only 16-bit frames of more than 2^21 pixels can pass 2^53 units;
+ * for the others, and for batches where no frame does, the call is
+ * vqx_plane_stats.  Otherwise it costs four more kernels and about two more
+ * reads of the planes.  Arguments and status codes as for vqx_plane_stats,
+ * plus VQX_EINVAL for more than 65535 frames in such a batch.
+ */
+int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
+                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                            vqx_frame_stats *out);
+
 /* The PSNR cap in dB for a bit depth (6 * bpc + 12: 60, 72, 84, 108), or a
  * NaN for an unsupported bpc.  ADR-1440 (Consequences) shows that a cap
  * exists but does not print its value; this value is a stated choice. */

@@ -1,0 +1,74 @@
+"""vqx_plane_stats_ordered against the oracle: every double of every frame
+bit for bit, also past 2^53 units, where the CPU's running double sum rounds
+and vqx_plane_stats only meets the bound of "ADR-1447 ..." (Decision)."""
+import numpy as np
+import pytest
+
+import parity
+from exact_full_reference_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+DOUBLES = ("noise", "mse", "psnr", "psnr_uncapped", "ref_mean", "ref_meansq", "dist_mean",
+           "dist_meansq")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def check_identical(rec, sc, un):
+    for f in range(len(rec)):
+        for k in parity.UNIT_FIELDS:
+            assert int(rec[f][k]) == int(un[f][k]), (f, k)
+        for k in DOUBLES:
+            assert rec[f][k].tobytes() == sc[f][k].tobytes(), (f, k, rec[f][k], sc[f][k])
+
+
+@pytest.mark.parametrize("name", ["stress_full_range_4k16", "stress_dark_tenth_4k16",
+                                  "stress_inverse_4k16", "3840x2160_16bit_x32",
+                                  "1920x1080_16bit_x64", "3840x2160_12bit_x32"])
+def test_ordered_equals_the_cpu_everywhere(lib, orc, name):
+    w = wl.WORKLOADS[name]
+    frames = range(w.n_frames) if w.n_frames <= 8 else [0, 1, 2, w.n_frames - 1]
+    ref, dist = w.generate(frames)
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    n = ref.shape[0]
+    rec = lib.vqx_plane_stats_ordered(pr, pd, w.width, w.height, stride, w.bpc, n)
+    sc, un = orc.batch(rb, db, w.width, w.height, stride, w.bpc, n)
+    check_identical(rec, sc, un)
+    if name.startswith("stress"):
+        # these frames do leave the exact range, and there the plain entry
+        # point differs from the CPU on at least one output
+        plain = lib.vqx_plane_stats(pr, pd, w.width, w.height, stride, w.bpc, n)
+        assert parity.exact_count(un) < n
+        assert any(plain[f][k].tobytes() != sc[f][k].tobytes() for f in range(n) for k in DOUBLES)
+
+
+def test_ordered_with_padded_rows_and_odd_sizes(lib, orc):
+    """Raster blocks cross rows and the last block is short: 4001 x 2399
+    (9.6 M pixels), full-range 16-bit, rows padded; the first frame is a
+    plane against its inverse, whose noise passes 2^53 units."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    ref = rng.integers(0, 65536, (2, 2399, 4001), dtype=np.uint16)
+    dist = (65535 - ref).astype(np.uint16)
+    dist[1] = rng.integers(0, 65536, (2399, 4001), dtype=np.uint16)
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist, stride=4001 * 2 + 38)
+    rec = lib.vqx_plane_stats_ordered(pr, pd, 4001, 2399, stride, 16, 2)
+    sc, un = orc.batch(rb, db, 4001, 2399, stride, 16, 2)
+    assert int(un[0]["noise_units"]) >= 2 ** 53
+    check_identical(rec, sc, un)
+
+
+def test_ordered_is_plain_below_the_limit(lib):
+    """Frames whose sums stay below 2^53 units: the same records as
+    vqx_plane_stats."""
+    w = wl.WORKLOADS["1920x1080_10bit_x48"]
+    ref, dist = w.generate([0, 1])
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    a = lib.vqx_plane_stats(pr, pd, w.width, w.height, stride, w.bpc, 2)
+    b = lib.vqx_plane_stats_ordered(pr, pd, w.width, w.height, stride, w.bpc, 2)
+    assert a.tobytes() == b.tobytes()
