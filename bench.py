@@ -371,7 +371,7 @@ def run_ours(args, wlo):
                 "timing": "CUDA events recorded by the library around each launch in a second "
                           "timed region of the same %d steps" % args.steps,
                 "instrumented_region_ms_per_step": inst_ms / args.steps,
-                "kernel": "fused_dense_tma<%d, 16, 1024, 3>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
+                "kernel": "fused_dense_tma<%d, 16, 1536, 2>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
                 "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
 

@@ -43,10 +43,11 @@ constexpr int kSumThreads = 128;  // stage-2 CTA size
 // Shape of the dense-layout stage-1 pipeline (fused_dense_tma): consumer
 // warps, 16-byte vectors per plane per stage, stages in the ring.  Chosen by
 // measurement on GB300 over 8-, 10-, 12- and 16-bit batches of 3840x2160 and
-// 1920x1080 frames; two CTAs (96 KB of ring each) are resident per SM.
+// 1920x1080 frames (two large stages beat three or more smaller ones: fewer
+// hand-offs per byte); two CTAs (96 KB of ring each) are resident per SM.
 constexpr int kTmaWarps = 16;
-constexpr int kTmaStageVecs = 1024;
-constexpr int kTmaStages = 3;
+constexpr int kTmaStageVecs = 1536;
+constexpr int kTmaStages = 2;
 constexpr int kTmaThreads = (kTmaWarps + 1) * 32;
 constexpr size_t kTmaSmem = (size_t)kTmaStages * 2 * kTmaStageVecs * 16;
 
