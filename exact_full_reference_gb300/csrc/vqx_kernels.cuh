@@ -1,10 +1,10 @@
 // Device side of the fused PSNR-noise + moment reduction (sm_103a).
 //
-// Stage 1 (fused_dense_tma / fused_rows): one pass over both planes, in
-// (frame, segment) units.  Dense planes stream through a persistent TMA
-// pipeline (bulk copies into a shared-memory ring, mbarrier hand-off to
-// consumer warps); other layouts are read row by row with 16-byte
-// non-allocating loads.  The per-pixel terms are formed and added as
+// Stage 1 (fused_stream_tma / fused_rows): one pass over both planes, in
+// (frame, segment) units.  Planes with 16-byte aligned rows stream through a
+// persistent TMA pipeline (1-D bulk copies for dense frames, 3-D tensor-map
+// tiles for padded rows, into a shared-memory ring, with an mbarrier
+// hand-off to consumer warps); other layouts are read row by row.  The per-pixel terms are formed and added as
 // integers; warp shuffles and a shared-memory step reduce each unit to one
 // Partial record, which is *written* (no atomics, nothing to clear
 // beforehand).
@@ -24,8 +24,10 @@
 // All sums are integers: exact, so the order of additions is free.
 #pragma once
 
-#include <cstdint>
+#include <cuda.h>  // CUtensorMap (a plain struct; nothing from the driver library is linked)
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace vqx {
 
@@ -40,7 +42,7 @@ struct Partial {
 constexpr int kThreads = 256;     // CTA size of the strided-layout stage-1 kernel
 constexpr int kSumThreads = 128;  // stage-2 CTA size
 
-// Shape of the dense-layout stage-1 pipeline (fused_dense_tma): consumer
+// Shape of the stage-1 TMA pipeline (fused_stream_tma): consumer
 // warps, 16-byte vectors per plane per stage, stages in the ring.  Chosen by
 // measurement on GB300 over 8-, 10-, 12- and 16-bit batches of 3840x2160 and
 // 1920x1080 frames (two large stages beat three or more smaller ones: fewer
@@ -132,6 +134,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             dst),
         "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// A 3-D tile of the tensor map tm at element coordinates (x, y, z) into
+// shared dst, completing its bytes on mbarrier bar.  x must be a multiple of
+// 16 bytes' worth of elements; parts of the box outside the tensor are
+// filled with zeros.
+__device__ __forceinline__ void tensor_g2s_3d(uint32_t dst, const CUtensorMap *tm, int x, int y,
+                                              int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 
@@ -543,18 +558,165 @@ __device__ __forceinline__ void consumer_reduce_store(u64 (&t)[6], u64 (*scratch
     consumer_sync<NCW>();  // scratch is reused by the next unit
 }
 
-// Dense layout (each frame of each plane frame_vecs contiguous, 16-byte
-// aligned 16-byte vectors) through a persistent TMA pipeline.  Unit u is
-// frame frame0 + u / segs, vectors [s * seg_vecs, min((s + 1) * seg_vecs,
-// frame_vecs)) with s = u % segs; CTA b takes units b, b + gridDim.x, ... in
-// order.  One producer lane (warp
-// NCW) streams them, stage by stage (SV vectors of each plane), into a ring
-// of STAGES shared-memory buffers with bulk copies; NCW consumer warps wait
-// for a stage's "full" mbarrier, fold it through TermSums from shared memory
-// and release it on its "empty" mbarrier (one arrive per warp) for the
-// producer to refill.  Loads stay in flight while the consumers compute,
-// without holding registers, and the ring does not drain between units: at
-// the end of a unit only the consumers meet, to reduce and write its record.
+// Where the persistent pipeline's stages come from.  A source maps a unit
+// (a (frame, segment) pair) to its stages and issues a stage's two copies
+// (reference and distorted plane), arming the stage's full mbarrier with the
+// bytes they will deliver.
+//
+// DenseSource: each frame of each plane is frame_vecs contiguous, 16-byte
+// aligned 16-byte vectors.  Unit u is frame frame0 + u / segs, vectors
+// [s * seg_vecs, min((s + 1) * seg_vecs, frame_vecs)), s = u % segs, moved
+// with 1-D bulk copies of up to SV vectors.
+struct DenseSource {
+    const unsigned char *ref, *dist;
+    size_t frame_pitch;
+    uint32_t frame_vecs, seg_vecs;
+    int segs, frame0;
+
+    struct Unit {
+        const unsigned char *r, *d;
+        uint32_t nvec;
+        size_t record;
+    };
+    __device__ __forceinline__ Unit unit(int u) const {
+        const int f = frame0 + u / segs, sg = u % segs;
+        const uint32_t v0 = min((uint32_t)sg * seg_vecs, frame_vecs);
+        Unit x;
+        x.nvec = min(v0 + seg_vecs, frame_vecs) - v0;
+        x.r = ref + (size_t)f * frame_pitch + (size_t)v0 * 16;
+        x.d = dist + (size_t)f * frame_pitch + (size_t)v0 * 16;
+        x.record = (size_t)f * segs + sg;
+        return x;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t stages(const Unit &x) const {
+        return (x.nvec + SV - 1) / SV;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t count(const Unit &x, uint32_t j) const {
+        return min((uint32_t)SV, x.nvec - j * SV);
+    }
+    template <int SV>
+    __device__ __forceinline__ void load(const Unit &x, uint32_t j, uint32_t dst_r, uint32_t dst_d,
+                                         uint32_t bar) const {
+        const uint32_t bytes = count<SV>(x, j) * 16;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s(dst_r, x.r + (size_t)j * SV * 16, bytes, bar);
+        bulk_g2s(dst_d, x.d + (size_t)j * SV * 16, bytes, bar);
+    }
+};
+
+// RowSource: rows that are a whole number of 16-byte vectors, 16-byte aligned
+// bases and row pitch (padded rows).  Unit u is frame frame0 + u / segs, rows
+// [s * seg_rows, min((s + 1) * seg_rows, height)); its rows, laid end to end,
+// are cut into stages of SV vectors exactly as a dense frame is, each stage
+// filled by one bulk copy per row piece it holds (a stage of 24 KB takes four
+// or five pieces of a 7680-byte row).
+struct RowSource {
+    const unsigned char *ref, *dist;
+    size_t frame_pitch, stride;
+    uint32_t row_vecs;
+    int height, seg_rows, segs, frame0;
+
+    struct Unit {
+        const unsigned char *r, *d;
+        uint32_t nvec;
+        size_t record;
+    };
+    __device__ __forceinline__ Unit unit(int u) const {
+        const int f = frame0 + u / segs, sg = u % segs;
+        const int y0 = min(sg * seg_rows, height);
+        Unit x;
+        x.nvec = (uint32_t)(min(y0 + seg_rows, height) - y0) * row_vecs;
+        x.r = ref + (size_t)f * frame_pitch + (size_t)y0 * stride;
+        x.d = dist + (size_t)f * frame_pitch + (size_t)y0 * stride;
+        x.record = (size_t)f * segs + sg;
+        return x;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t stages(const Unit &x) const {
+        return (x.nvec + SV - 1) / SV;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t count(const Unit &x, uint32_t j) const {
+        return min((uint32_t)SV, x.nvec - j * SV);
+    }
+    template <int SV>
+    __device__ __forceinline__ void load(const Unit &x, uint32_t j, uint32_t dst_r, uint32_t dst_d,
+                                         uint32_t bar) const {
+        const uint32_t v0 = j * SV, end = v0 + count<SV>(x, j);
+        mbar_arrive_expect_tx(bar, 2 * (end - v0) * 16);
+        for (uint32_t v = v0; v < end;) {
+            const uint32_t row = v / row_vecs, col = v - row * row_vecs;
+            const uint32_t n = min(row_vecs - col, end - v);
+            const size_t off = (size_t)row * stride + (size_t)col * 16;
+            bulk_g2s(dst_r + (v - v0) * 16, x.r + off, n * 16, bar);
+            bulk_g2s(dst_d + (v - v0) * 16, x.d + off, n * 16, bar);
+            v += n;
+        }
+    }
+};
+
+// TileSource: any layout whose bases and row pitch are 16-byte aligned,
+// through two 3-D tensor maps (width x height x frames elements of 1 to 8
+// bytes, with the row and frame pitches in bytes; the kernel never looks at
+// the element type, so the host picks the widest one that divides a row).
+// Unit u is frame frame0 + u / segs, rows [s * seg_rows, min((s + 1) *
+// seg_rows, height)), seg_rows a multiple of by; its stages are the bx x by
+// boxes covering those rows, left to right, top to bottom, each box_vecs
+// 16-byte vectors (at most one stage).  Parts of a box past the last column
+// or row are filled with zeros by the copy, and zero samples in both planes
+// add nothing to any sum.
+struct TileSource {
+    CUtensorMap tref, tdist;
+    int width, height, seg_rows, segs, frame0;
+    int bx, by;
+    uint32_t box_vecs;
+
+    struct Unit {
+        int z, y0, tiles_x;
+        uint32_t n;
+        size_t record;
+    };
+    __device__ __forceinline__ Unit unit(int u) const {
+        Unit x;
+        x.z = u / segs;
+        const int sg = u % segs;
+        x.y0 = sg * seg_rows;
+        const int rows = max(0, min(x.y0 + seg_rows, height) - x.y0);
+        x.tiles_x = (width + bx - 1) / bx;
+        x.n = (uint32_t)(((rows + by - 1) / by) * x.tiles_x);
+        x.record = (size_t)(frame0 + x.z) * segs + sg;
+        return x;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t stages(const Unit &x) const {
+        return x.n;
+    }
+    template <int SV>
+    __device__ __forceinline__ uint32_t count(const Unit &, uint32_t) const {
+        return box_vecs;
+    }
+    template <int SV>
+    __device__ __forceinline__ void load(const Unit &x, uint32_t j, uint32_t dst_r, uint32_t dst_d,
+                                         uint32_t bar) const {
+        const int ty = x.y0 + (int)(j / x.tiles_x) * by;
+        const int tx = (int)(j % x.tiles_x) * bx;
+        mbar_arrive_expect_tx(bar, 2 * box_vecs * 16);
+        tensor_g2s_3d(dst_r, &tref, tx, ty, x.z, bar);
+        tensor_g2s_3d(dst_d, &tdist, tx, ty, x.z, bar);
+    }
+};
+
+// The persistent TMA pipeline.  CTA b takes units b, b + gridDim.x, ... in
+// order.  One producer lane (warp NCW) streams them, stage by stage (SV
+// 16-byte vectors of each plane), into a ring of STAGES shared-memory buffers;
+// NCW consumer warps wait for a stage's "full" mbarrier, fold it through
+// TermSums from shared memory and release it on its "empty" mbarrier (one
+// arrive per warp) for the producer to refill.  Loads stay in flight while
+// the consumers compute, without holding registers, and the ring does not
+// drain between units: at the end of a unit only the consumers meet, to
+// reduce and write its record.
 //
 // Ring phases: the CTA's k-th stage (counted across its units) goes to buffer
 // k % STAGES; its full barrier completes phase k / STAGES, and the producer
@@ -563,11 +725,9 @@ __device__ __forceinline__ void consumer_reduce_store(u64 (&t)[6], u64 (*scratch
 // sets kErrTimeout in the waiting thread; from then on that warp waits for
 // nothing, still writes (flagged) records for its remaining units, and the
 // producer waits (bounded) for the copies it issued before the CTA exits.
-template <int BPC, int NCW, int SV, int STAGES>
+template <int BPC, int NCW, int SV, int STAGES, class Src>
 __global__ void __launch_bounds__((NCW + 1) * 32)
-    fused_dense_tma(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
-                    size_t frame_pitch, uint32_t frame_vecs, uint32_t seg_vecs, int segs,
-                    int frame0, int units, Partial *__restrict__ partials) {
+    fused_stream_tma(const __grid_constant__ Src src, int units, Partial *__restrict__ partials) {
     constexpr uint32_t kStageBytes = SV * 16;  // per plane
     constexpr uint32_t kPerThread = SV / (NCW * 32);
     static_assert(SV % (NCW * 32) == 0, "a full stage gives every consumer thread equal work");
@@ -595,23 +755,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         bool ok = true;
         uint32_t k = 0;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-            const int f = frame0 + u / segs;
-            const uint32_t v0 = min((uint32_t)(u % segs) * seg_vecs, frame_vecs);
-            const uint32_t nvec = min(v0 + seg_vecs, frame_vecs) - v0;
-            const unsigned char *R = ref + (size_t)f * frame_pitch + (size_t)v0 * 16;
-            const unsigned char *D = dist + (size_t)f * frame_pitch + (size_t)v0 * 16;
-            for (uint32_t j = 0; j * SV < nvec; j++, k++) {
+            const typename Src::Unit x = src.unit(u);
+            const uint32_t n = src.template stages<SV>(x);
+            for (uint32_t j = 0; j < n; j++, k++) {
                 const uint32_t st = k % STAGES;
                 if (k >= STAGES && !mbar_wait(empty0 + 8 * st, ((k / STAGES) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                const uint32_t bytes = min((uint32_t)SV, nvec - j * SV) * 16;
-                mbar_arrive_expect_tx(full0 + 8 * st, 2 * bytes);
-                bulk_g2s(ring0 + (2 * st) * kStageBytes, R + (size_t)j * kStageBytes, bytes,
-                         full0 + 8 * st);
-                bulk_g2s(ring0 + (2 * st + 1) * kStageBytes, D + (size_t)j * kStageBytes, bytes,
-                         full0 + 8 * st);
+                src.template load<SV>(x, j, ring0 + (2 * st) * kStageBytes,
+                                      ring0 + (2 * st + 1) * kStageBytes, full0 + 8 * st);
             }
         }
         // The last copies must have landed before the CTA (and its shared
@@ -624,13 +777,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     u64 err = 0;
     uint32_t k = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int f = frame0 + u / segs;
-        const int sg = u % segs;
-        const uint32_t v0 = min((uint32_t)sg * seg_vecs, frame_vecs);
-        const uint32_t nvec = min(v0 + seg_vecs, frame_vecs) - v0;
+        const typename Src::Unit x = src.unit(u);
+        const uint32_t n = src.template stages<SV>(x);
         TermSums<BPC> acc;
         uint32_t since_flush = 0;
-        for (uint32_t j = 0; j * SV < nvec; j++, k++) {
+        for (uint32_t j = 0; j < n; j++, k++) {
             if (err) continue;  // a wait of this warp timed out: skip, write flagged records
             const uint32_t st = k % STAGES;
             // every lane's wait is bounded; the warp then decides together,
@@ -641,7 +792,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
             }
             const uint4 *a = reinterpret_cast<const uint4 *>(ring + (2 * st) * kStageBytes);
             const uint4 *b = reinterpret_cast<const uint4 *>(ring + (2 * st + 1) * kStageBytes);
-            const uint32_t cnt = min((uint32_t)SV, nvec - j * SV);
+            const uint32_t cnt = src.template count<SV>(x, j);
             if (cnt == SV) {
 #pragma unroll
                 for (uint32_t q = 0; q < kPerThread; q++) {
@@ -661,7 +812,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         u64 t[6];
         acc.totals(t);
         t[5] |= err;
-        consumer_reduce_store<NCW>(t, red, partials[(size_t)f * segs + sg].v);
+        consumer_reduce_store<NCW>(t, red, partials[x.record].v);
     }
 }
 

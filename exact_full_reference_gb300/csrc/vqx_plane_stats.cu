@@ -12,6 +12,8 @@
 // and divides by scaler^2; "ADR-1447: float_moment_hip adds the float squares
 // the CPU adds ...", Decision: the two final divisions) is compiled with
 // contraction off, and uses only divisions, one product by 10 and log10.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -37,7 +39,13 @@ int cuda_status(cudaError_t e) {
 }
 
 // ------------------------------------------------------------------ paths
-enum Path { kDense = 0, kRowsVec = 1, kRowsScalar = 2, kPaths = 3 };
+// kDense: frames of contiguous, 16-byte aligned rows (1-D bulk copies);
+// kRows: padded rows of whole 16-byte vectors, at least kRowsMinBytes long,
+// on 16-byte aligned bases and pitch (1-D bulk copies of row pieces);
+// kTiles: other rows on 16-byte aligned bases and pitch (tensor-map boxes);
+// kRowsScalar: anything else (sample loads).
+enum Path { kDense = 0, kTiles = 1, kRowsScalar = 2, kRows = 3, kPaths = 4 };
+constexpr size_t kRowsMinBytes = 512;
 
 int bpc_index(int bpc) { return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3; }
 
@@ -48,16 +56,65 @@ struct Stage1Shape {
     size_t smem;
 };
 
+template <int BPC, class Src>
+constexpr auto stream_kernel() {
+    return vqx::fused_stream_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages, Src>;
+}
+
 template <int BPC>
 Stage1Shape stage1_shape(int path) {
     switch (path) {
     case kDense:
-        return {(const void *)vqx::fused_dense_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs,
-                                                   vqx::kTmaStages>,
-                vqx::kTmaThreads, vqx::kTmaSmem};
-    case kRowsVec: return {(const void *)vqx::fused_rows<BPC, true>, vqx::kThreads, 0};
+        return {(const void *)stream_kernel<BPC, vqx::DenseSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
+    case kTiles:
+        return {(const void *)stream_kernel<BPC, vqx::TileSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
+    case kRows:
+        return {(const void *)stream_kernel<BPC, vqx::RowSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
     default: return {(const void *)vqx::fused_rows<BPC, false>, vqx::kThreads, 0};
     }
+}
+
+// cuTensorMapEncodeTiled, found through the runtime (no link against the
+// driver library), once per process.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *out) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
+            g_encode_err = cudaErrorNotSupported;
+        g_encode_tiled = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    });
+    *out = g_encode_tiled;
+    return g_encode_err;
+}
+
+// A width x height x frames tensor of elem_bytes-byte elements starting at
+// base, rows `stride` bytes apart and frames height * stride apart, read in
+// bx x by x 1 boxes.
+cudaError_t encode_planes(CUtensorMap *tm, const void *base, int elem_bytes, int width, int height,
+                          size_t stride, int frames, int bx, int by) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = encode_fn(&enc);
+    if (e != cudaSuccess) return e;
+    const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)height, (cuuint64_t)frames};
+    const cuuint64_t strides[2] = {(cuuint64_t)stride, (cuuint64_t)stride * (cuuint64_t)height};
+    const cuuint32_t box[3] = {(cuuint32_t)bx, (cuuint32_t)by, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUtensorMapDataType type = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                     : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                       : CU_TENSOR_MAP_DATA_TYPE_INT64;
+    const CUresult r = enc(tm, type,
+                           3, const_cast<void *>(base), dims, strides, box, elem,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 Stage1Shape stage1_shape(int path, int bpc) {
@@ -227,7 +284,39 @@ struct Plan {
     size_t frame_pitch = 0;
     size_t stride = 0;
     int width = 0, height = 0;
+    int tile_elem = 0, tile_bx = 0, tile_by = 0;  // kTiles: element bytes, box
 };
+
+// The box of the tile path for rows of row_bytes bytes: the element is the
+// widest of 8, 4, 2 or 1 bytes that divides a row; a box line is a whole
+// number of 16-byte vectors and at most 256 elements, and a box at most one
+// pipeline stage, and at most max_by rows (so that a small batch still
+// splits into enough bands to keep every CTA busy).  Among those the box with
+// the least work per frame wins, counting the zero fill past the last column
+// and row as work, with a fixed cost per stage and per box line (a box of
+// short lines copies measurably slower than one of long lines with some fill).
+void choose_box(size_t row_bytes, int height, long long max_by, int *elem, int *bx, int *by) {
+    int eb = 8;
+    while (row_bytes % (size_t)eb) eb /= 2;
+    const long long row_elems = (long long)(row_bytes / (size_t)eb);
+    const long long cap = (long long)vqx::kTmaStageVecs * 16;
+    const long long kStageCost = 128, kLineCost = 64;  // in vectors' worth of work
+    long long best = -1;
+    for (int x = 16 / eb; x <= 256; x += 16 / eb) {
+        long long y = cap / ((long long)x * eb);
+        if (y > 256) y = 256;
+        if (y > height) y = height;
+        if (y > max_by) y = max_by;
+        const long long vecs = (long long)x * y * eb / 16;
+        const long long cost = ((row_elems + x - 1) / x) * ((height + y - 1) / y) * (vecs + kStageCost + y * kLineCost);
+        if (best < 0 || cost <= best) {  // ties: the longer line
+            best = cost;
+            *bx = x;
+            *by = (int)y;
+        }
+    }
+    *elem = eb;
+}
 
 // Segments per frame: the grid (frames x segments CTAs) should fill whole
 // waves of resident CTAs, so that no SM idles at the end; among equally full
@@ -270,15 +359,60 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
         p.path = kDense;
         p.work = (uint32_t)(frame_bytes >> 4);
     } else {
-        p.path = (aligned && (stride & 15u) == 0) ? kRowsVec : kRowsScalar;
+        // copies need 16-byte aligned rows; very narrow ones take the sample path
+        const bool pitched = aligned && (stride & 15u) == 0;
+        p.path = pitched && (row_bytes & 15u) == 0 && row_bytes >= kRowsMinBytes ? kRows
+                 : pitched && width >= 64                                         ? kTiles
+                                                                                  : kRowsScalar;
         p.work = (uint32_t)height;
     }
     p.resident = (long long)c.sms * c.resident[p.path][bpc_index(bpc)];
-    // a dense unit is at least one pipeline stage, a row unit one row per warp
-    const uint32_t min_unit = p.path == kDense ? (uint32_t)vqx::kTmaStageVecs : 8u;
+    if (p.path == kTiles) {
+        // rows per CTA were the batch spread over every resident CTA
+        long long max_by = (long long)height * frames_per_launch / (p.resident > 0 ? p.resident : 1);
+        if (max_by < 1) max_by = 1;
+        choose_box(row_bytes, height, max_by, &p.tile_elem, &p.tile_bx, &p.tile_by);
+    }
+    // a dense or row-piece unit is at least one pipeline stage, a tile unit
+    // one band of boxes, a scalar row unit one row per warp
+    const uint32_t band = (uint32_t)p.tile_by;
+    const uint32_t stage_rows = (uint32_t)(((size_t)vqx::kTmaStageVecs * 16 + row_bytes - 1) / row_bytes);
+    const uint32_t min_unit = p.path == kDense  ? (uint32_t)vqx::kTmaStageVecs
+                              : p.path == kRows  ? stage_rows
+                              : p.path == kTiles ? band
+                                                 : 8u;
     p.segs = choose_segs(frames_per_launch, p.work, min_unit, p.resident);
     p.seg_work = (p.work + (uint32_t)p.segs - 1) / (uint32_t)p.segs;
+    if (p.path == kTiles) {  // whole bands of boxes
+        p.seg_work = (p.seg_work + band - 1) / band * band;
+        p.segs = (int)((p.work + p.seg_work - 1) / p.seg_work);
+    }
     return p;
+}
+
+template <int BPC>
+cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned char *ref,
+                         const unsigned char *dist, int frame0, int frames, int units,
+                         Partial *partials) {
+    vqx::TileSource src;
+    memset(&src, 0, sizeof src);
+    const size_t first = (size_t)frame0 * p.frame_pitch;
+    const int row_elems = (int)((size_t)p.width * bytes_per_sample(BPC) / (size_t)p.tile_elem);
+    cudaError_t e = encode_planes(&src.tref, ref + first, p.tile_elem, row_elems, p.height, p.stride,
+                                  frames, p.tile_bx, p.tile_by);
+    if (e == cudaSuccess)
+        e = encode_planes(&src.tdist, dist + first, p.tile_elem, row_elems, p.height, p.stride,
+                          frames, p.tile_bx, p.tile_by);
+    if (e != cudaSuccess) return e;
+    src.width = row_elems;
+    src.height = p.height;
+    src.seg_rows = (int)p.seg_work;
+    src.segs = p.segs;
+    src.frame0 = frame0;
+    src.bx = p.tile_bx;
+    src.by = p.tile_by;
+    src.box_vecs = (uint32_t)((size_t)p.tile_bx * p.tile_by * p.tile_elem / 16);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource>(), src, units, partials);
 }
 
 template <int BPC>
@@ -287,25 +421,45 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     const long long units = (long long)frames * p.segs;
-    cfg.gridDim = dim3((unsigned)units);
-    cfg.blockDim = dim3(vqx::kThreads);
     cfg.stream = st;
-    if (p.path == kDense) {
-        // persistent: at most the resident CTAs, each walking several units
-        cfg.gridDim = dim3((unsigned)(units < p.resident ? units : p.resident));
-        cfg.blockDim = dim3(vqx::kTmaThreads);
-        cfg.dynamicSmemBytes = vqx::kTmaSmem;
-        return cudaLaunchKernelEx(
-            &cfg, vqx::fused_dense_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages>,
-            ref, dist, p.frame_pitch, p.work, p.seg_work, p.segs, frame0, (int)units, partials);
-    }
-    if (p.path == kRowsVec)
-        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, true>, ref, dist, p.frame_pitch,
+    if (p.path == kRowsScalar) {
+        cfg.gridDim = dim3((unsigned)units);
+        cfg.blockDim = dim3(vqx::kThreads);
+        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false>, ref, dist, p.frame_pitch,
                                   p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
                                   partials);
-    return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false>, ref, dist, p.frame_pitch,
-                              p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
-                              partials);
+    }
+    // persistent: at most the resident CTAs, each walking several units
+    cfg.gridDim = dim3((unsigned)(units < p.resident ? units : p.resident));
+    cfg.blockDim = dim3(vqx::kTmaThreads);
+    cfg.dynamicSmemBytes = vqx::kTmaSmem;
+    if (p.path == kDense) {
+        vqx::DenseSource src;
+        src.ref = ref;
+        src.dist = dist;
+        src.frame_pitch = p.frame_pitch;
+        src.frame_vecs = p.work;
+        src.seg_vecs = p.seg_work;
+        src.segs = p.segs;
+        src.frame0 = frame0;
+        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::DenseSource>(), src, (int)units,
+                                  partials);
+    }
+    if (p.path == kRows) {
+        vqx::RowSource src;
+        src.ref = ref;
+        src.dist = dist;
+        src.frame_pitch = p.frame_pitch;
+        src.stride = p.stride;
+        src.row_vecs = (uint32_t)((size_t)p.width * bytes_per_sample(BPC) / 16);
+        src.height = p.height;
+        src.seg_rows = (int)p.seg_work;
+        src.segs = p.segs;
+        src.frame0 = frame0;
+        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::RowSource>(), src, (int)units,
+                                  partials);
+    }
+    return launch_tiles<BPC>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
 }
 
 cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int frame0,

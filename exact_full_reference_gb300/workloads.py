@@ -138,6 +138,23 @@ def _inverse_pair(wl, rng, _f):
     return ref, (top - ref).astype(wl.dtype)
 
 
+def _eight_bit_widened(how):
+    """8-bit content (the noisy-copy pair at sigma 8) carried in a wider
+    container: shifted left by bpc - 8 bits, or multiplied by 257 to span the
+    16-bit range."""
+
+    def make(wl, rng, _f):
+        ref = rng.integers(0, 256, (wl.height, wl.width), dtype=np.int64)
+        noise = np.rint(rng.normal(0.0, 8.0, (wl.height, wl.width))).astype(np.int64)
+        dist = np.clip(ref + noise, 0, 255)
+        if how == "shift":
+            k = wl.bpc - 8
+            return (ref << k).astype(wl.dtype), (dist << k).astype(wl.dtype)
+        return (ref * 257).astype(wl.dtype), (dist * 257).astype(wl.dtype)
+
+    return make
+
+
 _FRAME_MAKERS = {
     "noisy_copy_8": _noisy_copy(8.0),
     "gradient_texture": _gradient_texture,
@@ -146,6 +163,8 @@ _FRAME_MAKERS = {
     "bright_checker": _bright_with_checker,
     "dark_tenth": _dark_tenth,
     "inverse": _inverse_pair,
+    "shifted_8": _eight_bit_widened("shift"),
+    "times_257": _eight_bit_widened("257"),
 }
 
 # The five measured configurations, then the stress frames used only for
@@ -161,6 +180,21 @@ WORKLOADS = {
                                     "uniform_bright", "bright 16-bit 1080p pair stand-in"),
     "3840x2160_16bit_x32": Workload("3840x2160_16bit_x32", 3840, 2160, 16, 32, 5,
                                     "bright_checker", "bright 16-bit 4K batch + checkerboard"),
+    # Other plane shapes and containers the pages run their twins on: 8-bit
+    # content shifted left to 10, 12 and 16 bits, 8-bit content scaled by 257
+    # to 16 bits, and 10-bit chroma planes of 4:2:2 and 4:2:0 576x324 video.
+    "576x324_8bit_shifted_10": Workload("576x324_8bit_shifted_10", 576, 324, 10, 2, 21, "shifted_8",
+                                        "8-bit clip shifted to 10 bits"),
+    "576x324_8bit_shifted_12": Workload("576x324_8bit_shifted_12", 576, 324, 12, 2, 22, "shifted_8",
+                                        "8-bit clip shifted to 12 bits"),
+    "576x324_8bit_shifted_16": Workload("576x324_8bit_shifted_16", 576, 324, 16, 2, 23, "shifted_8",
+                                        "8-bit clip shifted to 16 bits"),
+    "1920x1080_8bit_x257_16": Workload("1920x1080_8bit_x257_16", 1920, 1080, 16, 4, 24, "times_257",
+                                       "8-bit content times 257 as 16 bits"),
+    "288x324_10bit_chroma422": Workload("288x324_10bit_chroma422", 288, 324, 10, 4, 25,
+                                        "gradient_texture", "4:2:2 chroma plane, 10 bits"),
+    "288x162_10bit_chroma420": Workload("288x162_10bit_chroma420", 288, 162, 10, 4, 26,
+                                        "gradient_texture", "4:2:0 chroma plane, 10 bits"),
     "stress_full_range_4k16": Workload("stress_full_range_4k16", 3840, 2160, 16, 2, 11,
                                        "uniform_full", "full-range 16-bit 4K noise"),
     "stress_dark_tenth_4k16": Workload("stress_dark_tenth_4k16", 3840, 2160, 16, 2, 12,

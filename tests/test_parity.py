@@ -215,3 +215,29 @@ def test_profile_counts_launches(lib):
     lib.profile_enable(False)
     assert p["calls"] == 3 and p["kernel_launches"] == 6 and p["stage1_launches"] == 3
     assert p["stage1_ms"] > 0 and p["stage1_bytes"] == 3 * 2 * 576 * 324
+
+
+@pytest.mark.parametrize("bpc", [8, 10, 12, 16])
+@pytest.mark.parametrize("w,h,pad", [(3840, 2160, 256), (1000, 97, 48), (257, 49, 16), (64, 200, 64),
+                                     (1922, 67, 30), (4100, 13, 16), (2052, 3, 40), (4096, 50, 16),
+                                     (256, 70, 48), (1024, 33, 16), (1920, 1080, 128)])
+def test_padded_aligned_rows(lib, orc, bpc, w, h, pad):
+    """Rows on a 16-byte aligned pitch, with padding: bulk copies of row
+    pieces where a row is a whole number of 16-byte vectors (and at least
+    512 bytes), tensor-map boxes otherwise, including boxes past the last
+    column and row (zero-filled by the copy)."""
+    bps = 1 if bpc == 8 else 2
+    stride = (w * bps + pad + 15) // 16 * 16
+    n = 3 if w * h < 1_000_000 else 2
+    rng = np.random.Generator(np.random.PCG64(w + 7 * h + bpc))
+    dt = np.uint8 if bpc == 8 else np.uint16
+    ref = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    dist = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    run_case(lib, orc, ref, dist, bpc, stride=stride)
+
+
+def test_headline_batch_with_padded_rows(lib, orc):
+    """The 3840x2160 16-bit batch with 256 bytes of padding per row."""
+    w = wl.WORKLOADS["3840x2160_16bit_x32"]
+    ref, dist = w.generate(range(8))
+    run_case(lib, orc, ref, dist, 16, stride=3840 * 2 + 256)
