@@ -1,11 +1,13 @@
 #!/usr/bin/env python3
 """Throughput of the fused PSNR-noise + moment statistics on GB300.
 
-One step = one ``vqx_plane_stats`` call (the whole hot path: load, per-pixel
-terms, exact integer reduction, per-frame sums, read-back, conclusion in
-double) over one batch of synthetic planes already resident in HBM.  The
-default batch is 32 frame pairs of 3840x2160 16-bit luma (1.06 GB, larger than
-L2, so no flush is needed between steps).
+One step = one batch of synthetic planes already resident in HBM through
+``vqx_plane_stats_submit`` + ``vqx_plane_stats_finish`` (the whole hot path,
+the work of one ``vqx_plane_stats`` call: load, per-pixel terms, exact integer
+reduction, per-frame sums, read-back, conclusion in double).  Steps are
+pipelined one deep: batch i + 1 is enqueued before batch i is waited on and
+concluded.  The default batch is 32 frame pairs of 3840x2160 16-bit luma
+(1.06 GB, larger than L2, so no flush is needed between steps).
 
 Prints ONE JSON line (rank 0).  ``value`` is whole-job frame pairs/s; ``e2e``
 is the same metric through ``vqx_plane_stats_host`` with the planes in pinned
@@ -49,6 +51,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
+                   help="write the DRAM traffic record of the fused kernel from an ncu report "
+                        "(read here with ncu -i; needs no GPU) and exit")
     return p.parse_args()
 
 
@@ -179,10 +184,17 @@ def kernel_source_digest():
     return h.hexdigest()
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "fused_stream_traffic.json")
+KERNEL_LABEL = "fused_stream_tma<%d, 16, 1536, 2, DenseSource>"
+# the capture the traffic record is taken from (the plain command runs first)
+TRAFFIC_CAPTURE = ("ncu --set full --clock-control none -k regex:fused_stream -s 3 -c 1 "
+                   "-o prof_fused_stream python bench.py --steps 5 --warmup 3 --no-cpu --no-e2e")
+
+
 def recorded_traffic(workload_name):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
     or None when the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "fused_dense_traffic.json")
+    path = TRAFFIC_RECORD
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -192,6 +204,49 @@ def recorded_traffic(workload_name):
         return None
     per = rec.get("per_launch_bytes", {}).get(workload_name)
     return float(per) if per is not None else None
+
+
+def write_traffic_record(report, wlo):
+    """Read the fused kernel's launch from an ncu report (``ncu -i``, no GPU
+    needed) and write the traffic record that ``recorded_traffic`` reads,
+    keyed by the current kernel sources."""
+    import csv
+
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], capture_output=True,
+                         text=True, check=True).stdout
+    rows = list(csv.reader(out.splitlines()))
+    hdr, units = rows[0], rows[1]
+    launches = [dict(zip(hdr, zip(units, r))) for r in rows[2:]]
+    launches = [d for d in launches if "fused_stream_tma" in d.get("Kernel Name", ("", ""))[1]]
+    if not launches:
+        raise SystemExit("no fused_stream_tma launch in %s" % report)
+    d = launches[0]
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+             "ns": 1e-3, "us": 1.0, "ms": 1e3, "s": 1e6,
+             "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3, "second": 1e6}
+
+    def val(name):
+        unit, v = d[name]
+        return float(v.replace(",", "")) * scale.get(unit, 1.0)
+
+    rd, wr = val("dram__bytes_read.sum"), val("dram__bytes_write.sum")
+    bps = 1 if wlo.bpc == 8 else 2
+    rec = {
+        "kernel": KERNEL_LABEL % wlo.bpc,
+        "source_sha256": kernel_source_digest(),
+        "per_launch_bytes": {wlo.name: rd + wr},
+        "dram_bytes_read": rd,
+        "dram_bytes_write": wr,
+        "algorithmic_bytes": 2 * wlo.width * wlo.height * bps * wlo.n_frames,
+        "gpu_dram_throughput_pct": float(d["gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed"][1]),
+        "duration_us": val("gpu__time_duration.sum"),
+        "command": TRAFFIC_CAPTURE,
+    }
+    with open(TRAFFIC_RECORD, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec))
+    return 0
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -314,17 +369,38 @@ def run_ours(args, wlo):
     out_p = out.ctypes.data
     call_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh, out_p)
 
-    def step():
-        rc = so.vqx_plane_stats(*call_args)
+    submit_args = call_args[:-1]
+
+    def submit():
+        handle = ctypes.c_void_p()
+        rc = so.vqx_plane_stats_submit(*submit_args, ctypes.byref(handle))
         if rc != 0:
-            raise RuntimeError("vqx_plane_stats: %s" % vqx.status_string(rc))
+            raise RuntimeError("vqx_plane_stats_submit: %s" % vqx.status_string(rc))
+        return handle
+
+    def finish(handle):
+        rc = so.vqx_plane_stats_finish(handle, out_p)
+        if rc != 0:
+            raise RuntimeError("vqx_plane_stats_finish: %s" % vqx.status_string(rc))
+
+    def steps(k):
+        """k whole steps, pipelined: batch i + 1 is enqueued before batch i is
+        waited on and concluded, so the device runs the next batch's kernels
+        while the host concludes this one."""
+        prev = None
+        for _ in range(k):
+            cur = submit()
+            if prev is not None:
+                finish(prev)
+            prev = cur
+        if prev is not None:
+            finish(prev)
 
     def barrier():
         if pg is not None:
             pg.barrier()
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    steps(max(args.warmup, 3))
     torch.cuda.synchronize()
 
     def timed_region(instrumented):
@@ -341,8 +417,7 @@ def run_ours(args, wlo):
         ev1 = torch.cuda.Event(enable_timing=True)
         t0 = time.time()
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        steps(args.steps)  # the last conclusion is inside the region too
         ev1.record(stream)
         torch.cuda.synchronize()
         t1 = time.time()
@@ -371,7 +446,7 @@ def run_ours(args, wlo):
                 "timing": "CUDA events recorded by the library around each launch in a second "
                           "timed region of the same %d steps" % args.steps,
                 "instrumented_region_ms_per_step": inst_ms / args.steps,
-                "kernel": "fused_dense_tma<%d, 16, 1536, 2>" % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
+                "kernel": KERNEL_LABEL % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
                 "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
 
@@ -428,6 +503,8 @@ def run_ours(args, wlo):
             "config": {"workload": wlo.name, "frames_per_gpu": n, "width": w, "height": h,
                        "bpc": wlo.bpc, "batch_bytes": int(rbytes.nbytes + dbytes.nbytes),
                        "l2": "inputs 1.06 GB per step, larger than the 129 MB L2; no flush",
+                       "pipeline": "batch i + 1 submitted before batch i is finished "
+                                   "(vqx_plane_stats_submit / vqx_plane_stats_finish)",
                        "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e,
             "roofline": roofline,
@@ -448,6 +525,8 @@ def main():
     from exact_full_reference_gb300 import workloads as wl
 
     wlo = wl.WORKLOADS[args.workload or wl.HEADLINE]
+    if args.record_traffic:
+        return write_traffic_record(args.record_traffic, wlo)
     if args.impl == "reference":
         return run_reference(args, wlo)
     return run_ours(args, wlo)

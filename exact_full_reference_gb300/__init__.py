@@ -85,6 +85,10 @@ def library():
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
+        lib.vqx_plane_stats_submit.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.POINTER(vp)]
+        lib.vqx_plane_stats_submit.restype = i
+        lib.vqx_plane_stats_finish.argtypes = [vp, vp]
+        lib.vqx_plane_stats_finish.restype = i
         lib.vqx_psnr_cap.argtypes = [i]
         lib.vqx_psnr_cap.restype = ctypes.c_double
         lib.vqx_status_string.argtypes = [i]
@@ -152,6 +156,13 @@ def psnr_cap(bpc):
     return library().vqx_psnr_cap(bpc)
 
 
+def _raise(name, rc):
+    msg = "%s failed: %s (%d)" % (name, status_string(rc), rc)
+    if rc == VQX_ECUDA:
+        msg += ", cudaError %d" % library().vqx_last_cuda_error()
+    raise VqxError(rc, msg)
+
+
 def _call(name, ref, dist, width, height, stride, bpc, n_frames, stream, out, check):
     width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
     if out is None:
@@ -160,10 +171,7 @@ def _call(name, ref, dist, width, height, stride, bpc, n_frames, stream, out, ch
         _address(ref), _address(dist), width, height, stride, bpc, n_frames, stream,
         out.ctypes.data if out.size else None)
     if check and rc not in (VQX_OK,):
-        msg = "%s failed: %s (%d)" % (name, status_string(rc), rc)
-        if rc == VQX_ECUDA:
-            msg += ", cudaError %d" % library().vqx_last_cuda_error()
-        raise VqxError(rc, msg)
+        _raise(name, rc)
     return out, rc
 
 
@@ -179,6 +187,41 @@ def vqx_plane_stats(ref, dist, width=None, height=None, stride=None, bpc=16, n_f
     out, rc = _call("vqx_plane_stats", ref, dist, width, height, stride, bpc, n_frames,
                     _stream_handle(stream), out, check)
     return out if check else (out, rc)
+
+
+class Pending:
+    """A batch enqueued by ``vqx_plane_stats_submit``; ``finish()`` waits for
+    it and returns its records (call it exactly once)."""
+
+    def __init__(self, handle, n_frames, keep):
+        self._handle = handle
+        self.n_frames = n_frames
+        self._keep = keep  # the planes stay referenced until the batch is finished
+
+    def finish(self, out=None, check=True):
+        if self._handle is False:
+            raise RuntimeError("this batch was already finished")
+        if out is None:
+            out = np.zeros(self.n_frames, FRAME_STATS_DTYPE)
+        rc = library().vqx_plane_stats_finish(self._handle, out.ctypes.data if out.size else None)
+        self._handle, self._keep = False, None
+        if check and rc != VQX_OK:
+            _raise("vqx_plane_stats_finish", rc)
+        return out if check else (out, rc)
+
+
+def vqx_plane_stats_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
+                           n_frames=None, stream=None):
+    """Enqueue a batch of device planes without waiting; returns a
+    ``Pending`` whose ``finish()`` gives what ``vqx_plane_stats`` would."""
+    width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
+    handle = ctypes.c_void_p()
+    rc = library().vqx_plane_stats_submit(_address(ref), _address(dist), width, height, stride,
+                                          bpc, n_frames, _stream_handle(stream),
+                                          ctypes.byref(handle))
+    if rc != VQX_OK:
+        _raise("vqx_plane_stats_submit", rc)
+    return Pending(handle.value, max(n_frames, 0), (ref, dist))
 
 
 def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16,

@@ -558,6 +558,23 @@ __device__ __forceinline__ void consumer_reduce_store(u64 (&t)[6], u64 (*scratch
     consumer_sync<NCW>();  // scratch is reused by the next unit
 }
 
+// One warp's totals to one record: warp shuffles, lanes 0..5 store a word
+// each.  No other warp takes part, so no warp waits at the end of a unit.
+__device__ __forceinline__ void warp_reduce_store(u64 (&t)[6], u64 *dst) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < 5; k++) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
+        t[5] |= __shfl_xor_sync(0xffffffffu, t[5], o);
+    }
+    const int lane = threadIdx.x & 31;
+    u64 mine = 0;
+#pragma unroll
+    for (int k = 0; k < 6; k++)
+        if (lane == k) mine = t[k];
+    if (lane < 6) dst[lane] = mine;
+}
+
 // Where the persistent pipeline's stages come from.  A source maps a unit
 // (a (frame, segment) pair) to its stages and issues a stage's two copies
 // (reference and distorted plane), arming the stage's full mbarrier with the
@@ -725,9 +742,15 @@ struct TileSource {
 // sets kErrTimeout in the waiting thread; from then on that warp waits for
 // nothing, still writes (flagged) records for its remaining units, and the
 // producer waits (bounded) for the copies it issued before the CTA exits.
+//
+// Records: with warp_records every consumer warp writes its own record of
+// each unit (record r of the source becomes records r * NCW .. r * NCW +
+// NCW - 1) and ends a unit without waiting for the others; otherwise the
+// consumers reduce to one record per unit through shared memory.
 template <int BPC, int NCW, int SV, int STAGES, class Src>
 __global__ void __launch_bounds__((NCW + 1) * 32)
-    fused_stream_tma(const __grid_constant__ Src src, int units, Partial *__restrict__ partials) {
+    fused_stream_tma(const __grid_constant__ Src src, int units, int warp_records,
+                     Partial *__restrict__ partials) {
     constexpr uint32_t kStageBytes = SV * 16;  // per plane
     constexpr uint32_t kPerThread = SV / (NCW * 32);
     static_assert(SV % (NCW * 32) == 0, "a full stage gives every consumer thread equal work");
@@ -812,20 +835,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         u64 t[6];
         acc.totals(t);
         t[5] |= err;
-        consumer_reduce_store<NCW>(t, red, partials[x.record].v);
+        if (warp_records)
+            warp_reduce_store(t, partials[x.record * NCW + warp].v);
+        else
+            consumer_reduce_store<NCW>(t, red, partials[x.record].v);
     }
 }
 
 // ---------------------------------------------------------------- stage 2
-// One CTA per frame: the frame's segs Partial records, added in a fixed
-// order, written to out[frame] (pinned host memory mapped into the device).
+// One CTA per frame: the frame's per_frame Partial records, added in a
+// fixed order, written to out[frame] (pinned host memory mapped into the
+// device).
 __global__ void __launch_bounds__(kSumThreads)
-    frame_sums(const Partial *__restrict__ partials, int segs, Partial *__restrict__ out) {
+    frame_sums(const Partial *__restrict__ partials, int per_frame, Partial *__restrict__ out) {
     grid_dependency_wait();
     const int f = blockIdx.x;
     u64 t[6] = {0, 0, 0, 0, 0, 0};
-    for (int s = threadIdx.x; s < segs; s += kSumThreads) {
-        const Partial &p = partials[(size_t)f * segs + s];
+    for (int s = threadIdx.x; s < per_frame; s += kSumThreads) {
+        const Partial &p = partials[(size_t)f * per_frame + s];
 #pragma unroll
         for (int k = 0; k < 5; k++) t[k] += p.v[k];
         t[5] |= p.v[5];

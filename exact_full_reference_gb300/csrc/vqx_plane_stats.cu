@@ -237,20 +237,63 @@ void release_pinned(const PinnedBuf &b) {
 // ------------------------------------------------------------------ profiling
 struct Profiler {
     bool on = false;
-    bool events_ready = false;
-    cudaEvent_t ev[3] = {};
     vqx_profile totals = {};
 };
 thread_local Profiler t_prof;
 
-bool profiling_events() {
-    if (!t_prof.on) return false;
-    if (!t_prof.events_ready) {
-        for (auto &e : t_prof.ev)
-            if (cudaEventCreate(&e) != cudaSuccess) return false;
-        t_prof.events_ready = true;
+// ------------------------------------------------------------------ pending batches
+}  // namespace
+
+// A batch enqueued by vqx_plane_stats_submit: its pinned record buffer, the
+// event recorded after its last kernel and, when profiling, timing events.
+// Handles are kept on a per-device free list, events and all.
+struct vqx_pending {
+    PinnedBuf rec;
+    cudaEvent_t done = nullptr;
+    cudaEvent_t ev[3] = {};
+    bool timed = false;
+    DeviceCtx *ctx = nullptr;
+    int n_frames = 0, bpc = 0, width = 0, height = 0;
+};
+
+namespace {
+
+std::mutex g_pending_mu;
+std::vector<vqx_pending *> g_pending_free[kMaxDevices];
+
+int acquire_pending(DeviceCtx *ctx, bool timed, vqx_pending **out) {
+    const size_t d = (size_t)(ctx - g_dev);
+    vqx_pending *p = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_pending_mu);
+        if (!g_pending_free[d].empty()) {
+            p = g_pending_free[d].back();
+            g_pending_free[d].pop_back();
+        }
     }
-    return true;
+    if (!p) {
+        p = new (std::nothrow) vqx_pending;
+        if (!p) return VQX_ENOMEM;
+        p->ctx = ctx;
+        const cudaError_t e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            delete p;
+            return cuda_status(e);
+        }
+    }
+    p->timed = false;
+    if (timed) {
+        p->timed = true;
+        for (auto &e : p->ev)
+            if (!e && cudaEventCreate(&e) != cudaSuccess) p->timed = false;
+    }
+    *out = p;
+    return VQX_OK;
+}
+
+void release_pending(vqx_pending *p) {
+    std::lock_guard<std::mutex> lk(g_pending_mu);
+    g_pending_free[(size_t)(p->ctx - g_dev)].push_back(p);
 }
 
 // ------------------------------------------------------------------ validation
@@ -278,6 +321,7 @@ struct Plan {
     int path = kDense;
     int bpc = 8;
     int segs = 1;
+    int rec_per_unit = 1;    // records a unit writes (one per consumer warp, or one)
     long long resident = 1;  // CTAs of this variant resident on the whole GPU
     uint32_t work = 0;      // 16-byte vectors (dense) or rows per frame
     uint32_t seg_work = 0;  // per segment
@@ -318,34 +362,46 @@ void choose_box(size_t row_bytes, int height, long long max_by, int *elem, int *
     *elem = eb;
 }
 
-// Segments per frame: the grid (frames x segments CTAs) should fill whole
-// waves of resident CTAs, so that no SM idles at the end; among equally full
-// grids the one with fewer waves (bigger segments) wins.
-int choose_segs(long long frames, uint32_t work, uint32_t min_unit, long long resident) {
-    long long max_segs = work / min_unit;
+// Segments per frame.  The frames x segments units run in waves of the
+// resident CTAs, and a unit takes a whole number of pipeline stages, so a
+// launch lasts about waves x (stages per unit + kUnitCost) stage times; the
+// segment count with the fewest wins (ties: fewer units).  unit(s) gives the
+// segment work, the segment count and the stages per unit for s segments
+// asked for (whole bands can give fewer).  max_segs bounds s.
+constexpr double kUnitCost = 0.25;  // a unit's end, in stage times
+
+struct UnitShape {
+    uint32_t seg_work;
+    long long segs, stages;
+};
+
+template <class UnitFn>
+UnitShape choose_segs(long long frames, long long max_segs, long long resident, UnitFn unit) {
     if (max_segs < 1) max_segs = 1;
-    // More than four waves buys no better fill; it only shrinks the units.
-    const long long four_waves = (4 * resident + frames - 1) / frames;
-    if (max_segs > four_waves) max_segs = four_waves;
+    // More than eight waves buys no better fill; it only shrinks the units.
+    const long long eight_waves = (8 * resident + frames - 1) / frames;
+    if (max_segs > eight_waves) max_segs = eight_waves;
     while (max_segs > 1 && frames * max_segs > (1ll << 30)) max_segs /= 2;
-    int best = 1;
-    double best_eff = -1.0;
-    long long best_waves = 0;
+    UnitShape best = unit(1);
+    double best_t = -1.0;
     for (long long s = 1; s <= max_segs; s++) {
-        const long long units = frames * s;
-        const long long waves = (units + resident - 1) / resident;
-        const double eff = (double)units / (double)(waves * resident);
-        if (eff > best_eff + 1e-9 || (eff > best_eff - 1e-9 && waves < best_waves)) {
-            best = (int)s;
-            best_eff = eff;
-            best_waves = waves;
+        const UnitShape u = unit(s);
+        const long long waves = (frames * u.segs + resident - 1) / resident;
+        const double t = (double)waves * ((double)u.stages + kUnitCost);
+        if (best_t < 0 || t < best_t - 1e-9) {
+            best = u;
+            best_t = t;
         }
     }
     return best;
 }
 
+// max_records: at most this many stage-1 records per frame (a caller with a
+// fixed scratch); units then write one record each, and if need be the
+// frames get fewer segments.
 Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width, int height,
-               size_t stride, int bpc, long long frames_per_launch) {
+               size_t stride, int bpc, long long frames_per_launch,
+               long long max_records = 1ll << 40) {
     Plan p;
     p.bpc = bpc;
     p.width = width;
@@ -373,20 +429,38 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
         if (max_by < 1) max_by = 1;
         choose_box(row_bytes, height, max_by, &p.tile_elem, &p.tile_bx, &p.tile_by);
     }
-    // a dense or row-piece unit is at least one pipeline stage, a tile unit
-    // one band of boxes, a scalar row unit one row per warp
-    const uint32_t band = (uint32_t)p.tile_by;
-    const uint32_t stage_rows = (uint32_t)(((size_t)vqx::kTmaStageVecs * 16 + row_bytes - 1) / row_bytes);
-    const uint32_t min_unit = p.path == kDense  ? (uint32_t)vqx::kTmaStageVecs
-                              : p.path == kRows  ? stage_rows
-                              : p.path == kTiles ? band
-                                                 : 8u;
-    p.segs = choose_segs(frames_per_launch, p.work, min_unit, p.resident);
-    p.seg_work = (p.work + (uint32_t)p.segs - 1) / (uint32_t)p.segs;
-    if (p.path == kTiles) {  // whole bands of boxes
-        p.seg_work = (p.seg_work + band - 1) / band * band;
-        p.segs = (int)((p.work + p.seg_work - 1) / p.seg_work);
+    // Stage counts per unit: a dense or row-piece unit is cut into stages of
+    // SV vectors, a tile unit into bands of boxes (segments of whole bands), a
+    // scalar row unit into rows, one per warp (8 warps).
+    const uint32_t sv = (uint32_t)vqx::kTmaStageVecs;
+    const uint32_t band = p.path == kTiles ? (uint32_t)p.tile_by : 1u;
+    const uint32_t tiles_x =
+        p.path == kTiles ? (uint32_t)((row_bytes / (size_t)p.tile_elem + p.tile_bx - 1) / p.tile_bx) : 1u;
+    const uint64_t row_vecs = row_bytes / 16;
+    const uint32_t work = p.work;
+    auto unit = [&](long long asked) {
+        UnitShape u;
+        u.seg_work = (uint32_t)((work + asked - 1) / asked);
+        u.seg_work = (u.seg_work + band - 1) / band * band;
+        u.segs = (work + u.seg_work - 1) / u.seg_work;
+        switch (p.path) {
+        case kDense: u.stages = (u.seg_work + sv - 1) / sv; break;
+        case kRows: u.stages = (long long)(((uint64_t)u.seg_work * row_vecs + sv - 1) / sv); break;
+        case kTiles: u.stages = (long long)(u.seg_work / band) * tiles_x; break;
+        default: u.stages = (u.seg_work + 7) / 8; break;
+        }
+        return u;
+    };
+    // at least half a stage (dense), a band (tiles) or a row per unit
+    long long max_segs = p.path == kDense ? (long long)(2 * (uint64_t)work / sv) : (long long)(work / band);
+    p.rec_per_unit = p.path == kRowsScalar ? 1 : vqx::kTmaWarps;
+    UnitShape u = choose_segs(frames_per_launch, max_segs, p.resident, unit);
+    if (u.segs * p.rec_per_unit > max_records) {
+        p.rec_per_unit = 1;
+        if (u.segs > max_records) u = choose_segs(frames_per_launch, max_records, p.resident, unit);
     }
+    p.segs = (int)u.segs;
+    p.seg_work = u.seg_work;
     return p;
 }
 
@@ -412,7 +486,8 @@ cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned 
     src.bx = p.tile_bx;
     src.by = p.tile_by;
     src.box_vecs = (uint32_t)((size_t)p.tile_bx * p.tile_by * p.tile_elem / 16);
-    return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource>(), src, units, partials);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource>(), src, units,
+                              (int)(p.rec_per_unit > 1), partials);
 }
 
 template <int BPC>
@@ -443,7 +518,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.segs = p.segs;
         src.frame0 = frame0;
         return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::DenseSource>(), src, (int)units,
-                                  partials);
+                                  (int)(p.rec_per_unit > 1), partials);
     }
     if (p.path == kRows) {
         vqx::RowSource src;
@@ -457,7 +532,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.segs = p.segs;
         src.frame0 = frame0;
         return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::RowSource>(), src, (int)units,
-                                  partials);
+                                  (int)(p.rec_per_unit > 1), partials);
     }
     return launch_tiles<BPC>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
 }
@@ -486,7 +561,12 @@ cudaError_t launch_stage2(const Plan &p, int n_frames, const Partial *partials, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, vqx::frame_sums, partials, p.segs, out);
+    return cudaLaunchKernelEx(&cfg, vqx::frame_sums, partials, p.segs * p.rec_per_unit, out);
+}
+
+// Bytes of the stage-1 records of n_frames frames.
+size_t records_bytes(const Plan &p, long long n_frames) {
+    return (size_t)n_frames * (size_t)p.segs * (size_t)p.rec_per_unit * sizeof(Partial);
 }
 
 // ------------------------------------------------------------------ conclusion
@@ -573,52 +653,93 @@ void vqx_profile_read(vqx_profile *out, int reset) {
     if (reset) t_prof.totals = vqx_profile{};
 }
 
-int vqx_plane_stats(const void *ref, const void *dist, int width, int height, size_t stride,
-                    int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out) {
-    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
+                           size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                           vqx_pending **pending) {
+    if (!pending) return VQX_EINVAL;
+    *pending = nullptr;
+    // out is checked by vqx_plane_stats_finish; any non-null pointer passes here
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames,
+                      reinterpret_cast<const vqx_frame_stats *>(pending));
     if (rc != VQX_OK || n_frames == 0) return rc;
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     const Plan plan = make_plan(*ctx, ref, dist, width, height, stride, bpc, n_frames);
 
-    PinnedBuf rec;
-    if ((rc = acquire_pinned((size_t)n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
+    vqx_pending *p = nullptr;
+    if ((rc = acquire_pending(ctx, t_prof.on, &p)) != VQX_OK) return rc;
+    if ((rc = acquire_pinned((size_t)n_frames * sizeof(Partial), &p->rec)) != VQX_OK) {
+        release_pending(p);
+        return rc;
+    }
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)n_frames * plan.segs * sizeof(Partial),
-                                            ctx->pool, st);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, records_bytes(plan, n_frames), ctx->pool, st);
     if (e != cudaSuccess) {
-        release_pinned(rec);
+        release_pinned(p->rec);
+        release_pending(p);
         return cuda_status(e);
     }
     Partial *partials = (Partial *)ws;
-    const bool prof = profiling_events();
-    if (prof) cudaEventRecord(t_prof.ev[0], st);
+    if (p->timed) cudaEventRecord(p->ev[0], st);
     e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st);
-    if (e == cudaSuccess && prof) cudaEventRecord(t_prof.ev[1], st);
-    if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)rec.dev, st);
-    if (e == cudaSuccess && prof) cudaEventRecord(t_prof.ev[2], st);
+    if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[1], st);
+    if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)p->rec.dev, st);
+    if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[2], st);
     const cudaError_t ef = cudaFreeAsync(ws, st);
-    const cudaError_t es = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaEventRecord(p->done, st);
     if (e != cudaSuccess) {
-        release_pinned(rec);
+        // whatever was enqueued finishes before the record buffer is reused
+        cudaStreamSynchronize(st);
+        release_pinned(p->rec);
+        release_pending(p);
         return cuda_status(e);
     }
-    t_prof.totals.calls++;
-    t_prof.totals.kernel_launches += 2;
-    t_prof.totals.stage1_launches += 1;
-    t_prof.totals.stage1_bytes += plane_bytes(width, height, bpc, n_frames);
-    if (prof) {
-        float a = 0.f, b = 0.f;
-        cudaEventElapsedTime(&a, t_prof.ev[0], t_prof.ev[1]);
-        cudaEventElapsedTime(&b, t_prof.ev[1], t_prof.ev[2]);
-        t_prof.totals.stage1_ms += a;
-        t_prof.totals.stage2_ms += b;
+    p->n_frames = n_frames;
+    p->bpc = bpc;
+    p->width = width;
+    p->height = height;
+    *pending = p;
+    return VQX_OK;
+}
+
+int vqx_plane_stats_finish(vqx_pending *p, vqx_frame_stats *out) {
+    if (!p) return VQX_OK;
+    int rc = VQX_OK;
+    const cudaError_t e = cudaEventSynchronize(p->done);
+    if (e != cudaSuccess) {
+        rc = cuda_status(e);
+    } else if (!out) {
+        rc = VQX_EINVAL;
+    } else {
+        t_prof.totals.calls++;
+        t_prof.totals.kernel_launches += 2;
+        t_prof.totals.stage1_launches += 1;
+        t_prof.totals.stage1_bytes += plane_bytes(p->width, p->height, p->bpc, p->n_frames);
+        if (p->timed) {
+            float a = 0.f, b = 0.f;
+            cudaEventElapsedTime(&a, p->ev[0], p->ev[1]);
+            cudaEventElapsedTime(&b, p->ev[1], p->ev[2]);
+            t_prof.totals.stage1_ms += a;
+            t_prof.totals.stage2_ms += b;
+        }
+        rc = conclude_all((const Partial *)p->rec.host, p->n_frames, p->bpc, p->width, p->height,
+                          out);
     }
-    rc = conclude_all((const Partial *)rec.host, n_frames, bpc, width, height, out);
-    release_pinned(rec);
+    release_pinned(p->rec);
+    release_pending(p);
     return rc;
+}
+
+int vqx_plane_stats(const void *ref, const void *dist, int width, int height, size_t stride,
+                    int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    vqx_pending *p = nullptr;
+    rc = vqx_plane_stats_submit(ref, dist, width, height, stride, bpc, n_frames, stream, &p);
+    if (rc != VQX_OK) return rc;
+    return vqx_plane_stats_finish(p, out);
 }
 
 int vqx_plane_stats_host(const void *ref, const void *dist, int width, int height,
@@ -654,7 +775,7 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
     PinnedBuf rec;
     if ((rc = acquire_pinned((size_t)n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
     void *ws = nullptr;
-    const size_t part_bytes = ((size_t)n_frames * plan.segs * sizeof(Partial) + 255) & ~(size_t)255;
+    const size_t part_bytes = (records_bytes(plan, n_frames) + 255) & ~(size_t)255;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, 2 * plane_alloc + part_bytes + 256, ctx->pool, st);
     if (e != cudaSuccess) {
         release_pinned(rec);
@@ -845,14 +966,10 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
     std::call_once(c.once, [&] { c.err = init_noalloc(c, dev); });
     if (c.err != cudaSuccess) return cuda_status(c.err);
 
-    Plan plan = make_plan(c.planning, ref, dist, width, height, stride, bpc, n_frames);
     const long long room = (long long)VQX_NOALLOC_MAX_RECORDS / n_frames - 1;  // >= 1
-    if (plan.segs > room) {
-        plan.segs = (int)room;
-        plan.seg_work = (plan.work + (uint32_t)plan.segs - 1) / (uint32_t)plan.segs;
-    }
+    const Plan plan = make_plan(c.planning, ref, dist, width, height, stride, bpc, n_frames, room);
     Partial *partials = c.scratch;
-    Partial *sums = c.scratch + (size_t)n_frames * plan.segs;
+    Partial *sums = c.scratch + (size_t)n_frames * plan.segs * plan.rec_per_unit;
     cudaStream_t st = (cudaStream_t)stream;
     // Every record is written before it is read, so the scratch needs no
     // clearing between calls.

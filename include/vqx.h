@@ -118,6 +118,35 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
                     int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out);
 
 /*
+ * vqx_plane_stats_submit / vqx_plane_stats_finish: vqx_plane_stats in two
+ * halves, so that a caller can enqueue the next batch before it concludes
+ * this one (the device then runs the next batch's kernels while the host
+ * waits on and concludes this one).
+ *
+ * vqx_plane_stats_submit takes the arguments of vqx_plane_stats without
+ * `out`, checks them (same status codes; on an error nothing is enqueued and
+ * *pending is set to NULL), enqueues the batch's kernels on `stream` and
+ * returns without waiting.  *pending receives a library-owned handle, NULL
+ * for an empty batch.  ref and dist must stay valid and unchanged until
+ * vqx_plane_stats_finish on that handle has returned.
+ *
+ * vqx_plane_stats_finish waits for the batch, writes its n_frames records to
+ * out (host array, caller-owned) exactly as vqx_plane_stats would and
+ * returns that call's status; it releases the handle whatever it returns.
+ * Every handle must be finished exactly once, from any thread, in any order;
+ * a NULL handle (an empty batch) returns VQX_OK and touches nothing.  Device
+ * times (vqx_profile_enable) are recorded if profiling was enabled on the
+ * submitting thread and counted on the finishing thread.
+ */
+typedef struct vqx_pending vqx_pending;
+
+int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
+                           size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                           vqx_pending **pending);
+
+int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out);
+
+/*
  * vqx_plane_stats_host: the same results for planes in host memory.  The
  * frames are copied to the device in chunks on an internal copy stream while
  * earlier chunks are reduced on `stream` (copy and compute overlap); pinned

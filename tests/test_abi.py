@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -80,6 +81,30 @@ def test_argument_errors_need_no_gpu(lib, args, status):
         rc = getattr(so, name)(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
                                a["stride"], a["bpc"], a["n_frames"], None, out)
         assert rc == status, (name, args, rc)
+
+
+@pytest.mark.parametrize("args,status", [(dict(bpc=9), -2), (dict(width=0), -1), (dict(ref=0), -1),
+                                         (dict(stride=2 * 64 + 1), -1), (dict(n_frames=-2), -1)])
+def test_submit_argument_errors_need_no_gpu(lib, args, status):
+    a = dict(ref=FAKE, dist=FAKE, width=64, height=4, stride=128, bpc=16, n_frames=2)
+    a.update(args)
+    so = lib.library()
+    handle = ctypes.c_void_p(1234)
+    rc = so.vqx_plane_stats_submit(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
+                                   a["stride"], a["bpc"], a["n_frames"], None, ctypes.byref(handle))
+    assert rc == status
+    assert handle.value is None  # cleared on every error
+
+
+def test_submit_finish_empty_and_null(lib):
+    so = lib.library()
+    handle = ctypes.c_void_p(1234)
+    assert so.vqx_plane_stats_submit(None, None, 0, 0, 0, 16, 0, None, ctypes.byref(handle)) == 0
+    assert handle.value is None
+    assert so.vqx_plane_stats_finish(None, None) == 0
+    assert so.vqx_plane_stats_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, None) == -1
+    p = lib.vqx_plane_stats_submit(np.zeros((0, 4, 4), np.uint16), np.zeros((0, 4, 4), np.uint16))
+    assert p.finish().size == 0
 
 
 def test_empty_batch_is_ok_without_gpu(lib):

@@ -241,3 +241,43 @@ def test_headline_batch_with_padded_rows(lib, orc):
     w = wl.WORKLOADS["3840x2160_16bit_x32"]
     ref, dist = w.generate(range(8))
     run_case(lib, orc, ref, dist, 16, stride=3840 * 2 + 256)
+
+
+def test_submit_finish_matches_the_blocking_call(lib):
+    """Batches enqueued back to back (on one stream, then on two) and
+    finished in another order give the blocking call's records."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    cases = []
+    for bpc, (n, h, w) in [(16, (4, 540, 960)), (10, (3, 270, 480)), (8, (5, 99, 640))]:
+        dt = np.uint8 if bpc == 8 else np.uint16
+        ref = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+        dist = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+        keep, pr, pd, stride, _ = parity.place(ref, dist)
+        geo = (w, h, stride, bpc, n)
+        cases.append((keep, pr, pd, geo, lib.vqx_plane_stats(pr, pd, *geo)))
+    pend = [lib.vqx_plane_stats_submit(pr, pd, *geo) for _, pr, pd, geo, _ in cases]
+    for k in (2, 0, 1):
+        assert pend[k].finish().tobytes() == cases[k][4].tobytes()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    pend = [lib.vqx_plane_stats_submit(pr, pd, *geo, stream=streams[k % 2])
+            for k, (_, pr, pd, geo, _) in enumerate(cases * 2)]
+    for k in reversed(range(len(pend))):
+        assert pend[k].finish().tobytes() == cases[k % 3][4].tobytes()
+    with pytest.raises(RuntimeError):
+        pend[0].finish()
+
+
+def test_submit_profiles_on_the_finishing_thread(lib):
+    w = wl.WORKLOADS["576x324_8bit_x1"]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    lib.profile_enable(True)
+    lib.profile_read(reset=True)
+    pend = [lib.vqx_plane_stats_submit(pr, pd, 576, 324, stride, 8, 1) for _ in range(4)]
+    for p in pend:
+        p.finish()
+    prof = lib.profile_read(reset=True)
+    lib.profile_enable(False)
+    assert prof["calls"] == 4 and prof["stage1_launches"] == 4 and prof["stage1_ms"] > 0
