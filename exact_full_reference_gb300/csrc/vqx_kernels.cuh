@@ -522,57 +522,64 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 }
 
-// The consumer warps' totals reduced to one record: warp shuffles, one
-// value per warp through shared memory, warp 0.  Only consumer threads take
-// part (named barrier 1), so the producer lane keeps streaming meanwhile.
-template <int NCW>
-__device__ __forceinline__ void consumer_reduce_store(u64 (&t)[6], u64 (*scratch)[6], u64 *dst) {
+// A warp's totals, reduced and spread over its lanes: t[0..4] summed, t[5]
+// ORed.  The sums take a reduce-scatter over eight slots (t[0..4] and three
+// zeros): at each of the first three halvings a lane sends its partner the
+// half of its slots the partner keeps, so 18 shuffles do the work of 60.
+// Afterwards lane L holds the sum of slot (L >> 2) & 7 (in all four lanes of
+// its group); the OR of t[5] (two 32-bit warp reductions) is in every lane.
+struct WarpTotals {
+    u64 sum;    // slot (lane >> 2) & 7
+    u64 flags;  // OR of t[5]
+};
+
+__device__ __forceinline__ WarpTotals warp_reduce_scatter(const u64 (&t)[6]) {
+    const int lane = threadIdx.x & 31;
+    WarpTotals w;
+    w.flags = ((u64)__reduce_or_sync(0xffffffffu, (uint32_t)(t[5] >> 32)) << 32) |
+              __reduce_or_sync(0xffffffffu, (uint32_t)t[5]);
+    const bool up16 = lane & 16, up8 = lane & 8, up4 = lane & 4;
+    u64 a[4];  // lanes below 16: slots 0..3; from 16: slots 4..7 = t[4], 0, 0, 0
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int k = 0; k < 5; k++) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
-        t[5] |= __shfl_xor_sync(0xffffffffu, t[5], o);
+    for (int i = 0; i < 4; i++) {
+        const u64 lo = t[i], hi = i == 0 ? t[4] : 0ull;
+        a[i] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) {
+    u64 b[2];
 #pragma unroll
-        for (int k = 0; k < 6; k++) scratch[warp][k] = t[k];
-    }
-    consumer_sync<NCW>();
-    if (warp == 0) {
-        u64 y[6];
-#pragma unroll
-        for (int k = 0; k < 6; k++) y[k] = lane < NCW ? scratch[lane][k] : 0ull;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int k = 0; k < 5; k++) y[k] += __shfl_xor_sync(0xffffffffu, y[k], o);
-            y[5] |= __shfl_xor_sync(0xffffffffu, y[5], o);
-        }
-        u64 mine = 0;
-#pragma unroll
-        for (int k = 0; k < 6; k++)
-            if (lane == k) mine = y[k];
-        if (lane < 6) dst[lane] = mine;
-    }
-    consumer_sync<NCW>();  // scratch is reused by the next unit
+    for (int i = 0; i < 2; i++)
+        b[i] = (up8 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, up8 ? a[i] : a[2 + i], 8);
+    u64 c = (up4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, up4 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    w.sum = c;
+    return w;
 }
 
-// One warp's totals to one record: warp shuffles, lanes 0..5 store a word
-// each.  No other warp takes part, so no warp waits at the end of a unit.
-__device__ __forceinline__ void warp_reduce_store(u64 (&t)[6], u64 *dst) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int k = 0; k < 5; k++) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
-        t[5] |= __shfl_xor_sync(0xffffffffu, t[5], o);
+// One warp's totals to one record (lanes 0, 4, .., 20 store a word each).
+// No other warp takes part, so no warp waits at the end of a unit.
+__device__ __forceinline__ void warp_reduce_store(const u64 (&t)[6], u64 *dst) {
+    const WarpTotals w = warp_reduce_scatter(t);
+    const int lane = threadIdx.x & 31, slot = (lane >> 2) & 7;
+    if ((lane & 3) == 0 && slot < 6) dst[slot] = slot < 5 ? w.sum : w.flags;
+}
+
+// The consumer warps' totals reduced to one record: each warp's totals
+// through shared memory (warp_reduce_scatter), then lanes 0..5 of warp 0 add
+// (or OR) one word each over the warps.  Only consumer threads take part
+// (named barrier 1), so the producer lane keeps streaming meanwhile.
+template <int NCW>
+__device__ __forceinline__ void consumer_reduce_store(const u64 (&t)[6], u64 (*scratch)[6], u64 *dst) {
+    const WarpTotals w = warp_reduce_scatter(t);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, slot = (lane >> 2) & 7;
+    if ((lane & 3) == 0 && slot < 6) scratch[warp][slot] = slot < 5 ? w.sum : w.flags;
+    consumer_sync<NCW>();
+    if (warp == 0 && lane < 6) {
+        u64 y = 0;
+        for (int k = 0; k < NCW; k++) y = lane < 5 ? y + scratch[k][lane] : (y | scratch[k][lane]);
+        dst[lane] = y;
     }
-    const int lane = threadIdx.x & 31;
-    u64 mine = 0;
-#pragma unroll
-    for (int k = 0; k < 6; k++)
-        if (lane == k) mine = t[k];
-    if (lane < 6) dst[lane] = mine;
+    consumer_sync<NCW>();  // scratch is reused by the next unit
 }
 
 // Where the persistent pipeline's stages come from.  A source maps a unit
@@ -775,6 +782,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 
     if (warp == NCW) {
         if (lane != 0) return;
+        // Launched as a programmatic dependent, this grid may be resident
+        // before the kernel ahead of it on the stream has finished: read
+        // nothing it may still be writing (returns at once otherwise).
+        grid_dependency_wait();
         bool ok = true;
         uint32_t k = 0;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -799,6 +810,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 
     u64 err = 0;
     uint32_t k = 0;
+    bool waited = false;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const typename Src::Unit x = src.unit(u);
         const uint32_t n = src.template stages<SV>(x);
@@ -835,6 +847,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         u64 t[6];
         acc.totals(t);
         t[5] |= err;
+        // The same before the first record store (the kernel ahead may still
+        // read records from this memory).
+        if (!waited) {
+            grid_dependency_wait();
+            waited = true;
+        }
         if (warp_records)
             warp_reduce_store(t, partials[x.record * NCW + warp].v);
         else
@@ -848,6 +866,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 // device).
 __global__ void __launch_bounds__(kSumThreads)
     frame_sums(const Partial *__restrict__ partials, int per_frame, Partial *__restrict__ out) {
+    allow_dependent_launch();  // the next batch's stage 1 may start on free SMs
     grid_dependency_wait();
     const int f = blockIdx.x;
     u64 t[6] = {0, 0, 0, 0, 0, 0};

@@ -492,7 +492,8 @@ cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned 
 
 template <int BPC>
 cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const unsigned char *dist,
-                              int frame0, int frames, Partial *partials, cudaStream_t st) {
+                              int frame0, int frames, Partial *partials, cudaStream_t st,
+                              bool overlap) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     const long long units = (long long)frames * p.segs;
@@ -508,6 +509,13 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     cfg.gridDim = dim3((unsigned)(units < p.resident ? units : p.resident));
     cfg.blockDim = dim3(vqx::kTmaThreads);
     cfg.dynamicSmemBytes = vqx::kTmaSmem;
+    cudaLaunchAttribute attr[1];
+    if (overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     if (p.path == kDense) {
         vqx::DenseSource src;
         src.ref = ref;
@@ -537,15 +545,18 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     return launch_tiles<BPC>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
 }
 
+// overlap: launch the persistent kernels as programmatic dependents of the
+// kernel before them on the stream, so that their CTAs are set up while that
+// kernel finishes; they wait for it before their first load and store.
 cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int frame0,
-                          int frames, Partial *partials, cudaStream_t st) {
+                          int frames, Partial *partials, cudaStream_t st, bool overlap = false) {
     const unsigned char *r = (const unsigned char *)ref;
     const unsigned char *d = (const unsigned char *)dist;
     switch (p.bpc) {
-    case 8: return launch_stage1_bpc<8>(p, r, d, frame0, frames, partials, st);
-    case 10: return launch_stage1_bpc<10>(p, r, d, frame0, frames, partials, st);
-    case 12: return launch_stage1_bpc<12>(p, r, d, frame0, frames, partials, st);
-    default: return launch_stage1_bpc<16>(p, r, d, frame0, frames, partials, st);
+    case 8: return launch_stage1_bpc<8>(p, r, d, frame0, frames, partials, st, overlap);
+    case 10: return launch_stage1_bpc<10>(p, r, d, frame0, frames, partials, st, overlap);
+    case 12: return launch_stage1_bpc<12>(p, r, d, frame0, frames, partials, st, overlap);
+    default: return launch_stage1_bpc<16>(p, r, d, frame0, frames, partials, st, overlap);
     }
 }
 
@@ -682,7 +693,7 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
     }
     Partial *partials = (Partial *)ws;
     if (p->timed) cudaEventRecord(p->ev[0], st);
-    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st);
+    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st, true);
     if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[1], st);
     if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)p->rec.dev, st);
     if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[2], st);
