@@ -368,7 +368,7 @@ void choose_box(size_t row_bytes, int height, long long max_by, int *elem, int *
 // segment count with the fewest wins (ties: fewer units).  unit(s) gives the
 // segment work, the segment count and the stages per unit for s segments
 // asked for (whole bands can give fewer).  max_segs bounds s.
-constexpr double kUnitCost = 0.25;  // a unit's end, in stage times
+constexpr double kUnitCost = 0.35;  // a unit's end, in stage times (measured)
 
 struct UnitShape {
     uint32_t seg_work;
