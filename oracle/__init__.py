@@ -1,4 +1,5 @@
-"""CPU oracle for the fused float_psnr noise and float_moment statistics.
+"""CPU oracle for the fused float_psnr noise and float_moment statistics, and
+for the integer psnr.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference leg of ``bench.py`` may import this package.  The GPU
@@ -40,6 +41,15 @@ UNITS_DTYPE = np.dtype(
     ]
 )
 
+INT_PSNR_DTYPE = np.dtype(
+    [
+        ("sse", "<u8"),
+        ("mse", "<f8"),
+        ("psnr", "<f8"),
+        ("psnr_uncapped", "<f8"),
+    ]
+)
+
 
 class Oracle:
     """ctypes handle on one build of the oracle library (the real one, or a
@@ -53,6 +63,8 @@ class Oracle:
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         lib.vqx_oracle_batch.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
         lib.vqx_oracle_batch.restype = i
+        lib.vqx_oracle_int_psnr_batch.argtypes = [vp, vp, i, i, sz, i, i, vp]
+        lib.vqx_oracle_int_psnr_batch.restype = i
         lib.vqx_oracle_psnr_cap.argtypes = [i]
         lib.vqx_oracle_psnr_cap.restype = ctypes.c_double
         self._lib = lib
@@ -90,6 +102,33 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the arguments (status %d)" % rc)
         return sc, un
+
+    def int_psnr(self, ref, dist, width, height, stride, bpc, n_frames, offset=0):
+        """Integer psnr of ``n_frames`` frames (same layout as ``batch``):
+        an ``INT_PSNR_DTYPE`` array."""
+        ref = np.ascontiguousarray(ref)
+        dist = np.ascontiguousarray(dist)
+        need = offset + (n_frames - 1) * height * stride + (height - 1) * stride + width * (
+            1 if bpc == 8 else 2) if n_frames > 0 else 0
+        if ref.nbytes < need or dist.nbytes < need:
+            raise ValueError("plane buffer smaller than the frame geometry needs")
+        out = np.zeros(n_frames, INT_PSNR_DTYPE)
+        rc = self._lib.vqx_oracle_int_psnr_batch(ref.ctypes.data + offset, dist.ctypes.data + offset,
+                                                 width, height, stride, bpc, n_frames,
+                                                 out.ctypes.data if n_frames else None)
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (status %d)" % rc)
+        return out
+
+    def int_psnr_frames(self, ref, dist, bpc):
+        """Convenience form for dense arrays of shape (n, h, w) or (h, w)."""
+        ref = np.asarray(ref)
+        dist = np.asarray(dist)
+        if ref.ndim == 2:
+            ref = ref[None]
+            dist = dist[None]
+        n, h, w = ref.shape
+        return self.int_psnr(ref, dist, w, h, w * ref.itemsize, bpc, n)
 
     def frames(self, ref, dist, bpc, scores=True, units=True):
         """Convenience form for dense arrays of shape (n, h, w) or (h, w)."""

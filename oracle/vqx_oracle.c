@@ -38,6 +38,9 @@
  * (Decision) and ADR-1447 (Decision) state that these integers, divided by
  * scaler^2 (or scaler), are the CPU's terms and sums.
  *
+ * The integer psnr (vqx_oracle_int_psnr_frame) is stated beside them, with
+ * its own readings.
+ *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fno-tree-vectorize.
  * Contraction must stay off: the pages' CPU reference is a strict build.
  */
@@ -169,6 +172,59 @@ int vqx_oracle_units_frame(const void *ref, const void *dist, int w, int h, size
     out->dist_sum = ds;
     out->ref_sumsq = rss;
     out->dist_sumsq = dss;
+    return VQX_ORACLE_OK;
+}
+
+/*
+ * Integer psnr, the integer sibling of float_psnr.  "ADR-1440: float_psnr_hip
+ * adds its squared differences as integers ..." (Alternatives) names its HIP
+ * twin, psnr_hip, as keeping one uint64 per frame; the pages give no formula
+ * beyond that.  Readings taken (also listed in the design notes):
+ *  - SSE = the sum over pixels of (r - d)^2, raw samples at their own depth,
+ *    in uint64 (exact: at most 2^25 (2^16 - 1)^2 < 2^57);
+ *  - MSE = SSE / (w * h), one double division of the converted SSE;
+ *  - PSNR = 10 log10(peak^2 / MSE), peak = 2^bpc - 1 (the largest sample),
+ *    capped as float_psnr is; +inf uncapped when the SSE is 0.
+ */
+typedef struct {
+    uint64_t sse;
+    double mse, psnr, psnr_uncapped;
+} vqx_oracle_int_psnr;
+
+int vqx_oracle_int_psnr_frame(const void *ref, const void *dist, int w, int h, size_t stride,
+                              int bpc, vqx_oracle_int_psnr *out) {
+    if (!ref || !dist || !out || w <= 0 || h <= 0 || !valid_bpc(bpc)) return VQX_ORACLE_EINVAL;
+    if (stride < (size_t)w * (bpc == 8 ? 1u : 2u)) return VQX_ORACLE_EINVAL;
+    const unsigned char *rp = (const unsigned char *)ref;
+    const unsigned char *dp = (const unsigned char *)dist;
+    uint64_t sse = 0;
+    for (int y = 0; y < h; y++) {
+        const unsigned char *rrow = rp + (size_t)y * stride;
+        const unsigned char *drow = dp + (size_t)y * stride;
+        for (int x = 0; x < w; x++) {
+            const int64_t e = (int64_t)sample_at(rrow, x, bpc) - (int64_t)sample_at(drow, x, bpc);
+            sse += (uint64_t)(e * e);
+        }
+    }
+    out->sse = sse;
+    out->mse = (double)sse / ((double)w * (double)h);
+    const double peak = (double)((1u << bpc) - 1);
+    out->psnr_uncapped = 10.0 * log10(peak * peak / out->mse);
+    const double cap = vqx_oracle_psnr_cap(bpc);
+    out->psnr = out->psnr_uncapped < cap ? out->psnr_uncapped : cap;
+    return VQX_ORACLE_OK;
+}
+
+int vqx_oracle_int_psnr_batch(const void *ref, const void *dist, int w, int h, size_t stride,
+                              int bpc, int n_frames, vqx_oracle_int_psnr *out) {
+    if (n_frames < 0 || (n_frames > 0 && !out)) return VQX_ORACLE_EINVAL;
+    const size_t pitch = (size_t)h * stride;
+    for (int f = 0; f < n_frames; f++) {
+        const int rc = vqx_oracle_int_psnr_frame((const unsigned char *)ref + (size_t)f * pitch,
+                                                 (const unsigned char *)dist + (size_t)f * pitch,
+                                                 w, h, stride, bpc, &out[f]);
+        if (rc != VQX_ORACLE_OK) return rc;
+    }
     return VQX_ORACLE_OK;
 }
 

@@ -303,7 +303,98 @@ def check_noise_limit_2_53(orc):
     assert diff <= _o.mse_bound(N, ex["noise_units"])
 
 
+# ---------------------------------------------------------------- integer psnr
+def int_run(orc, ref, dist, bpc):
+    return orc.int_psnr_frames(ref, dist, bpc)[0]
+
+
+def check_int_psnr_closed_forms(orc):
+    """A constant difference k: SSE = N k^2, and the uncapped PSNR is
+    20 log10((2^bpc - 1) / k) (the peak reading: the largest sample); a
+    PSNR above the cap is capped.  Full-scale differences on many pixels
+    need all 64 bits of the sum (64 (2^16 - 1)^2 > 2^32)."""
+    for bpc in (8, 10, 12, 16):
+        top = (1 << bpc) - 1
+        dt = np.uint8 if bpc == 8 else np.uint16
+        for k in (1, 3, top):
+            h, w = 8, 8
+            ref = np.full((h, w), k, dt) if k == top else np.arange(h * w, dtype=np.int64).reshape(h, w) % (top - k) + k
+            dist = (ref.astype(np.int64) - k).astype(dt)
+            out = int_run(orc, ref.astype(dt), dist, bpc)
+            assert int(out["sse"]) == h * w * k * k, (bpc, k, int(out["sse"]))
+            assert out["mse"] == float(k * k)
+            want = 20.0 * math.log10(top / k)
+            assert abs(out["psnr_uncapped"] - want) <= 1e-12 * max(1.0, want), (bpc, k, out["psnr_uncapped"], want)
+            assert out["psnr"] == min(out["psnr_uncapped"], CAPS[bpc])
+    # one code value in 10^4 pixels at 16 bits: 10 log10(65535^2 * 10^4) dB, capped at 108
+    r = np.zeros((100, 100), np.uint16)
+    r[5, 5] = 1
+    out = int_run(orc, r, np.zeros_like(r), 16)
+    assert int(out["sse"]) == 1 and out["mse"] == 1e-4
+    assert abs(out["psnr_uncapped"] - 10 * math.log10(65535.0 ** 2 * 1e4)) <= 1e-12 * 200
+    assert out["psnr"] == CAPS[16]
+
+
+def check_int_psnr_identical_and_swap(orc):
+    """Identical planes: SSE 0, PSNR at the cap, uncapped infinite; swapping
+    the planes changes nothing."""
+    for bpc in (8, 10, 12, 16):
+        ref, dist = small_random(bpc, 500 + bpc)
+        same = int_run(orc, ref, ref.copy(), bpc)
+        assert int(same["sse"]) == 0 and same["mse"] == 0.0 and same["psnr"] == CAPS[bpc]
+        assert math.isinf(same["psnr_uncapped"]) and same["psnr_uncapped"] > 0
+        a, b = int_run(orc, ref, dist, bpc), int_run(orc, dist, ref, bpc)
+        assert a.tobytes() == b.tobytes()
+
+
+def check_int_psnr_against_float_units(orc):
+    """Up to 12 bits the float square of a difference is the integer square
+    (below 2^24), so the SSE equals float_psnr's exact noise units (pinned on
+    their own above); at 16 bits the SSE exceeds them by the rounding the
+    float squares drop, which the pure-integer rounding gives term by term,
+    and the one-pixel golden values show it (4097^2 - 16785408 = 1)."""
+    for bpc in (8, 10, 12, 16):
+        for seed in range(2):
+            ref, dist = small_random(bpc, 600 + 10 * bpc + seed)
+            _, un = run(orc, ref, dist, bpc)
+            out = int_run(orc, ref, dist, bpc)
+            e2 = ((ref.astype(np.int64) - dist.astype(np.int64)) ** 2).astype(np.uint64)
+            dropped = int((e2 - rne24(e2)).astype(np.int64).sum())
+            assert int(out["sse"]) == int(un[0]["noise_units"]) + dropped, (bpc, seed)
+            if bpc <= 12:
+                assert dropped == 0 and int(out["sse"]) == int(un[0]["noise_units"])
+            n = ref.size
+            assert out["mse"] == correctly_rounded(int(out["sse"]), n)
+    for bpc, r, d, nu, _, _ in (map(int, row) for row in read_table("single_pixel_terms.txt")):
+        dt = np.uint8 if bpc == 8 else np.uint16
+        out = int_run(orc, np.array([[r]], dt), np.array([[d]], dt), bpc)
+        assert int(out["sse"]) == (r - d) ** 2 and (r - d) ** 2 - nu >= 0, (bpc, r, d)
+
+
+def check_int_psnr_layout(orc):
+    """Padded rows and frames of a batch: the padding is never read, and frame
+    f of the batch is the frame alone."""
+    for bpc in (8, 16):
+        bps = 1 if bpc == 8 else 2
+        ref, dist = small_random(bpc, 700 + bpc, h=9, w=13)
+        alone = int_run(orc, ref, dist, bpc)
+        pad = 7 * bps
+        stride = 13 * bps + pad
+        rb = np.full((3, 9, stride), 0xA5, np.uint8)
+        db = np.full((3, 9, stride), 0x5A, np.uint8)
+        for f in range(3):
+            rb[f, :, : 13 * bps] = ref.view(np.uint8).reshape(9, 13 * bps)
+            db[f, :, : 13 * bps] = dist.view(np.uint8).reshape(9, 13 * bps)
+        out = orc.int_psnr(rb, db, 13, 9, stride, bpc, 3)
+        for f in range(3):
+            assert out[f].tobytes() == alone.tobytes()
+
+
 ALL_CHECKS = [
+    check_int_psnr_closed_forms,
+    check_int_psnr_identical_and_swap,
+    check_int_psnr_against_float_units,
+    check_int_psnr_layout,
     check_single_pixel_golden,
     check_psnr_closed_forms,
     check_identical_planes,

@@ -52,14 +52,38 @@ MUTANTS = [
      "10.0 * log10(255.0 * 255.0 / out->mse)",
      "10.0 * log10(1023.0 * 1023.0 / out->mse)"),
     ("no PSNR cap",
-     "out->psnr = out->psnr_uncapped < cap ? out->psnr_uncapped : cap;",
-     "out->psnr = out->psnr_uncapped;"),
+     "out->psnr = out->psnr_uncapped < cap ? out->psnr_uncapped : cap;\n\n    plane_moments",
+     "out->psnr = out->psnr_uncapped;\n\n    plane_moments"),
     ("distorted moments taken from the reference",
      "plane_moments(d, w, h, stride, bpc, &out->dist_mean, &out->dist_meansq);",
      "plane_moments(r, w, h, stride, bpc, &out->dist_mean, &out->dist_meansq);"),
     ("row pitch ignored",
      "const unsigned char *rrow = ref + (size_t)y * stride;",
      "const unsigned char *rrow = ref + (size_t)y * (size_t)w * (bpc == 8 ? 1u : 2u);"),
+    ("integer psnr: peak 2^bpc",
+     "const double peak = (double)((1u << bpc) - 1);",
+     "const double peak = (double)(1u << bpc);"),
+    ("integer psnr: peak 255 at every depth",
+     "const double peak = (double)((1u << bpc) - 1);",
+     "const double peak = 255.0;"),
+    ("integer psnr: 32-bit sum",
+     "uint64_t sse = 0;",
+     "uint32_t sse = 0;"),
+    ("integer psnr: float squares",
+     "sse += (uint64_t)(e * e);",
+     "sse += (uint64_t)((float)e * (float)e);"),
+    ("integer psnr: absolute differences",
+     "sse += (uint64_t)(e * e);",
+     "sse += (uint64_t)(e < 0 ? -e : e);"),
+    ("integer psnr: MSE over n - 1",
+     "out->mse = (double)sse / ((double)w * (double)h);",
+     "out->mse = (double)sse / ((double)w * (double)h - 1.0);"),
+    ("integer psnr: no cap",
+     "out->psnr = out->psnr_uncapped < cap ? out->psnr_uncapped : cap;\n    return VQX_ORACLE_OK;\n}\n\nint vqx_oracle_int_psnr_batch",
+     "out->psnr = out->psnr_uncapped;\n    return VQX_ORACLE_OK;\n}\n\nint vqx_oracle_int_psnr_batch"),
+    ("integer psnr: distorted plane read as the reference",
+     "(int64_t)sample_at(rrow, x, bpc) - (int64_t)sample_at(drow, x, bpc)",
+     "(int64_t)sample_at(rrow, x, bpc) - (int64_t)sample_at(rrow, x, bpc)"),
     ("sample byte order swapped",
      "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return v;",
      "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return (uint16_t)((v >> 8) | (v << 8));"),
