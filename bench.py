@@ -37,6 +37,13 @@ if ROOT not in sys.path:
 
 METRIC = "frame pairs/s and HBM GB/s (fused PSNR+moments), 3840x2160 16-bit, 1 GB300"
 UNIT = "frame pairs/s"
+
+
+def metric_for(op, wlo):
+    if op == "stats":
+        return METRIC
+    return "frame pairs/s and HBM GB/s (integer psnr), %dx%d %d-bit, 1 GB300" % (
+        wlo.width, wlo.height, wlo.bpc)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -51,6 +58,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--op", choices=["stats", "int_psnr"], default="stats",
+                   help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
+                        "the integer psnr (vqx_plane_int_psnr)")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
                    help="write the DRAM traffic record of the fused kernel from an ncu report "
                         "(read here with ncu -i; needs no GPU) and exit")
@@ -250,7 +260,7 @@ def write_traffic_record(report, wlo):
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1):
+def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="stats"):
     """Run the CPU oracle over frames (or bands of ``rows`` rows) of the batch
     on ``cores`` threads until ``seconds`` have passed.  Returns (pairs/s,
     pairs done, elapsed s).  ctypes drops the GIL inside the C calls."""
@@ -266,7 +276,10 @@ def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1):
     def one(k):
         f = k % n
         y0 = (k * 7919) % (h - band + 1) if band < h else 0
-        orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
+        if op == "stats":
+            orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
+        else:
+            orc.int_psnr(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
         return band
 
     done_rows = 0
@@ -295,15 +308,15 @@ def run_reference(args, wlo):
     ref, dist = wlo.generate(frames)
     # size one step so that warm-up plus timed steps take about two minutes
     per_step_s = min(0.5, 120.0 / max(args.steps + args.warmup, 1))
-    rate, _, _ = time_oracle(wlo, ref, dist, 0.0, 1, rows=64)  # one thread, calibration
+    rate, _, _ = time_oracle(wlo, ref, dist, 0.0, 1, rows=64, op=args.op)  # one thread, calibration
     rows_per_s = rate * wlo.height
     rows = int(max(1, min(wlo.height, rows_per_s * per_step_s)))
     for _ in range(args.warmup):
-        time_oracle(wlo, ref, dist, 0.0, cores, rows=rows)
+        time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op)
     t0 = time.perf_counter()
     pairs = 0.0
     for _ in range(args.steps):
-        _, p, _ = time_oracle(wlo, ref, dist, 0.0, cores, rows=rows)
+        _, p, _ = time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op)
         pairs += p
     el = time.perf_counter() - t0
     value = pairs / el
@@ -311,7 +324,7 @@ def run_reference(args, wlo):
               % (cores, rows, wlo.height, wlo.name))
     line = {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": metric_for(args.op, wlo),
         "value": value,
         "unit": UNIT,
         "n_gpus": args.gpus,
@@ -321,7 +334,7 @@ def run_reference(args, wlo):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 terms, f64 sums",
+        "dtype": "f32 terms, f64 sums" if args.op == "stats" else "int64 squares, u64 sums",
         "data": "synthetic",
         "config": {"workload": wlo.name, "frames": wlo.n_frames, "width": wlo.width,
                    "height": wlo.height, "bpc": wlo.bpc, "oracle": "plain C, raster-order double sums"},
@@ -365,23 +378,23 @@ def run_ours(args, wlo):
     torch.cuda.synchronize()
 
     so = vqx.library()
-    out = np.zeros(n, vqx.FRAME_STATS_DTYPE)
+    out = np.zeros(n, vqx.FRAME_STATS_DTYPE if args.op == "stats" else vqx.INT_PSNR_DTYPE)
     out_p = out.ctypes.data
-    call_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh, out_p)
-
-    submit_args = call_args[:-1]
+    submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh)
+    submit_fn = getattr(so, "vqx_plane_%s_submit" % args.op)
+    finish_fn = getattr(so, "vqx_plane_%s_finish" % args.op)
 
     def submit():
         handle = ctypes.c_void_p()
-        rc = so.vqx_plane_stats_submit(*submit_args, ctypes.byref(handle))
+        rc = submit_fn(*submit_args, ctypes.byref(handle))
         if rc != 0:
-            raise RuntimeError("vqx_plane_stats_submit: %s" % vqx.status_string(rc))
+            raise RuntimeError("submit: %s" % vqx.status_string(rc))
         return handle
 
     def finish(handle):
-        rc = so.vqx_plane_stats_finish(handle, out_p)
+        rc = finish_fn(handle, out_p)
         if rc != 0:
-            raise RuntimeError("vqx_plane_stats_finish: %s" % vqx.status_string(rc))
+            raise RuntimeError("finish: %s" % vqx.status_string(rc))
 
     def steps(k):
         """k whole steps, pipelined: batch i + 1 is enqueued before batch i is
@@ -440,19 +453,22 @@ def run_ours(args, wlo):
     avg_ms = prof["stage1_ms"] / launches
     bytes_per_launch = prof["stage1_bytes"] / launches
     achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
-    traffic = recorded_traffic(wlo.name)
+    traffic = recorded_traffic(wlo.name) if args.op == "stats" else None
+    label = KERNEL_LABEL % wlo.bpc
+    if args.op == "int_psnr" and wlo.bpc == 16:
+        label = "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                 "timing": "CUDA events recorded by the library around each launch in a second "
                           "timed region of the same %d steps" % args.steps,
                 "instrumented_region_ms_per_step": inst_ms / args.steps,
-                "kernel": KERNEL_LABEL % wlo.bpc, "avg_launch_us": avg_ms * 1e3,
+                "kernel": label, "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
                 "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
 
     # end to end: planes in pinned host memory, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.op == "stats":
         h_ref = torch.from_numpy(rbytes).pin_memory()
         h_dist = torch.from_numpy(dbytes).pin_memory()
         e2e_out = np.zeros(n, vqx.FRAME_STATS_DTYPE)
@@ -480,14 +496,15 @@ def run_ours(args, wlo):
     if rank == 0 and world == 1 and not args.no_cpu:
         cores = host_cores()
         sub = list(range(min(n, cores)))
-        rate, pairs, el = time_oracle(wlo, ref[sub], dist_np[sub], args.cpu_seconds, cores)
+        rate, pairs, el = time_oracle(wlo, ref[sub], dist_np[sub], args.cpu_seconds, cores,
+                                      op=args.op)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%.1f frame pairs of %s (whole frames, one per thread) in %.1f s"
                          % (pairs, wlo.name, el)}
 
     if rank == 0:
         line = {
-            "metric": METRIC,
+            "metric": metric_for(args.op, wlo),
             "value": value,
             "unit": UNIT,
             "n_gpus": world,
@@ -497,14 +514,16 @@ def run_ours(args, wlo):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "u16 samples, f32 terms, u64 sums",
+            "dtype": ("u%d samples, %s" % (8 if wlo.bpc == 8 else 16,
+                      "f32 terms, u64 sums" if args.op == "stats" else "exact integer squares, u64 sums")),
             "data": "synthetic",
             "hbm_gbs": value * wlo.pair_bytes / 1e9 / world,
             "config": {"workload": wlo.name, "frames_per_gpu": n, "width": w, "height": h,
                        "bpc": wlo.bpc, "batch_bytes": int(rbytes.nbytes + dbytes.nbytes),
-                       "l2": "inputs 1.06 GB per step, larger than the 129 MB L2; no flush",
+                       "l2": "inputs %.2f GB per step, larger than the 129 MB L2; no flush"
+                             % ((rbytes.nbytes + dbytes.nbytes) / 1e9),
                        "pipeline": "batch i + 1 submitted before batch i is finished "
-                                   "(vqx_plane_stats_submit / vqx_plane_stats_finish)",
+                                   "(vqx_plane_%s_submit / _finish)" % args.op,
                        "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e,
             "roofline": roofline,

@@ -49,6 +49,17 @@ FRAME_STATS_DTYPE = np.dtype(
     ]
 )
 
+INT_PSNR_DTYPE = np.dtype(
+    [
+        ("sse", "<u8"),
+        ("flags", "<u4"),
+        ("reserved", "<u4"),
+        ("mse", "<f8"),
+        ("psnr", "<f8"),
+        ("psnr_uncapped", "<f8"),
+    ]
+)
+
 
 class VqxProfile(ctypes.Structure):
     _fields_ = [
@@ -81,14 +92,17 @@ def library():
         lib = ctypes.CDLL(LIB_PATH)
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         for name in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_stats_noalloc",
-                     "vqx_plane_stats_ordered"):
+                     "vqx_plane_stats_ordered", "vqx_plane_int_psnr"):
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
-        lib.vqx_plane_stats_submit.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.POINTER(vp)]
-        lib.vqx_plane_stats_submit.restype = i
-        lib.vqx_plane_stats_finish.argtypes = [vp, vp]
-        lib.vqx_plane_stats_finish.restype = i
+        for kind in ("stats", "int_psnr"):
+            sub = getattr(lib, "vqx_plane_%s_submit" % kind)
+            sub.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.POINTER(vp)]
+            sub.restype = i
+            fin = getattr(lib, "vqx_plane_%s_finish" % kind)
+            fin.argtypes = [vp, vp]
+            fin.restype = i
         lib.vqx_psnr_cap.argtypes = [i]
         lib.vqx_psnr_cap.restype = ctypes.c_double
         lib.vqx_status_string.argtypes = [i]
@@ -163,10 +177,11 @@ def _raise(name, rc):
     raise VqxError(rc, msg)
 
 
-def _call(name, ref, dist, width, height, stride, bpc, n_frames, stream, out, check):
+def _call(name, ref, dist, width, height, stride, bpc, n_frames, stream, out, check,
+          dtype=FRAME_STATS_DTYPE):
     width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
     if out is None:
-        out = np.zeros(max(n_frames, 0), FRAME_STATS_DTYPE)
+        out = np.zeros(max(n_frames, 0), dtype)
     rc = getattr(library(), name)(
         _address(ref), _address(dist), width, height, stride, bpc, n_frames, stream,
         out.ctypes.data if out.size else None)
@@ -193,35 +208,57 @@ class Pending:
     """A batch enqueued by ``vqx_plane_stats_submit``; ``finish()`` waits for
     it and returns its records (call it exactly once)."""
 
-    def __init__(self, handle, n_frames, keep):
+    def __init__(self, handle, n_frames, keep, kind="stats"):
         self._handle = handle
         self.n_frames = n_frames
+        self.kind = kind
         self._keep = keep  # the planes stay referenced until the batch is finished
 
     def finish(self, out=None, check=True):
         if self._handle is False:
             raise RuntimeError("this batch was already finished")
         if out is None:
-            out = np.zeros(self.n_frames, FRAME_STATS_DTYPE)
-        rc = library().vqx_plane_stats_finish(self._handle, out.ctypes.data if out.size else None)
+            out = np.zeros(self.n_frames, FRAME_STATS_DTYPE if self.kind == "stats" else INT_PSNR_DTYPE)
+        name = "vqx_plane_%s_finish" % self.kind
+        rc = getattr(library(), name)(self._handle, out.ctypes.data if out.size else None)
         self._handle, self._keep = False, None
         if check and rc != VQX_OK:
-            _raise("vqx_plane_stats_finish", rc)
+            _raise(name, rc)
         return out if check else (out, rc)
+
+
+def _submit(kind, ref, dist, width, height, stride, bpc, n_frames, stream):
+    width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
+    handle = ctypes.c_void_p()
+    name = "vqx_plane_%s_submit" % kind
+    rc = getattr(library(), name)(_address(ref), _address(dist), width, height, stride, bpc,
+                                  n_frames, _stream_handle(stream), ctypes.byref(handle))
+    if rc != VQX_OK:
+        _raise(name, rc)
+    return Pending(handle.value, max(n_frames, 0), (ref, dist), kind)
 
 
 def vqx_plane_stats_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
                            n_frames=None, stream=None):
     """Enqueue a batch of device planes without waiting; returns a
     ``Pending`` whose ``finish()`` gives what ``vqx_plane_stats`` would."""
-    width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
-    handle = ctypes.c_void_p()
-    rc = library().vqx_plane_stats_submit(_address(ref), _address(dist), width, height, stride,
-                                          bpc, n_frames, _stream_handle(stream),
-                                          ctypes.byref(handle))
-    if rc != VQX_OK:
-        _raise("vqx_plane_stats_submit", rc)
-    return Pending(handle.value, max(n_frames, 0), (ref, dist))
+    return _submit("stats", ref, dist, width, height, stride, bpc, n_frames, stream)
+
+
+def vqx_plane_int_psnr_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
+                              n_frames=None, stream=None):
+    """The same for the integer psnr (``finish()`` gives ``INT_PSNR_DTYPE``)."""
+    return _submit("int_psnr", ref, dist, width, height, stride, bpc, n_frames, stream)
+
+
+def vqx_plane_int_psnr(ref, dist, width=None, height=None, stride=None, bpc=16, n_frames=None,
+                       stream=None, out=None, check=True):
+    """Integer psnr per frame of device-resident planes: the exact SSE of the
+    raw samples, its MSE and the PSNR with peak 2^bpc - 1 (``INT_PSNR_DTYPE``
+    records)."""
+    out, rc = _call("vqx_plane_int_psnr", ref, dist, width, height, stride, bpc, n_frames,
+                    _stream_handle(stream), out, check, INT_PSNR_DTYPE)
+    return out if check else (out, rc)
 
 
 def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16,

@@ -432,6 +432,38 @@ struct TermSums<16> {
     }
 };
 
+// Integer psnr at 16 bits: the exact sum of (r - d)^2 (each below 2^32) in a
+// 64-bit integer.  Per 32-bit word one packed absolute difference gives the
+// two |r - d|, each squared and added by a 64-bit integer multiply-add.  (Up
+// to 12 bits the noise terms of TermSums are these squares already: a square
+// below 2^24 is exact in fp32.)  Slots 1..5 of the record stay 0.
+struct SseSums16 {
+    static constexpr uint32_t kFlushVecs = 1u << 20;  // nothing to flush
+    u64 sse = 0;
+
+    __device__ __forceinline__ void word(uint32_t a, uint32_t b) {
+        const uint32_t d = __vabsdiffu2(a, b);
+        const uint32_t lo = d & 0xffffu, hi = d >> 16;
+        sse += (u64)lo * lo;
+        sse += (u64)hi * hi;
+    }
+    __device__ __forceinline__ void vec(const uint4 &a, const uint4 &b) {
+        word(a.x, b.x);
+        word(a.y, b.y);
+        word(a.z, b.z);
+        word(a.w, b.w);
+    }
+    __device__ __forceinline__ void sample(uint32_t r, uint32_t d) {
+        const uint32_t e = r > d ? r - d : d - r;
+        sse += (u64)e * e;
+    }
+    __device__ __forceinline__ void flush() {}
+    __device__ __forceinline__ void totals(u64 (&t)[6]) {
+        t[0] = sse;
+        t[1] = t[2] = t[3] = t[4] = t[5] = 0;
+    }
+};
+
 // ---------------------------------------------------------------- reduction
 // Warp shuffles, then one value per warp through shared memory, then warp 0.
 // Integer sums: exact and independent of the order.
@@ -474,7 +506,7 @@ __device__ __forceinline__ void block_reduce_store(u64 (&t)[6], u64 *dst) {
 // min((s + 1) * seg_rows, height)).  A warp walks one row at a time.  With
 // VEC, rows start 16-byte aligned and are read as 16-byte vectors plus a
 // scalar tail; without, every sample is read on its own.
-template <int BPC, bool VEC>
+template <int BPC, bool VEC, class Acc = TermSums<BPC>>
 __global__ void __launch_bounds__(kThreads)
     fused_rows(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
                size_t frame_pitch, size_t stride, int width, int height, int seg_rows, int segs,
@@ -490,7 +522,7 @@ __global__ void __launch_bounds__(kThreads)
     const unsigned char *rf = ref + (size_t)f * frame_pitch;
     const unsigned char *df = dist + (size_t)f * frame_pitch;
 
-    TermSums<BPC> acc;
+    Acc acc;
     for (int y = y0 + warp; y < y1; y += kThreads / 32) {
         const unsigned char *rr = rf + (size_t)y * stride;
         const unsigned char *dr = df + (size_t)y * stride;
@@ -498,7 +530,7 @@ __global__ void __launch_bounds__(kThreads)
         if constexpr (VEC) {
             const int nvec = (width * kBps) >> 4;
             for (int c = lane; c < nvec;) {
-                const int stop = min(nvec, c + (int)TermSums<BPC>::kFlushVecs * 32);
+                const int stop = min(nvec, c + (int)Acc::kFlushVecs * 32);
                 for (; c < stop; c += 32)
                     acc.vec(ld_stream16(rr + 16 * (size_t)c), ld_stream16(dr + 16 * (size_t)c));
                 acc.flush();
@@ -506,7 +538,7 @@ __global__ void __launch_bounds__(kThreads)
             x0 = nvec * (16 / kBps);
         }
         for (int x = x0 + lane; x < width;) {
-            const int stop = min(width, x + (int)TermSums<BPC>::kFlushVecs * 32);
+            const int stop = min(width, x + (int)Acc::kFlushVecs * 32);
             for (; x < stop; x += 32) acc.sample(ld_sample<BPC>(rr, x), ld_sample<BPC>(dr, x));
             acc.flush();
         }
@@ -754,15 +786,15 @@ struct TileSource {
 // each unit (record r of the source becomes records r * NCW .. r * NCW +
 // NCW - 1) and ends a unit without waiting for the others; otherwise the
 // consumers reduce to one record per unit through shared memory.
-template <int BPC, int NCW, int SV, int STAGES, class Src>
+template <int BPC, int NCW, int SV, int STAGES, class Src, class Acc = TermSums<BPC>>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     fused_stream_tma(const __grid_constant__ Src src, int units, int warp_records,
                      Partial *__restrict__ partials) {
     constexpr uint32_t kStageBytes = SV * 16;  // per plane
     constexpr uint32_t kPerThread = SV / (NCW * 32);
     static_assert(SV % (NCW * 32) == 0, "a full stage gives every consumer thread equal work");
-    static_assert(kPerThread <= TermSums<BPC>::kFlushVecs, "flush at least once per stage");
-    constexpr uint32_t kStagesPerFlush = TermSums<BPC>::kFlushVecs / kPerThread;
+    static_assert(kPerThread <= Acc::kFlushVecs, "flush at least once per stage");
+    constexpr uint32_t kStagesPerFlush = Acc::kFlushVecs / kPerThread;
     extern __shared__ __align__(128) unsigned char ring[];  // [STAGES][2][kStageBytes]
     __shared__ __align__(8) u64 full[STAGES], empty[STAGES];
     __shared__ u64 red[NCW][6];
@@ -814,7 +846,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const typename Src::Unit x = src.unit(u);
         const uint32_t n = src.template stages<SV>(x);
-        TermSums<BPC> acc;
+        Acc acc;
         uint32_t since_flush = 0;
         for (uint32_t j = 0; j < n; j++, k++) {
             if (err) continue;  // a wait of this warp timed out: skip, write flagged records

@@ -47,7 +47,16 @@ int cuda_status(cudaError_t e) {
 enum Path { kDense = 0, kTiles = 1, kRowsScalar = 2, kRows = 3, kPaths = 4 };
 constexpr size_t kRowsMinBytes = 512;
 
-int bpc_index(int bpc) { return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3; }
+// What a call computes: the fused statistics, or the integer psnr.  Up to 12
+// bits the integer psnr's SSE is the fused pass's noise sum (its squares are
+// exact), so only 16 bits has a kernel variant of its own.
+enum Kind { kStats = 0, kIntPsnr = 1 };
+constexpr int kVariants = 5;  // fused 8, 10, 12, 16 bits; integer psnr 16 bits
+
+int variant_index(int bpc, int kind) {
+    if (kind == kIntPsnr && bpc == 16) return 4;
+    return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3;
+}
 
 // Kernel, CTA size and dynamic shared memory of each stage-1 variant.
 struct Stage1Shape {
@@ -56,21 +65,24 @@ struct Stage1Shape {
     size_t smem;
 };
 
-template <int BPC, class Src>
+template <int BPC, class Src, class Acc>
 constexpr auto stream_kernel() {
-    return vqx::fused_stream_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages, Src>;
+    return vqx::fused_stream_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages, Src, Acc>;
 }
 
-template <int BPC>
+template <int BPC, class Acc>
 Stage1Shape stage1_shape(int path) {
     switch (path) {
     case kDense:
-        return {(const void *)stream_kernel<BPC, vqx::DenseSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
+        return {(const void *)stream_kernel<BPC, vqx::DenseSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
     case kTiles:
-        return {(const void *)stream_kernel<BPC, vqx::TileSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
+        return {(const void *)stream_kernel<BPC, vqx::TileSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
     case kRows:
-        return {(const void *)stream_kernel<BPC, vqx::RowSource>(), vqx::kTmaThreads, vqx::kTmaSmem};
-    default: return {(const void *)vqx::fused_rows<BPC, false>, vqx::kThreads, 0};
+        return {(const void *)stream_kernel<BPC, vqx::RowSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
+    default: return {(const void *)vqx::fused_rows<BPC, false, Acc>, vqx::kThreads, 0};
     }
 }
 
@@ -117,22 +129,22 @@ cudaError_t encode_planes(CUtensorMap *tm, const void *base, int elem_bytes, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-Stage1Shape stage1_shape(int path, int bpc) {
-    switch (bpc) {
-    case 8: return stage1_shape<8>(path);
-    case 10: return stage1_shape<10>(path);
-    case 12: return stage1_shape<12>(path);
-    default: return stage1_shape<16>(path);
+Stage1Shape stage1_shape(int path, int variant) {
+    switch (variant) {
+    case 0: return stage1_shape<8, vqx::TermSums<8>>(path);
+    case 1: return stage1_shape<10, vqx::TermSums<10>>(path);
+    case 2: return stage1_shape<12, vqx::TermSums<12>>(path);
+    case 3: return stage1_shape<16, vqx::TermSums<16>>(path);
+    default: return stage1_shape<16, vqx::SseSums16>(path);
     }
 }
 
 // Per device: allow the dense kernels their shared-memory ring and count
 // the CTAs of each variant that fit on one SM.
-cudaError_t prepare_stage1(int (&resident)[kPaths][4]) {
-    const int bpcs[4] = {8, 10, 12, 16};
+cudaError_t prepare_stage1(int (&resident)[kPaths][kVariants]) {
     for (int p = 0; p < kPaths; p++)
-        for (int b = 0; b < 4; b++) {
-            const Stage1Shape sh = stage1_shape(p, bpcs[b]);
+        for (int b = 0; b < kVariants; b++) {
+            const Stage1Shape sh = stage1_shape(p, b);
             cudaError_t e = cudaSuccess;
             if (sh.smem > 48 * 1024)
                 e = cudaFuncSetAttribute(sh.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -155,7 +167,7 @@ struct DeviceCtx {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     int sms = 0;
-    int resident[kPaths][4] = {};
+    int resident[kPaths][kVariants] = {};
     cudaMemPool_t pool = nullptr;
     cudaStream_t copy_stream = nullptr;
 };
@@ -253,6 +265,7 @@ struct vqx_pending {
     cudaEvent_t ev[3] = {};
     bool timed = false;
     DeviceCtx *ctx = nullptr;
+    int kind = 0;  // Kind: what the batch computes
     int n_frames = 0, bpc = 0, width = 0, height = 0;
 };
 
@@ -320,6 +333,7 @@ int validate(const void *ref, const void *dist, int width, int height, size_t st
 struct Plan {
     int path = kDense;
     int bpc = 8;
+    int variant = 0;         // variant_index(bpc, kind)
     int segs = 1;
     int rec_per_unit = 1;    // records a unit writes (one per consumer warp, or one)
     long long resident = 1;  // CTAs of this variant resident on the whole GPU
@@ -400,10 +414,11 @@ UnitShape choose_segs(long long frames, long long max_segs, long long resident, 
 // fixed scratch); units then write one record each, and if need be the
 // frames get fewer segments.
 Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width, int height,
-               size_t stride, int bpc, long long frames_per_launch,
+               size_t stride, int bpc, long long frames_per_launch, int kind = kStats,
                long long max_records = 1ll << 40) {
     Plan p;
     p.bpc = bpc;
+    p.variant = variant_index(bpc, kind);
     p.width = width;
     p.height = height;
     p.stride = stride;
@@ -422,7 +437,7 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
                                                                                   : kRowsScalar;
         p.work = (uint32_t)height;
     }
-    p.resident = (long long)c.sms * c.resident[p.path][bpc_index(bpc)];
+    p.resident = (long long)c.sms * c.resident[p.path][p.variant];
     if (p.path == kTiles) {
         // rows per CTA were the batch spread over every resident CTA
         long long max_by = (long long)height * frames_per_launch / (p.resident > 0 ? p.resident : 1);
@@ -464,7 +479,7 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
     return p;
 }
 
-template <int BPC>
+template <int BPC, class Acc>
 cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned char *ref,
                          const unsigned char *dist, int frame0, int frames, int units,
                          Partial *partials) {
@@ -486,11 +501,11 @@ cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned 
     src.bx = p.tile_bx;
     src.by = p.tile_by;
     src.box_vecs = (uint32_t)((size_t)p.tile_bx * p.tile_by * p.tile_elem / 16);
-    return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource>(), src, units,
+    return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource, Acc>(), src, units,
                               (int)(p.rec_per_unit > 1), partials);
 }
 
-template <int BPC>
+template <int BPC, class Acc>
 cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const unsigned char *dist,
                               int frame0, int frames, Partial *partials, cudaStream_t st,
                               bool overlap) {
@@ -501,7 +516,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     if (p.path == kRowsScalar) {
         cfg.gridDim = dim3((unsigned)units);
         cfg.blockDim = dim3(vqx::kThreads);
-        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false>, ref, dist, p.frame_pitch,
+        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false, Acc>, ref, dist, p.frame_pitch,
                                   p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
                                   partials);
     }
@@ -525,7 +540,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.seg_vecs = p.seg_work;
         src.segs = p.segs;
         src.frame0 = frame0;
-        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::DenseSource>(), src, (int)units,
+        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::DenseSource, Acc>(), src, (int)units,
                                   (int)(p.rec_per_unit > 1), partials);
     }
     if (p.path == kRows) {
@@ -539,10 +554,10 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.seg_rows = (int)p.seg_work;
         src.segs = p.segs;
         src.frame0 = frame0;
-        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::RowSource>(), src, (int)units,
+        return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::RowSource, Acc>(), src, (int)units,
                                   (int)(p.rec_per_unit > 1), partials);
     }
-    return launch_tiles<BPC>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
+    return launch_tiles<BPC, Acc>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
 }
 
 // overlap: launch the persistent kernels as programmatic dependents of the
@@ -552,11 +567,12 @@ cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int 
                           int frames, Partial *partials, cudaStream_t st, bool overlap = false) {
     const unsigned char *r = (const unsigned char *)ref;
     const unsigned char *d = (const unsigned char *)dist;
-    switch (p.bpc) {
-    case 8: return launch_stage1_bpc<8>(p, r, d, frame0, frames, partials, st, overlap);
-    case 10: return launch_stage1_bpc<10>(p, r, d, frame0, frames, partials, st, overlap);
-    case 12: return launch_stage1_bpc<12>(p, r, d, frame0, frames, partials, st, overlap);
-    default: return launch_stage1_bpc<16>(p, r, d, frame0, frames, partials, st, overlap);
+    switch (p.variant) {
+    case 0: return launch_stage1_bpc<8, vqx::TermSums<8>>(p, r, d, frame0, frames, partials, st, overlap);
+    case 1: return launch_stage1_bpc<10, vqx::TermSums<10>>(p, r, d, frame0, frames, partials, st, overlap);
+    case 2: return launch_stage1_bpc<12, vqx::TermSums<12>>(p, r, d, frame0, frames, partials, st, overlap);
+    case 3: return launch_stage1_bpc<16, vqx::TermSums<16>>(p, r, d, frame0, frames, partials, st, overlap);
+    default: return launch_stage1_bpc<16, vqx::SseSums16>(p, r, d, frame0, frames, partials, st, overlap);
     }
 }
 
@@ -581,6 +597,14 @@ size_t records_bytes(const Plan &p, long long n_frames) {
 }
 
 // ------------------------------------------------------------------ conclusion
+// The flags of a record: a sample at or above 2^bpc, a device wait that
+// timed out.
+uint32_t record_flags(const Partial &s, int bpc) {
+    uint32_t flags = ((s.v[5] & 0xffffffffull) >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
+    if (s.v[5] & vqx::kErrTimeout) flags |= VQX_FLAG_TIMEOUT;
+    return flags;
+}
+
 // cpu, when given, holds the CPU's sequential double sums (noise, reference
 // squares, distorted squares) in units, replayed on the device; otherwise
 // the exact integer sums are rounded once.
@@ -594,8 +618,7 @@ void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats 
     o->dist_sum = s.v[2];
     o->ref_sumsq = s.v[3];
     o->dist_sumsq = s.v[4];
-    o->flags = ((s.v[5] & 0xffffffffull) >> bpc) != 0 ? VQX_FLAG_RANGE : 0u;
-    if (s.v[5] & vqx::kErrTimeout) o->flags |= VQX_FLAG_TIMEOUT;
+    o->flags = record_flags(s, bpc);
     o->reserved = 0;
     o->noise = (double)(cpu ? cpu[0] : s.v[0]) / S2;
     o->mse = o->noise / n;
@@ -610,10 +633,28 @@ void conclude(const Partial &s, int bpc, int width, int height, vqx_frame_stats 
 
 // The call's status from the frames' flags: a timed-out device wait first
 // (its sums are incomplete), then an out-of-range sample.
-int merge_status(int rc, const vqx_frame_stats &f) {
-    if (f.flags & VQX_FLAG_TIMEOUT) return VQX_ETIMEOUT;
-    if ((f.flags & VQX_FLAG_RANGE) && rc == VQX_OK) return VQX_ERANGE;
+int merge_status_flags(int rc, uint32_t flags) {
+    if (flags & VQX_FLAG_TIMEOUT) return VQX_ETIMEOUT;
+    if ((flags & VQX_FLAG_RANGE) && rc == VQX_OK) return VQX_ERANGE;
     return rc;
+}
+
+int merge_status(int rc, const vqx_frame_stats &f) { return merge_status_flags(rc, f.flags); }
+
+// Integer psnr of one frame from its record: slot 0 is the exact SSE (the
+// integer-psnr kernel's sum at 16 bits, the fused pass's noise sum below,
+// where the float squares are the integer squares).  MSE = SSE / N, one
+// division; PSNR = 10 log10(peak^2 / MSE), peak = 2^bpc - 1, capped as
+// float_psnr is.
+void conclude_int_psnr(const Partial &s, int bpc, int width, int height, vqx_int_psnr_stats *o) {
+    o->sse = s.v[0];
+    o->flags = record_flags(s, bpc);
+    o->reserved = 0;
+    o->mse = (double)s.v[0] / ((double)width * (double)height);
+    const double peak = (double)((1u << bpc) - 1);
+    o->psnr_uncapped = 10.0 * log10(peak * peak / o->mse);
+    const double cap = vqx_psnr_cap(bpc);
+    o->psnr = o->psnr_uncapped < cap ? o->psnr_uncapped : cap;
 }
 
 int conclude_all(const Partial *sums, int n_frames, int bpc, int width, int height,
@@ -664,9 +705,12 @@ void vqx_profile_read(vqx_profile *out, int reset) {
     if (reset) t_prof.totals = vqx_profile{};
 }
 
-int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
-                           size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                           vqx_pending **pending) {
+}  // extern "C"
+
+namespace {
+
+int submit_impl(const void *ref, const void *dist, int width, int height, size_t stride, int bpc,
+                int n_frames, vqx_stream_t stream, int kind, vqx_pending **pending) {
     if (!pending) return VQX_EINVAL;
     *pending = nullptr;
     // out is checked by vqx_plane_stats_finish; any non-null pointer passes here
@@ -676,7 +720,7 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    const Plan plan = make_plan(*ctx, ref, dist, width, height, stride, bpc, n_frames);
+    const Plan plan = make_plan(*ctx, ref, dist, width, height, stride, bpc, n_frames, kind);
 
     vqx_pending *p = nullptr;
     if ((rc = acquire_pending(ctx, t_prof.on, &p)) != VQX_OK) return rc;
@@ -707,6 +751,7 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
         release_pending(p);
         return cuda_status(e);
     }
+    p->kind = kind;
     p->n_frames = n_frames;
     p->bpc = bpc;
     p->width = width;
@@ -715,13 +760,15 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
     return VQX_OK;
 }
 
-int vqx_plane_stats_finish(vqx_pending *p, vqx_frame_stats *out) {
+// Waits for a batch, concludes it into out (vqx_frame_stats or
+// vqx_int_psnr_stats records, as kind says) and releases the handle.
+int finish_impl(vqx_pending *p, int kind, void *out) {
     if (!p) return VQX_OK;
     int rc = VQX_OK;
     const cudaError_t e = cudaEventSynchronize(p->done);
     if (e != cudaSuccess) {
         rc = cuda_status(e);
-    } else if (!out) {
+    } else if (!out || p->kind != kind) {
         rc = VQX_EINVAL;
     } else {
         t_prof.totals.calls++;
@@ -735,13 +782,58 @@ int vqx_plane_stats_finish(vqx_pending *p, vqx_frame_stats *out) {
             t_prof.totals.stage1_ms += a;
             t_prof.totals.stage2_ms += b;
         }
-        rc = conclude_all((const Partial *)p->rec.host, p->n_frames, p->bpc, p->width, p->height,
-                          out);
+        const Partial *sums = (const Partial *)p->rec.host;
+        if (kind == kStats) {
+            rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
+        } else {
+            vqx_int_psnr_stats *o = (vqx_int_psnr_stats *)out;
+            for (int f = 0; f < p->n_frames; f++) {
+                conclude_int_psnr(sums[f], p->bpc, p->width, p->height, &o[f]);
+                rc = merge_status_flags(rc, o[f].flags);
+            }
+        }
     }
     release_pinned(p->rec);
     release_pending(p);
     return rc;
 }
+
+}  // namespace
+
+extern "C" {
+
+int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
+                           size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                           vqx_pending **pending) {
+    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kStats, pending);
+}
+
+int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out) {
+    return finish_impl(pending, kStats, out);
+}
+
+int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int height,
+                              size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                              vqx_pending **pending) {
+    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr,
+                       pending);
+}
+
+int vqx_plane_int_psnr_finish(vqx_pending *pending, vqx_int_psnr_stats *out) {
+    return finish_impl(pending, kIntPsnr, out);
+}
+
+int vqx_plane_int_psnr(const void *ref, const void *dist, int width, int height, size_t stride,
+                       int bpc, int n_frames, vqx_stream_t stream, vqx_int_psnr_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames,
+                      reinterpret_cast<const vqx_frame_stats *>(out));
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    vqx_pending *p = nullptr;
+    rc = submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr, &p);
+    if (rc != VQX_OK) return rc;
+    return finish_impl(p, kIntPsnr, out);
+}
+
 
 int vqx_plane_stats(const void *ref, const void *dist, int width, int height, size_t stride,
                     int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out) {
@@ -978,7 +1070,8 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
     if (c.err != cudaSuccess) return cuda_status(c.err);
 
     const long long room = (long long)VQX_NOALLOC_MAX_RECORDS / n_frames - 1;  // >= 1
-    const Plan plan = make_plan(c.planning, ref, dist, width, height, stride, bpc, n_frames, room);
+    const Plan plan =
+        make_plan(c.planning, ref, dist, width, height, stride, bpc, n_frames, kStats, room);
     Partial *partials = c.scratch;
     Partial *sums = c.scratch + (size_t)n_frames * plan.segs * plan.rec_per_unit;
     cudaStream_t st = (cudaStream_t)stream;

@@ -147,6 +147,39 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
 int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out);
 
 /*
+ * Integer psnr of one frame pair: the integer sibling of float_psnr.
+ * "ADR-1440: float_psnr_hip adds its squared differences as integers ..."
+ * (Alternatives) names psnr_hip as keeping one uint64 per frame; the pages
+ * give no more of it, so the conclusion below is a stated reading.
+ */
+typedef struct {
+    uint64_t sse;         /* sum over pixels of (r - d)^2, raw samples, exact */
+    uint32_t flags;       /* VQX_FLAG_* as in vqx_frame_stats */
+    uint32_t reserved;    /* 0 */
+    double mse;           /* sse / (width * height), at the samples' own scale */
+    double psnr;          /* min(psnr_uncapped, vqx_psnr_cap(bpc)) */
+    double psnr_uncapped; /* 10 log10((2^bpc - 1)^2 / mse); +inf when sse == 0 */
+} vqx_int_psnr_stats;     /* 40 bytes */
+
+/*
+ * vqx_plane_int_psnr: the integer psnr of every frame of a batch of
+ * device-resident planes.  Arguments, layout, ownership and status codes as
+ * for vqx_plane_stats, with out an array of n_frames vqx_int_psnr_stats.  The
+ * SSE is exact at every depth (at most 2^25 * (2^16 - 1)^2 < 2^57); mse is
+ * its one correctly rounded division by the pixel count.
+ */
+int vqx_plane_int_psnr(const void *ref, const void *dist, int width, int height, size_t stride,
+                       int bpc, int n_frames, vqx_stream_t stream, vqx_int_psnr_stats *out);
+
+/* The same in two halves, as vqx_plane_stats_submit / _finish (a handle
+ * from one pair is not accepted by the other: VQX_EINVAL, handle released). */
+int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int height,
+                              size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                              vqx_pending **pending);
+
+int vqx_plane_int_psnr_finish(vqx_pending *pending, vqx_int_psnr_stats *out);
+
+/*
  * vqx_plane_stats_host: the same results for planes in host memory.  The
  * frames are copied to the device in chunks on an internal copy stream while
  * earlier chunks are reduced on `stream` (copy and compute overlap); pinned

@@ -25,7 +25,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_status_string",
+    for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr",
+              "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
               "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
         assert n in names
 
@@ -77,7 +78,7 @@ def test_argument_errors_need_no_gpu(lib, args, status):
     a.update(args)
     out = (ctypes.c_char * (152 * 4))()
     so = lib.library()
-    for name in ("vqx_plane_stats", "vqx_plane_stats_host"):
+    for name in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr"):
         rc = getattr(so, name)(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
                                a["stride"], a["bpc"], a["n_frames"], None, out)
         assert rc == status, (name, args, rc)
@@ -103,6 +104,9 @@ def test_submit_finish_empty_and_null(lib):
     assert handle.value is None
     assert so.vqx_plane_stats_finish(None, None) == 0
     assert so.vqx_plane_stats_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, None) == -1
+    assert so.vqx_plane_int_psnr_submit(None, None, 0, 0, 0, 12, 0, None, ctypes.byref(handle)) == 0
+    assert handle.value is None and so.vqx_plane_int_psnr_finish(None, None) == 0
+    assert so.vqx_plane_int_psnr(None, None, 0, 0, 0, 8, 0, None, None) == 0
     p = lib.vqx_plane_stats_submit(np.zeros((0, 4, 4), np.uint16), np.zeros((0, 4, 4), np.uint16))
     assert p.finish().size == 0
 
@@ -121,6 +125,8 @@ def test_null_output_rejected(lib):
 def test_record_layout_matches_header(lib):
     # 5 uint64 + 2 uint32 + 8 doubles = 112 bytes, no padding
     assert lib.FRAME_STATS_DTYPE.itemsize == 112
+    # 1 uint64 + 2 uint32 + 3 doubles = 40 bytes
+    assert lib.INT_PSNR_DTYPE.itemsize == 40
     assert ctypes.sizeof(lib.VqxProfile) == 48
 
 
