@@ -42,8 +42,9 @@ UNIT = "frame pairs/s"
 def metric_for(op, wlo):
     if op == "stats":
         return METRIC
-    return "frame pairs/s and HBM GB/s (integer psnr), %dx%d %d-bit, 1 GB300" % (
-        wlo.width, wlo.height, wlo.bpc)
+    what = "integer psnr" if op == "int_psnr" else "fused PSNR+moments, CPU-order replay"
+    return "frame pairs/s and HBM GB/s (%s), %dx%d %d-bit, 1 GB300" % (
+        what, wlo.width, wlo.height, wlo.bpc)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -58,9 +59,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["stats", "int_psnr"], default="stats",
+    p.add_argument("--op", choices=["stats", "int_psnr", "ordered"], default="stats",
                    help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
-                        "the integer psnr (vqx_plane_int_psnr)")
+                        "the integer psnr (vqx_plane_int_psnr); ordered: the CPU-order replay "
+                        "past 2^53 units (vqx_plane_stats_ordered, one blocking call a step)")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
                    help="write the DRAM traffic record of the fused kernel from an ncu report "
                         "(read here with ncu -i; needs no GPU) and exit")
@@ -276,7 +278,7 @@ def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="sta
     def one(k):
         f = k % n
         y0 = (k * 7919) % (h - band + 1) if band < h else 0
-        if op == "stats":
+        if op != "int_psnr":
             orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
         else:
             orc.int_psnr(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
@@ -334,7 +336,7 @@ def run_reference(args, wlo):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 terms, f64 sums" if args.op == "stats" else "int64 squares, u64 sums",
+        "dtype": "int64 squares, u64 sums" if args.op == "int_psnr" else "f32 terms, f64 sums",
         "data": "synthetic",
         "config": {"workload": wlo.name, "frames": wlo.n_frames, "width": wlo.width,
                    "height": wlo.height, "bpc": wlo.bpc, "oracle": "plain C, raster-order double sums"},
@@ -378,11 +380,19 @@ def run_ours(args, wlo):
     torch.cuda.synchronize()
 
     so = vqx.library()
-    out = np.zeros(n, vqx.FRAME_STATS_DTYPE if args.op == "stats" else vqx.INT_PSNR_DTYPE)
+    out = np.zeros(n, vqx.INT_PSNR_DTYPE if args.op == "int_psnr" else vqx.FRAME_STATS_DTYPE)
     out_p = out.ctypes.data
     submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh)
-    submit_fn = getattr(so, "vqx_plane_%s_submit" % args.op)
-    finish_fn = getattr(so, "vqx_plane_%s_finish" % args.op)
+    if args.op == "ordered":
+        # a blocking call per step: submit runs it, finish has nothing left to do
+        def submit_fn(*a):
+            return so.vqx_plane_stats_ordered(*a[:-1], out_p)
+
+        def finish_fn(handle, out_ptr):
+            return 0
+    else:
+        submit_fn = getattr(so, "vqx_plane_%s_submit" % args.op)
+        finish_fn = getattr(so, "vqx_plane_%s_finish" % args.op)
 
     def submit():
         handle = ctypes.c_void_p()
@@ -457,6 +467,8 @@ def run_ours(args, wlo):
     label = KERNEL_LABEL % wlo.bpc
     if args.op == "int_psnr" and wlo.bpc == 16:
         label = "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
+    if args.op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
+        label = "ordered_block_sums"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                 "timing": "CUDA events recorded by the library around each launch in a second "
@@ -522,8 +534,10 @@ def run_ours(args, wlo):
                        "bpc": wlo.bpc, "batch_bytes": int(rbytes.nbytes + dbytes.nbytes),
                        "l2": "inputs %.2f GB per step, larger than the 129 MB L2; no flush"
                              % ((rbytes.nbytes + dbytes.nbytes) / 1e9),
-                       "pipeline": "batch i + 1 submitted before batch i is finished "
-                                   "(vqx_plane_%s_submit / _finish)" % args.op,
+                       "pipeline": ("one blocking vqx_plane_stats_ordered call a step"
+                                    if args.op == "ordered" else
+                                    "batch i + 1 submitted before batch i is finished "
+                                    "(vqx_plane_%s_submit / _finish)" % args.op),
                        "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e,
             "roofline": roofline,

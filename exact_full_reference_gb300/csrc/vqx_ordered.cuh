@@ -25,8 +25,12 @@
 // - One walk per frame and sum applies the blocks in order.
 //
 // Kernels: ordered_block_sums -> ordered_classify -> ordered_tables ->
-// ordered_walk.  The terms are recomputed from the planes in the literal
-// form (fp32 subtract and square, then the exact integer conversion).
+// ordered_walk.  The terms are recomputed from the planes: an fp32 subtract
+// and square (each rounded to nearest even, never fused), then the exact
+// integer conversion.  Dense frames (contiguous rows, 16-byte aligned) are
+// read as 16-byte vectors and their samples turned into floats without a
+// conversion instruction (the bits 0x4B000000 | s are the float 2^23 + s);
+// other layouts are read sample by sample.
 #pragma once
 
 #include <cstdint>
@@ -49,31 +53,81 @@ struct OrdTable {
     int p[2];        // output parity for input parity 0, 1
 };
 
-__device__ __forceinline__ uint32_t ord_term(int q, uint32_t r, uint32_t d) {
-    const float fr = __uint2float_rn(r), fd = __uint2float_rn(d);
-    if (q == 0) {
-        const float diff = __fsub_rn(fr, fd);
-        return __float2uint_rn(__fmul_rn(diff, diff));
-    }
-    const float x = q == 1 ? fr : fd;
-    return __float2uint_rn(__fmul_rn(x, x));
+
+
+// Where a plane pair's frames are: frame f of each plane starts f *
+// frame_pitch bytes after its base, rows stride bytes apart; the pixels of a
+// frame are numbered in raster order and cut into nb blocks of kOrdBlock.
+// dense: rows contiguous (stride = 2 width), bases 16-byte aligned and the
+// pixel count a multiple of 8, so that block b of frame f is the bytes
+// [2 b kOrdBlock, 2 (b kOrdBlock + len)) of the frame, whole 16-byte vectors.
+struct OrdPlanes {
+    const unsigned char *ref, *dist;
+    size_t frame_pitch, stride;
+    int width;
+    uint32_t pixels;
+    int nb;
+    int dense;
+};
+
+__device__ __forceinline__ uint32_t ord_len(const OrdPlanes &g, int b) {
+    return min((uint32_t)kOrdBlock, g.pixels - (uint32_t)b * kOrdBlock);
 }
 
-// Calls fn(j, r, d) for the raster pixels [i0, i0 + len) of frame f, j the
-// offset in the block; the CTA's threads share the work row segment by row
-// segment (coalesced within a row).
+// The float of a 16-bit sample without a conversion: (2^23 + s) - 2^23.
+__device__ __forceinline__ float ord_float(uint32_t s) {
+    return __fsub_rn(__uint_as_float(0x4B000000u | s), 8388608.0f);
+}
+
+// The three terms of one pixel: fl(fl(r) - fl(d))^2, fl(r * r), fl(d * d),
+// each an integer below 2^32.
+__device__ __forceinline__ void ord_terms(uint32_t r, uint32_t d, uint32_t (&t)[kOrdSeqs]) {
+    const float fr = ord_float(r), fd = ord_float(d);
+    const float diff = __fsub_rn(fr, fd);
+    t[0] = __float2uint_rn(__fmul_rn(diff, diff));
+    t[1] = __float2uint_rn(__fmul_rn(fr, fr));
+    t[2] = __float2uint_rn(__fmul_rn(fd, fd));
+}
+
+__device__ __forceinline__ uint32_t ord_term(int q, uint32_t r, uint32_t d) {
+    uint32_t t[kOrdSeqs];
+    ord_terms(r, d, t);
+    return t[q];
+}
+
+__device__ __forceinline__ uint4 ord_ld16(const unsigned char *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Calls fn(j, r, d) for every pixel j of block b of frame f, the lanes
+// (threads) of the calling group sharing the work: nthreads of them, this
+// one tid.  Dense frames go 16-byte vector by vector (8 pixels, j in raster
+// order), others row segment by row segment (coalesced within a row).
 template <class Fn>
-__device__ __forceinline__ void ord_block_pixels(const unsigned char *ref, const unsigned char *dist,
-                                                 size_t frame_pitch, size_t stride, int width,
-                                                 int f, uint32_t i0, uint32_t len, Fn fn) {
-    uint32_t y = i0 / (uint32_t)width, x = i0 - y * (uint32_t)width;
+__device__ __forceinline__ void ord_block_pixels(const OrdPlanes &g, int f, int b, int tid,
+                                                 int nthreads, Fn fn) {
+    const uint32_t i0 = (uint32_t)b * kOrdBlock, len = ord_len(g, b);
+    const unsigned char *rf = g.ref + (size_t)f * g.frame_pitch;
+    const unsigned char *df = g.dist + (size_t)f * g.frame_pitch;
+    if (g.dense) {
+        const unsigned char *rb = rf + 2 * (size_t)i0, *db = df + 2 * (size_t)i0;
+        for (uint32_t v = tid; v < len / 8; v += nthreads) {
+            const uint4 a = ord_ld16(rb + 16 * (size_t)v), c = ord_ld16(db + 16 * (size_t)v);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int w = 0; w < 4; w++) {
+                fn(8 * v + 2 * w, aw[w] & 0xffffu, cw[w] & 0xffffu);
+                fn(8 * v + 2 * w + 1, aw[w] >> 16, cw[w] >> 16);
+            }
+        }
+        return;
+    }
+    uint32_t y = i0 / (uint32_t)g.width, x = i0 - y * (uint32_t)g.width;
     for (uint32_t j0 = 0; j0 < len;) {
-        const uint32_t n = min((uint32_t)width - x, len - j0);
-        const unsigned short *rr = reinterpret_cast<const unsigned short *>(
-                                       ref + (size_t)f * frame_pitch + (size_t)y * stride) + x;
-        const unsigned short *dr = reinterpret_cast<const unsigned short *>(
-                                       dist + (size_t)f * frame_pitch + (size_t)y * stride) + x;
-        for (uint32_t k = threadIdx.x; k < n; k += blockDim.x) fn(j0 + k, (uint32_t)rr[k], (uint32_t)dr[k]);
+        const uint32_t n = min((uint32_t)g.width - x, len - j0);
+        const unsigned short *rr = reinterpret_cast<const unsigned short *>(rf + (size_t)y * g.stride) + x;
+        const unsigned short *dr = reinterpret_cast<const unsigned short *>(df + (size_t)y * g.stride) + x;
+        for (uint32_t k = tid; k < n; k += nthreads) fn(j0 + k, (uint32_t)rr[k], (uint32_t)dr[k]);
         j0 += n;
         y++;
         x = 0;
@@ -81,86 +135,141 @@ __device__ __forceinline__ void ord_block_pixels(const unsigned char *ref, const
 }
 
 // Grid (blocks per frame, frames), 128 threads: the exact sums of the three
-// term sequences over each block, sums[(f * nb + b) * 3 + q], and the OR of
-// each sequence's terms, ors[same index] (a block whose terms are all
-// multiples of the ulp it works at adds without rounding).
+// term sequences over each block, sums[(f * nb + b) * 3 + q], the OR of each
+// sequence's terms, ors[same index] (a block whose terms are all multiples of
+// the ulp it works at adds without rounding), and the sums of the block's
+// reference and distorted samples, ssums[(f * nb + b) * 2 + 0, 1] (below
+// 4096 * 2^16 = 2^28).
 __global__ void __launch_bounds__(128)
-    ordered_block_sums(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
-                       size_t frame_pitch, size_t stride, int width, uint32_t pixels, int nb,
-                       u64 *__restrict__ sums, uint32_t *__restrict__ ors) {
+    ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
+                       uint32_t *__restrict__ ssums) {
     const int b = blockIdx.x, f = blockIdx.y;
-    const uint32_t i0 = (uint32_t)b * kOrdBlock;
-    const uint32_t len = min((uint32_t)kOrdBlock, pixels - i0);
     u64 t[kOrdSeqs] = {0, 0, 0};
     uint32_t o[kOrdSeqs] = {0, 0, 0};
-    ord_block_pixels(ref, dist, frame_pitch, stride, width, f, i0, len,
-                     [&](uint32_t, uint32_t r, uint32_t d) {
+    uint32_t sr = 0, sd = 0;
+    ord_block_pixels(g, f, b, threadIdx.x, 128, [&](uint32_t, uint32_t r, uint32_t d) {
+        uint32_t x[kOrdSeqs];
+        ord_terms(r, d, x);
 #pragma unroll
-                         for (int q = 0; q < kOrdSeqs; q++) {
-                             const uint32_t x = ord_term(q, r, d);
-                             t[q] += x;
-                             o[q] |= x;
-                         }
-                     });
+        for (int q = 0; q < kOrdSeqs; q++) {
+            t[q] += x[q];
+            o[q] |= x[q];
+        }
+        sr += r;
+        sd += d;
+    });
+    sr = __reduce_add_sync(0xffffffffu, sr);
+    sd = __reduce_add_sync(0xffffffffu, sd);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1)
 #pragma unroll
-        for (int q = 0; q < kOrdSeqs; q++) {
-            t[q] += __shfl_xor_sync(0xffffffffu, t[q], sh);
-            o[q] |= __shfl_xor_sync(0xffffffffu, o[q], sh);
-        }
+        for (int q = 0; q < kOrdSeqs; q++) t[q] += __shfl_xor_sync(0xffffffffu, t[q], sh);
+#pragma unroll
+    for (int q = 0; q < kOrdSeqs; q++) o[q] = __reduce_or_sync(0xffffffffu, o[q]);
     __shared__ u64 ts[4][kOrdSeqs];
     __shared__ uint32_t os[4][kOrdSeqs];
+    __shared__ uint32_t ss[4][2];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0)
+    if (lane == 0) {
         for (int q = 0; q < kOrdSeqs; q++) {
             ts[warp][q] = t[q];
             os[warp][q] = o[q];
         }
+        ss[warp][0] = sr;
+        ss[warp][1] = sd;
+    }
     __syncthreads();
     if (threadIdx.x < kOrdSeqs) {
         const int q = threadIdx.x;
-        const size_t slot = ((size_t)f * nb + b) * kOrdSeqs + q;
+        const size_t slot = ((size_t)f * g.nb + b) * kOrdSeqs + q;
         sums[slot] = ts[0][q] + ts[1][q] + ts[2][q] + ts[3][q];
         ors[slot] = os[0][q] | os[1][q] | os[2][q] | os[3][q];
+    } else if (threadIdx.x < kOrdSeqs + 2) {
+        const int k = threadIdx.x - kOrdSeqs;
+        ssums[((size_t)f * g.nb + b) * 2 + k] = ss[0][k] + ss[1][k] + ss[2][k] + ss[3][k];
     }
 }
 
 __device__ __forceinline__ int binade_of(u64 x) { return 63 - __clzll((long long)x); }
 
+// A tabulated block to compute: frame, sequence, block.
+struct OrdWork {
+    int f, q, b;
+};
+
+constexpr int kOrdBatch = 8;  // chunks of 32 blocks loaded at once by the one-warp kernels
+constexpr int kOrdOut = 8;    // words per frame of the ordered kernels' output
+
 // Grid (frames, 3), one warp: prefix sums over the blocks of one sequence
-// and the class of every block, cls[(f * 3 + q) * nb + b].  A single-binade
-// block whose terms are all multiples of the binade's ulp is exact.
+// and the class of every block, cls[(f * 3 + q) * nb + b]; the q = 0 warp
+// also adds the blocks' sample sums into out[f * kOrdOut + 6, 7].  The
+// blocks go in chunks of 32 (one per lane, coalesced), the prefix by a warp
+// scan.  A single-binade block whose terms are all multiples of the
+// binade's ulp is exact.  Every tabulated block is appended to work (count
+// in *n_work, which starts at 0).
+
 __global__ void __launch_bounds__(32)
-    ordered_classify(const u64 *__restrict__ sums, const uint32_t *__restrict__ ors, int nb,
-                     int *__restrict__ cls) {
+    ordered_classify(const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
+                     const uint32_t *__restrict__ ssums, int nb, int *__restrict__ cls,
+                     OrdWork *__restrict__ work, int *__restrict__ n_work, u64 *__restrict__ out) {
     const int f = blockIdx.x, q = blockIdx.y, lane = threadIdx.x;
-    const int per = (nb + 31) / 32;
-    const int b0 = min(lane * per, nb), b1 = min(b0 + per, nb);
-    u64 mine = 0;
-    for (int b = b0; b < b1; b++) mine += sums[((size_t)f * nb + b) * 3 + q];
-    u64 incl = mine;
+    u64 base = 0;  // prefix of the chunk's first block
+    u64 sr = 0, sd = 0;
+    for (int cb = 0; cb < nb; cb += 32 * kOrdBatch) {
+        u64 Tb[kOrdBatch];
+        uint32_t Ob[kOrdBatch];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    u64 P = incl - mine;  // exclusive prefix of this lane's first block
-    for (int b = b0; b < b1; b++) {
-        const u64 T = sums[((size_t)f * nb + b) * 3 + q];
-        const u64 P1 = P + T;
-        int c;
-        if (P1 < kTwo53) {
-            c = kOrdExact;
-        } else if (P >= kTwo53 + kOrdMargin && binade_of(P - kOrdMargin) == binade_of(P1 + kOrdMargin)) {
-            c = binade_of(P) - 52;
-            // the running sum is a multiple of 2^c here; so are the terms?
-            if ((ors[((size_t)f * nb + b) * 3 + q] & ((1u << c) - 1)) == 0) c = kOrdExact;
-        } else {
-            c = kOrdReplay;
+        for (int u = 0; u < kOrdBatch; u++) {  // all loads first, then the chunks in order
+            const int b = cb + 32 * u + lane;
+            const size_t in = ((size_t)f * nb + b) * kOrdSeqs + q;
+            Tb[u] = b < nb ? sums[in] : 0;
+            Ob[u] = b < nb ? ors[in] : 0;
+            if (q == 0 && b < nb) {
+                sr += ssums[((size_t)f * nb + b) * 2];
+                sd += ssums[((size_t)f * nb + b) * 2 + 1];
+            }
         }
-        cls[((size_t)f * kOrdSeqs + q) * nb + b] = c;
-        P = P1;
+#pragma unroll
+        for (int u = 0; u < kOrdBatch; u++) {
+            const int b = cb + 32 * u + lane;
+            const bool valid = b < nb;
+            const u64 T = Tb[u];
+            u64 incl = T;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const u64 P = base + incl - T, P1 = P + T;
+            int c = kOrdReplay;
+            if (P1 < kTwo53) {
+                c = kOrdExact;
+            } else if (P >= kTwo53 + kOrdMargin &&
+                       binade_of(P - kOrdMargin) == binade_of(P1 + kOrdMargin)) {
+                c = binade_of(P) - 52;
+                // the running sum is a multiple of 2^c here; so are the terms?
+                if ((Ob[u] & ((1u << c) - 1)) == 0) c = kOrdExact;
+            }
+            const bool tab = valid && c != kOrdExact && c != kOrdReplay;
+            const unsigned m = __ballot_sync(0xffffffffu, tab);
+            int first = 0;
+            if (lane == 0 && m) first = atomicAdd(n_work, __popc(m));
+            first = __shfl_sync(0xffffffffu, first, 0);
+            if (valid) cls[((size_t)f * kOrdSeqs + q) * nb + b] = c;
+            if (tab) work[first + __popc(m & ((1u << lane) - 1))] = OrdWork{f, q, b};
+            base = __shfl_sync(0xffffffffu, P1, 31);
+        }
+    }
+    if (q == 0) {
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) {
+            sr += __shfl_xor_sync(0xffffffffu, sr, sh);
+            sd += __shfl_xor_sync(0xffffffffu, sd, sh);
+        }
+        if (lane == 0) {
+            out[(size_t)f * kOrdOut + 6] = sr;
+            out[(size_t)f * kOrdOut + 7] = sd;
+        }
     }
 }
 
@@ -174,140 +283,252 @@ __device__ __forceinline__ int ord_step(uint32_t t, int k, int &p) {
     return up ? (int)(u - r) : -(int)r;
 }
 
-// Grid (blocks per frame, frames, 3), one warp: the transfer table of each
-// single-binade block.  The block's terms are staged in shared memory with
-// one pad word every kOrdLane words, so that lane l reading its run
-// [l * kOrdLane, (l + 1) * kOrdLane) hits a different bank than the others.
-__global__ void __launch_bounds__(32)
-    ordered_tables(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
-                   size_t frame_pitch, size_t stride, int width, uint32_t pixels, int nb,
-                   const int *__restrict__ cls, OrdTable *__restrict__ tables) {
-    const int b = blockIdx.x, f = blockIdx.y, q = blockIdx.z, lane = threadIdx.x;
-    const size_t slot = ((size_t)f * kOrdSeqs + q) * nb + b;
-    const int k = cls[slot];
-    if (k == kOrdExact || k == kOrdReplay) return;
-    __shared__ uint32_t terms[kOrdBlock + kOrdBlock / kOrdLane];
-    const uint32_t i0 = (uint32_t)b * kOrdBlock;
-    const uint32_t len = min((uint32_t)kOrdBlock, pixels - i0);
-    ord_block_pixels(ref, dist, frame_pitch, stride, width, f, i0, len,
-                     [&](uint32_t j, uint32_t r, uint32_t d) { terms[j + j / kOrdLane] = ord_term(q, r, d); });
-    __syncwarp();
-    // this lane's run, for both input parities
-    long long e0 = 0, e1 = 0;
-    int p0 = 0, p1 = 1;
-    const uint32_t j0 = (uint32_t)lane * kOrdLane;
-    for (uint32_t j = j0; j < j0 + kOrdLane && j < len; j++) {
-        const uint32_t t = terms[j + j / kOrdLane];
-        e0 += ord_step(t, k, p0);
-        e1 += ord_step(t, k, p1);
+// A block's effect at one ulp 2^k, for input parity 0 and 1: the rounding
+// error and the output parity.  compose(g, h) is g, then h.
+struct OrdFn {
+    long long e0, e1;
+    int p0, p1;
+};
+
+__device__ __forceinline__ OrdFn ord_compose(const OrdFn &g, const OrdFn &h) {
+    OrdFn c;
+    c.e0 = g.e0 + (g.p0 ? h.e1 : h.e0);
+    c.p0 = g.p0 ? h.p1 : h.p0;
+    c.e1 = g.e1 + (g.p1 ? h.e1 : h.e0);
+    c.p1 = g.p1 ? h.p1 : h.p0;
+    return c;
+}
+
+// Inclusive scan of the lanes' functions in lane order (lane l ends with
+// f_0, then f_1, .., then f_l).
+__device__ __forceinline__ OrdFn ord_scan(OrdFn fn, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        OrdFn g;
+        g.e0 = __shfl_up_sync(0xffffffffu, fn.e0, o);
+        g.e1 = __shfl_up_sync(0xffffffffu, fn.e1, o);
+        g.p0 = __shfl_up_sync(0xffffffffu, fn.p0, o);
+        g.p1 = __shfl_up_sync(0xffffffffu, fn.p1, o);
+        if (lane >= o) fn = ord_compose(g, fn);
     }
-    // compose the lanes' functions in lane order
-    long long E0 = 0, E1 = 0;
-    int P0 = 0, P1 = 1;
-    for (int l = 0; l < 32; l++) {
-        const long long le0 = __shfl_sync(0xffffffffu, e0, l), le1 = __shfl_sync(0xffffffffu, e1, l);
-        const int lp0 = __shfl_sync(0xffffffffu, p0, l), lp1 = __shfl_sync(0xffffffffu, p1, l);
-        E0 += P0 ? le1 : le0;
-        P0 = P0 ? lp1 : lp0;
-        E1 += P1 ? le1 : le0;
-        P1 = P1 ? lp1 : lp0;
-    }
-    if (lane == 0) {
-        OrdTable tb;
-        tb.e[0] = E0;
-        tb.e[1] = E1;
-        tb.p[0] = P0;
-        tb.p[1] = P1;
-        tables[slot] = tb;
+    return fn;
+}
+
+constexpr int kTableWarps = 2;  // warps per CTA in ordered_tables (33 KB of staged terms)
+
+// Fixed grid of kTableWarps-warp CTAs: each warp takes tabulated blocks from
+// the work list and writes their transfer tables.  The block's terms are
+// staged in the warp's shared memory with one pad word every kOrdLane
+// words, so that lane l reading its run [l * kOrdLane, (l + 1) * kOrdLane)
+// hits a different bank than the others; each lane folds its run for both
+// input parities and a warp scan composes the runs.
+__global__ void __launch_bounds__(32 * kTableWarps)
+    ordered_tables(const OrdPlanes g, const int *__restrict__ cls, const OrdWork *__restrict__ work,
+                   const int *__restrict__ n_work, OrdTable *__restrict__ tables) {
+    __shared__ uint32_t terms_all[kTableWarps][kOrdBlock + kOrdBlock / kOrdLane];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    uint32_t *terms = terms_all[wib];
+    const int n = *n_work;
+    for (int w = blockIdx.x * kTableWarps + wib; w < n; w += gridDim.x * kTableWarps) {
+        const OrdWork job = work[w];
+        const size_t slot = ((size_t)job.f * kOrdSeqs + job.q) * g.nb + job.b;
+        const int k = cls[slot];
+        const uint32_t len = ord_len(g, job.b);
+        ord_block_pixels(g, job.f, job.b, lane, 32, [&](uint32_t j, uint32_t r, uint32_t d) {
+            terms[j + j / kOrdLane] = ord_term(job.q, r, d);
+        });
+        __syncwarp();
+        OrdFn fn{0, 0, 0, 1};
+        const uint32_t j0 = (uint32_t)lane * kOrdLane;
+        for (uint32_t j = j0; j < j0 + kOrdLane && j < len; j++) {
+            const uint32_t t = terms[j + j / kOrdLane];
+            fn.e0 += ord_step(t, k, fn.p0);
+            fn.e1 += ord_step(t, k, fn.p1);
+        }
+        fn = ord_scan(fn, lane);
+        if (lane == 31) {
+            OrdTable tb;
+            tb.e[0] = fn.e0;
+            tb.e[1] = fn.e1;
+            tb.p[0] = fn.p0;
+            tb.p[1] = fn.p1;
+            tables[slot] = tb;
+        }
+        __syncwarp();  // terms is rewritten by the next job
     }
 }
 
-// Grid (frames, 3), one warp: the walk.  Lane 0 carries the CPU's running
-// sum S (an integer below 2^57, exact in a double and in 64 bits) through the
-// blocks; block metadata is staged in shared memory a chunk at a time, and a
-// replayed block's terms are computed by the warp, then added one by one
-// with double-precision round-to-nearest-even adds.  out[f * 3 + q] = S.
+// One add of t to S (an integer below 2^58 that a double holds exactly), as
+// the CPU's double add does it: the exact integer sum rounded to 53
+// significant bits, to nearest with ties to even.
+__device__ __forceinline__ u64 ord_add_rne(u64 S, uint32_t t) {
+    u64 x = S + t;
+    const int nbits = 64 - __clzll((long long)x);
+    if (nbits <= 53) return x;
+    const int sh = nbits - 53;
+    const u64 ulp = 1ull << sh, r = x & (ulp - 1), half = ulp >> 1;
+    x -= r;
+    if (r > half || (r == half && ((x >> sh) & 1))) x += ulp;
+    return x;
+}
+
+// A replayed block (its len terms staged in shared memory, seen by the whole
+// warp) added to S.  Lane l takes the run [l kOrdLane, (l + 1) kOrdLane):
+// its exact sum and, from S and the runs before it, its class as in
+// ordered_classify (exact below 2^53; inside one binade with the margin;
+// otherwise crossing a boundary).  A single-binade run folds its function
+// of the parity at that binade's ulp; then the runs are applied in order, a
+// crossing run (at most a few in a frame) term by term.
+__device__ u64 ord_replay_block(u64 S, const uint32_t *terms, uint32_t len, int lane) {
+    const uint32_t j0 = (uint32_t)lane * kOrdLane, j1 = min(j0 + (uint32_t)kOrdLane, len);
+    u64 R = 0;
+    for (uint32_t j = j0; j < j1; j++) R += terms[j];
+    u64 incl = R;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const u64 a = S + (incl - R), a1 = a + R;
+    int c = kOrdReplay;
+    if (a1 < kTwo53)
+        c = kOrdExact;
+    else if (a >= kTwo53 + kOrdMargin && binade_of(a - kOrdMargin) == binade_of(a1 + kOrdMargin))
+        c = binade_of(a) - 52;
+    OrdFn fn{0, 0, 0, 1};
+    if (c != kOrdExact && c != kOrdReplay)
+        for (uint32_t j = j0; j < j1; j++) {
+            fn.e0 += ord_step(terms[j], c, fn.p0);
+            fn.e1 += ord_step(terms[j], c, fn.p1);
+        }
+    for (int l = 0; l < 32; l++) {
+        const int cl = __shfl_sync(0xffffffffu, c, l);
+        const u64 Rl = __shfl_sync(0xffffffffu, R, l);
+        if (cl == kOrdExact) {
+            S += Rl;
+        } else if (cl != kOrdReplay) {
+            const long long e0 = __shfl_sync(0xffffffffu, fn.e0, l);
+            const long long e1 = __shfl_sync(0xffffffffu, fn.e1, l);
+            S += Rl + (u64)(((S >> cl) & 1) ? e1 : e0);
+        } else {
+            if (lane == 0) {
+                const uint32_t k1 = min((uint32_t)(l + 1) * kOrdLane, len);
+                for (uint32_t j = (uint32_t)l * kOrdLane; j < k1; j++) S = ord_add_rne(S, terms[j]);
+            }
+            S = __shfl_sync(0xffffffffu, S, 0);
+        }
+    }
+    return S;
+}
+
+// Grid (frames, 3), one warp: the walk.  Every lane carries the CPU's
+// running sum S (an integer below 2^57, exact in a double and in 64 bits)
+// through the blocks, 32 at a time, one per lane (kOrdBatch chunks loaded at
+// once):
+// - a chunk of exact blocks adds its exact sum;
+// - a chunk of blocks that all work at one ulp 2^k (tabulated at k, or exact
+//   with a sum that is a multiple of 2^k) composes the blocks' functions of
+//   the parity (S / 2^k) mod 2 by a warp scan and applies the result once;
+// - any other chunk goes block by block: exact and tabulated blocks as
+//   above; a block near a boundary adds exactly when the running sum and all
+//   of its terms are multiples of the largest ulp it can reach, and is
+//   otherwise replayed (ord_replay_block).
+// out[f * kOrdOut + q] = S, out[f * kOrdOut + 3 + q] = the exact sum of the
+// sequence.
 __global__ void __launch_bounds__(32)
-    ordered_walk(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
-                 size_t frame_pitch, size_t stride, int width, uint32_t pixels, int nb,
-                 const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
+    ordered_walk(const OrdPlanes g, const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
                  const int *__restrict__ cls, const OrdTable *__restrict__ tables,
                  u64 *__restrict__ out) {
     const int f = blockIdx.x, q = blockIdx.y, lane = threadIdx.x;
-    constexpr int kChunk = 128;
-    __shared__ int c_s[kChunk];
-    __shared__ u64 t_s[kChunk];
-    __shared__ OrdTable tb_s[kChunk];
     __shared__ uint32_t terms[kOrdBlock];
-    __shared__ uint32_t o_s[kChunk];
-    __shared__ int replay_list[kChunk];
-    __shared__ int n_replay;
-    __shared__ int do_replay;
-    u64 S = 0;
-    for (int c0 = 0; c0 < nb; c0 += kChunk) {
-        const int n = min(kChunk, nb - c0);
-        for (int i = lane; i < n; i += 32) {
-            const size_t slot = ((size_t)f * kOrdSeqs + q) * nb + c0 + i;
-            c_s[i] = cls[slot];
-            t_s[i] = sums[((size_t)f * nb + c0 + i) * 3 + q];
-            o_s[i] = ors[((size_t)f * nb + c0 + i) * 3 + q];
-            if (c_s[i] != kOrdExact && c_s[i] != kOrdReplay) tb_s[i] = tables[slot];
+    const int nb = g.nb;
+    u64 S = 0, exact = 0;
+    for (int cb = 0; cb < nb; cb += 32 * kOrdBatch) {
+        int cB[kOrdBatch];
+        u64 TB[kOrdBatch];
+        uint32_t oB[kOrdBatch];
+        OrdTable tbB[kOrdBatch];
+#pragma unroll
+        for (int u = 0; u < kOrdBatch; u++) {  // all loads first, then the chunks in order
+            const int b = cb + 32 * u + lane;
+            const bool valid = b < nb;
+            const size_t slot = ((size_t)f * kOrdSeqs + q) * nb + b;
+            const size_t in = ((size_t)f * nb + b) * kOrdSeqs + q;
+            cB[u] = valid ? cls[slot] : kOrdExact;
+            TB[u] = valid ? sums[in] : 0;
+            oB[u] = valid ? ors[in] : 0;
+            tbB[u] = OrdTable{{0, 0}, {0, 1}};
+            if (valid && cB[u] != kOrdExact && cB[u] != kOrdReplay) tbB[u] = tables[slot];
         }
-        __syncwarp();
-        if (lane == 0) {
-            int m = 0;
-            for (int i = 0; i < n; i++)
-                if (c_s[i] == kOrdReplay) replay_list[m++] = i;
-            n_replay = m;
-        }
-        __syncwarp();
-        // walk the chunk; stop at each replayed block to stage its terms
-        int i = 0;
-        for (int rix = 0; rix <= n_replay; rix++) {
-            const int stop = rix < n_replay ? replay_list[rix] : n;
-            if (lane == 0) {
-                for (; i < stop; i++) {
-                    if (c_s[i] == kOrdExact) {
-                        S += t_s[i];
+#pragma unroll
+        for (int u = 0; u < kOrdBatch; u++) {
+            const int c0 = cb + 32 * u;
+            if (c0 >= nb) break;
+            const int c = cB[u];
+            const u64 T = TB[u];
+            const bool tab = c != kOrdExact && c != kOrdReplay;
+            u64 sumT = T;
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) sumT += __shfl_xor_sync(0xffffffffu, sumT, sh);
+            exact += sumT;
+            if (__all_sync(0xffffffffu, c == kOrdExact)) {
+                S += sumT;
+                continue;
+            }
+            const int kmin = __reduce_min_sync(0xffffffffu, tab ? c : 1000);
+            const int kmax = __reduce_max_sync(0xffffffffu, tab ? c : -1);
+            const bool fits = c != kOrdReplay && (tab || (T & ((1ull << kmin) - 1)) == 0);
+            if (kmin == kmax && __all_sync(0xffffffffu, fits)) {
+                const int k = kmin;
+                OrdFn fn;
+                if (tab) {
+                    fn = OrdFn{tbB[u].e[0], tbB[u].e[1], tbB[u].p[0], tbB[u].p[1]};
+                } else {  // exact, a multiple of 2^k: the parity flips with bit k of T
+                    const int t1 = (int)((T >> k) & 1);
+                    fn = OrdFn{0, 0, t1, t1 ^ 1};
+                }
+                fn = ord_scan(fn, lane);
+                const long long e0 = __shfl_sync(0xffffffffu, fn.e0, 31);
+                const long long e1 = __shfl_sync(0xffffffffu, fn.e1, 31);
+                S += sumT + (u64)(((S >> k) & 1) ? e1 : e0);
+                continue;
+            }
+            // block by block (every lane follows the same steps)
+            const int n = min(32, nb - c0);
+            for (int i = 0; i < n; i++) {
+                const int ci = __shfl_sync(0xffffffffu, c, i);
+                const u64 Ti = __shfl_sync(0xffffffffu, T, i);
+                if (ci == kOrdExact) {
+                    S += Ti;
+                } else if (ci != kOrdReplay) {
+                    const long long e0 = __shfl_sync(0xffffffffu, tbB[u].e[0], i);
+                    const long long e1 = __shfl_sync(0xffffffffu, tbB[u].e[1], i);
+                    S += Ti + (u64)(((S >> ci) & 1) ? e1 : e0);
+                } else {
+                    const uint32_t oi = __shfl_sync(0xffffffffu, oB[u], i);
+                    const u64 top = S + Ti + kOrdMargin;
+                    const int kneed = top < kTwo53 ? 0 : binade_of(top) - 52;
+                    const u64 mask = (1ull << kneed) - 1;
+                    if (((S | (u64)oi) & mask) == 0) {
+                        S += Ti;
                     } else {
-                        const int k = c_s[i];
-                        const int p = (int)((S >> k) & 1);
-                        S += t_s[i] + (u64)tb_s[i].e[p];
+                        const int bb = c0 + i;
+                        const uint32_t len = ord_len(g, bb);
+                        ord_block_pixels(g, f, bb, lane, 32, [&](uint32_t j, uint32_t r, uint32_t d) {
+                            terms[j] = ord_term(q, r, d);
+                        });
+                        __syncwarp();
+                        S = ord_replay_block(S, terms, len, lane);
+                        __syncwarp();  // terms is rewritten by the next replayed block
                     }
                 }
             }
-            // A block near a boundary adds exactly when the running sum and all
-            // of its terms are multiples of the largest ulp it can reach.
-            if (lane == 0 && rix < n_replay) {
-                const u64 top = S + t_s[stop] + kOrdMargin;
-                const int kneed = top < kTwo53 ? 0 : binade_of(top) - 52;
-                const u64 mask = (1ull << kneed) - 1;
-                do_replay = ((S | (u64)o_s[stop]) & mask) != 0;
-                if (!do_replay) {
-                    S += t_s[stop];
-                    i = stop + 1;
-                }
-            }
-            __syncwarp();
-            if (rix < n_replay && do_replay) {
-                const int b = c0 + stop;
-                const uint32_t i0 = (uint32_t)b * kOrdBlock;
-                const uint32_t len = min((uint32_t)kOrdBlock, pixels - i0);
-                ord_block_pixels(ref, dist, frame_pitch, stride, width, f, i0, len,
-                                 [&](uint32_t j, uint32_t r, uint32_t d) { terms[j] = ord_term(q, r, d); });
-                __syncwarp();
-                if (lane == 0) {
-                    double s = (double)S;
-                    for (uint32_t j = 0; j < len; j++) s = __dadd_rn(s, (double)terms[j]);
-                    S = (u64)s;
-                    i = stop + 1;
-                }
-            }
-            __syncwarp();  // do_replay and terms are rewritten next iteration
         }
-        __syncwarp();
     }
-    if (lane == 0) out[(size_t)f * kOrdSeqs + q] = S;
+    if (lane == 0) {
+        out[(size_t)f * kOrdOut + q] = S;
+        out[(size_t)f * kOrdOut + 3 + q] = exact;
+    }
 }
 
 }  // namespace vqx

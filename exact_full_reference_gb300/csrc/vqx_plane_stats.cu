@@ -951,51 +951,78 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
     if (bpc != 16 || pixels <= (1u << 21))
         return vqx_plane_stats(ref, dist, width, height, stride, bpc, n_frames, stream, out);
     if (n_frames > 65535) return VQX_EINVAL;
-    rc = vqx_plane_stats(ref, dist, width, height, stride, bpc, n_frames, stream, out);
-    if (rc != VQX_OK) return rc;
-    bool any = false;
-    for (int f = 0; f < n_frames; f++)
-        any |= out[f].noise_units >= vqx::kTwo53 || out[f].ref_sumsq >= vqx::kTwo53 ||
-               out[f].dist_sumsq >= vqx::kTwo53;
-    if (!any) return VQX_OK;
-
+    // The replay kernels produce every integer sum as well (the blocks' exact
+    // sums), so the plain pass is not run here.
     DeviceCtx *ctx = nullptr;
     if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     const int nb = (int)((pixels + vqx::kOrdBlock - 1) / vqx::kOrdBlock);
     const size_t cells = (size_t)n_frames * vqx::kOrdSeqs * nb;
     const size_t sums_b = cells * sizeof(u64), cls_b = cells * sizeof(int),
-                 tab_b = cells * sizeof(vqx::OrdTable), ors_b = cells * sizeof(uint32_t);
+                 tab_b = cells * sizeof(vqx::OrdTable), ors_b = cells * sizeof(uint32_t),
+                 work_b = cells * sizeof(vqx::OrdWork),
+                 ssum_b = (size_t)n_frames * nb * 2 * sizeof(uint32_t);
     PinnedBuf res;
-    if ((rc = acquire_pinned((size_t)n_frames * vqx::kOrdSeqs * sizeof(u64), &res)) != VQX_OK) return rc;
+    if ((rc = acquire_pinned((size_t)n_frames * vqx::kOrdOut * sizeof(u64), &res)) != VQX_OK) return rc;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, sums_b + cls_b + tab_b + ors_b + 256, ctx->pool, st);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, sums_b + cls_b + tab_b + ors_b + work_b + ssum_b + 256,
+                                            ctx->pool, st);
     if (e != cudaSuccess) {
         release_pinned(res);
         return cuda_status(e);
     }
+    // sums and tables (8-byte aligned), then the 4-byte arrays
     u64 *sums = (u64 *)ws;
     vqx::OrdTable *tables = (vqx::OrdTable *)((unsigned char *)ws + sums_b);
     int *cls = (int *)((unsigned char *)ws + sums_b + tab_b);
     uint32_t *ors = (uint32_t *)((unsigned char *)ws + sums_b + tab_b + cls_b);
-    const unsigned char *r = (const unsigned char *)ref, *d = (const unsigned char *)dist;
-    const size_t pitch = (size_t)height * stride;
-    const uint32_t px = (uint32_t)pixels;
-    vqx::ordered_block_sums<<<dim3(nb, n_frames), 128, 0, st>>>(r, d, pitch, stride, width, px, nb,
-                                                                 sums, ors);
-    e = cudaGetLastError();
+    vqx::OrdWork *work = (vqx::OrdWork *)((unsigned char *)ws + sums_b + tab_b + cls_b + ors_b);
+    uint32_t *ssums = (uint32_t *)((unsigned char *)ws + sums_b + tab_b + cls_b + ors_b + work_b);
+    int *n_work = (int *)((unsigned char *)ws + sums_b + tab_b + cls_b + ors_b + work_b + ssum_b);
+    vqx::OrdPlanes g;
+    g.ref = (const unsigned char *)ref;
+    g.dist = (const unsigned char *)dist;
+    g.frame_pitch = (size_t)height * stride;
+    g.stride = stride;
+    g.width = width;
+    g.pixels = (uint32_t)pixels;
+    g.nb = nb;
+    g.dense = stride == (size_t)width * 2 && (pixels & 7u) == 0 &&
+              (((uintptr_t)ref | (uintptr_t)dist) & 15u) == 0;
+    // with profiling on, the block-sum kernel (the pass over every pixel) is
+    // timed as this call's stage-1 launch
+    struct Events {  // destroyed on every return
+        cudaEvent_t e[2] = {nullptr, nullptr};
+        ~Events() {
+            for (cudaEvent_t x : e)
+                if (x) cudaEventDestroy(x);
+        }
+    } evs;
+    cudaEvent_t *ev = evs.e;
+    const bool timed = t_prof.on && cudaEventCreate(&ev[0]) == cudaSuccess &&
+                       cudaEventCreate(&ev[1]) == cudaSuccess;
+    e = cudaMemsetAsync(n_work, 0, sizeof(int), st);
     if (e == cudaSuccess) {
-        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(sums, ors, nb, cls);
+        if (timed) cudaEventRecord(ev[0], st);
+        vqx::ordered_block_sums<<<dim3(nb, n_frames), 128, 0, st>>>(g, sums, ors, ssums);
+        e = cudaGetLastError();
+        if (timed) cudaEventRecord(ev[1], st);
+    }
+    if (e == cudaSuccess) {
+        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(
+            sums, ors, ssums, nb, cls, work, n_work, (u64 *)res.dev);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
-        vqx::ordered_tables<<<dim3(nb, n_frames, vqx::kOrdSeqs), 32, 0, st>>>(r, d, pitch, stride, width,
-                                                                            px, nb, cls, tables);
+        // a fixed grid of warps takes the tabulated blocks from the list
+        const size_t jobs_max = (cells + vqx::kTableWarps - 1) / vqx::kTableWarps;
+        const unsigned grid = (unsigned)(jobs_max < (size_t)ctx->sms * 6 ? jobs_max : (size_t)ctx->sms * 6);
+        vqx::ordered_tables<<<grid, 32 * vqx::kTableWarps, 0, st>>>(g, cls, work, n_work, tables);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
-        vqx::ordered_walk<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(
-            r, d, pitch, stride, width, px, nb, sums, ors, cls, tables, (u64 *)res.dev);
+        vqx::ordered_walk<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(g, sums, ors, cls, tables,
+                                                                         (u64 *)res.dev);
         e = cudaGetLastError();
     }
     const cudaError_t ef = cudaFreeAsync(ws, st);
@@ -1005,20 +1032,31 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
         release_pinned(res);
         return cuda_status(e);
     }
-    t_prof.totals.kernel_launches += 4;
-    const u64 *cpu = (const u64 *)res.host;
+    t_prof.totals.calls++;
+    t_prof.totals.kernel_launches += 4;  // and one memset
+    t_prof.totals.stage1_launches += 1;
+    t_prof.totals.stage1_bytes += plane_bytes(width, height, bpc, n_frames);
+    if (timed) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, ev[0], ev[1]);
+        t_prof.totals.stage1_ms += ms;
+    }
+    const u64 *w = (const u64 *)res.host;
+    rc = VQX_OK;
     for (int f = 0; f < n_frames; f++) {
+        const u64 *o = w + (size_t)f * vqx::kOrdOut;
         Partial s_f;
-        s_f.v[0] = out[f].noise_units;
-        s_f.v[1] = out[f].ref_sum;
-        s_f.v[2] = out[f].dist_sum;
-        s_f.v[3] = out[f].ref_sumsq;
-        s_f.v[4] = out[f].dist_sumsq;
-        s_f.v[5] = 0;  // 16-bit: no range flag; a timeout would have returned above
-        conclude(s_f, bpc, width, height, &out[f], cpu + (size_t)f * vqx::kOrdSeqs);
+        s_f.v[0] = o[3];  // exact noise units
+        s_f.v[1] = o[6];  // sample sums
+        s_f.v[2] = o[7];
+        s_f.v[3] = o[4];  // exact squares
+        s_f.v[4] = o[5];
+        s_f.v[5] = 0;  // 16 bits: no sample is out of range; no device wait to time out
+        conclude(s_f, bpc, width, height, &out[f], o);
+        rc = merge_status(rc, out[f]);
     }
     release_pinned(res);
-    return VQX_OK;
+    return rc;
 }
 
 // ====================================================================== no-allocation variant

@@ -204,10 +204,13 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
  * frame), so noise, mse, psnr, psnr_uncapped, ref_meansq and dist_meansq
  * equal the CPU's doubles for every frame.  The integer fields stay the exact
  * sums.  Only 16-bit frames of more than 2^21 pixels can pass 2^53 units;
- * for the others, and for batches where no frame does, the call is
- * vqx_plane_stats.  Otherwise it costs four more kernels and about two more
- * reads of the planes.  Arguments and status codes as for vqx_plane_stats,
- * plus VQX_EINVAL for more than 65535 frames in such a batch.
+ * for the others the call is vqx_plane_stats.  For those it runs four
+ * kernels of its own instead (block sums of every sequence, their
+ * classification, transfer tables of the blocks that need them, and one walk
+ * per frame and sum), which read the planes once plus again for the blocks
+ * that are tabulated or replayed.  Arguments and status codes as for
+ * vqx_plane_stats, plus VQX_EINVAL for more than 65535 frames in such a
+ * batch.
  */
 int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
                             size_t stride, int bpc, int n_frames, vqx_stream_t stream,
