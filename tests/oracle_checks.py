@@ -52,19 +52,23 @@ def rne24(x):
     return (q + up.astype(np.uint64)) << s
 
 
-def exact_units(ref, dist):
+def exact_units(ref, dist, chunk=1 << 20):
     """Independent exact sums (Python integers) of one frame: the rounded
-    squares of the raw differences and of the raw samples, and the samples."""
-    r = np.asarray(ref, np.int64).ravel()
-    d = np.asarray(dist, np.int64).ravel()
-    D = np.abs(r - d).astype(np.uint64)
-    return {
-        "noise_units": int(rne24(D * D).sum(dtype=np.uint64)),
-        "ref_sum": int(r.sum()),
-        "dist_sum": int(d.sum()),
-        "ref_sumsq": int(rne24(r.astype(np.uint64) ** 2).sum(dtype=np.uint64)),
-        "dist_sumsq": int(rne24(d.astype(np.uint64) ** 2).sum(dtype=np.uint64)),
-    }
+    squares of the raw differences and of the raw samples, and the samples.
+    Taken a chunk of pixels at a time (small temporaries)."""
+    rr = np.asarray(ref).ravel()
+    dd = np.asarray(dist).ravel()
+    out = dict.fromkeys(("noise_units", "ref_sum", "dist_sum", "ref_sumsq", "dist_sumsq"), 0)
+    for i in range(0, rr.size, chunk):
+        r = rr[i : i + chunk].astype(np.int64)
+        d = dd[i : i + chunk].astype(np.int64)
+        D = np.abs(r - d).astype(np.uint64)
+        out["noise_units"] += int(rne24(D * D).sum(dtype=np.uint64))
+        out["ref_sum"] += int(r.sum())
+        out["dist_sum"] += int(d.sum())
+        out["ref_sumsq"] += int(rne24(r.astype(np.uint64) ** 2).sum(dtype=np.uint64))
+        out["dist_sumsq"] += int(rne24(d.astype(np.uint64) ** 2).sum(dtype=np.uint64))
+    return out
 
 
 def correctly_rounded(num, den):
