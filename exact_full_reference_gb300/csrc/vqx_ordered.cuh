@@ -134,59 +134,91 @@ __device__ __forceinline__ void ord_block_pixels(const OrdPlanes &g, int f, int 
     }
 }
 
-// Grid (blocks per frame, frames), 128 threads: the exact sums of the three
-// term sequences over each block, sums[(f * nb + b) * 3 + q], the OR of each
-// sequence's terms, ors[same index] (a block whose terms are all multiples of
-// the ulp it works at adds without rounding), and the sums of the block's
-// reference and distorted samples, ssums[(f * nb + b) * 2 + 0, 1] (below
-// 4096 * 2^16 = 2^28).
-__global__ void __launch_bounds__(128)
-    ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
-                       uint32_t *__restrict__ ssums) {
-    const int b = blockIdx.x, f = blockIdx.y;
+// Grid (blocks per frame / kSumWarps, frames), one warp per block: the exact
+// sums of the three term sequences over each block, sums[(f * nb + b) * 3 +
+// q], the OR of each sequence's terms, ors[same index] (a block whose terms
+// are all multiples of the ulp it works at adds without rounding), and the
+// sums of the block's reference and distorted samples, ssums[(f * nb + b) *
+// 2 + 0, 1] (below 4096 * 2^16 = 2^28).
+// Dense frames, two pixels of a 32-bit word at a time: the samples' floats
+// from their bits, the three products as packed fp32 pairs (each lane one
+// round-to-nearest-even product, fma with +0 so that nothing fuses), their
+// exact integer conversions added in 64 bits and ORed three inputs at a
+// time, the samples summed by a two-way dot product.
+struct OrdWordSums {
     u64 t[kOrdSeqs] = {0, 0, 0};
     uint32_t o[kOrdSeqs] = {0, 0, 0};
     uint32_t sr = 0, sd = 0;
-    ord_block_pixels(g, f, b, threadIdx.x, 128, [&](uint32_t, uint32_t r, uint32_t d) {
-        uint32_t x[kOrdSeqs];
-        ord_terms(r, d, x);
+
+    __device__ __forceinline__ void word(uint32_t a, uint32_t b) {
+        constexpr uint32_t kBias = 0x4B000000u;
+        const f32x2 two23 = ((f32x2)kBias << 32) | kBias;
+        const f32x2 xr = f2_pack((a & 0xffffu) | kBias, __byte_perm(a, kBias, 0x7632));
+        const f32x2 xd = f2_pack((b & 0xffffu) | kBias, __byte_perm(b, kBias, 0x7632));
+        uint32_t v[kOrdSeqs][2];
+        f2_unpack(f2_square(f2_sub(xr, xd)), v[0][0], v[0][1]);
+        f2_unpack(f2_square(f2_sub(xr, two23)), v[1][0], v[1][1]);
+        f2_unpack(f2_square(f2_sub(xd, two23)), v[2][0], v[2][1]);
 #pragma unroll
         for (int q = 0; q < kOrdSeqs; q++) {
-            t[q] += x[q];
-            o[q] |= x[q];
+            const uint32_t x0 = __float2uint_rn(__uint_as_float(v[q][0]));
+            const uint32_t x1 = __float2uint_rn(__uint_as_float(v[q][1]));
+            t[q] += (u64)x0 + x1;
+            o[q] |= x0 | x1;
         }
-        sr += r;
-        sd += d;
-    });
-    sr = __reduce_add_sync(0xffffffffu, sr);
-    sd = __reduce_add_sync(0xffffffffu, sd);
+        sr = __dp2a_lo(a, 0x01010101u, sr);
+        sd = __dp2a_lo(b, 0x01010101u, sd);
+    }
+};
+
+constexpr int kSumWarps = 4;  // blocks (one per warp) per CTA of ordered_block_sums
+
+__global__ void __launch_bounds__(32 * kSumWarps)
+    ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
+                       uint32_t *__restrict__ ssums) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kSumWarps + (threadIdx.x >> 5), f = blockIdx.y;
+    if (b >= g.nb) return;
+    OrdWordSums w;
+    if (g.dense) {
+        const uint32_t len = ord_len(g, b);
+        const size_t off = (size_t)f * g.frame_pitch + 2 * (size_t)b * kOrdBlock;
+        const unsigned char *rb = g.ref + off, *db = g.dist + off;
+#pragma unroll 4
+        for (uint32_t v = lane; v < len / 8; v += 32) {
+            const uint4 x = ord_ld16(rb + 16 * (size_t)v), y = ord_ld16(db + 16 * (size_t)v);
+            w.word(x.x, y.x);
+            w.word(x.y, y.y);
+            w.word(x.z, y.z);
+            w.word(x.w, y.w);
+        }
+    } else {
+        ord_block_pixels(g, f, b, lane, 32, [&](uint32_t, uint32_t r, uint32_t d) {
+            uint32_t x[kOrdSeqs];
+            ord_terms(r, d, x);
+#pragma unroll
+            for (int q = 0; q < kOrdSeqs; q++) {
+                w.t[q] += x[q];
+                w.o[q] |= x[q];
+            }
+            w.sr += r;
+            w.sd += d;
+        });
+    }
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1)
 #pragma unroll
-        for (int q = 0; q < kOrdSeqs; q++) t[q] += __shfl_xor_sync(0xffffffffu, t[q], sh);
+        for (int q = 0; q < kOrdSeqs; q++) w.t[q] += __shfl_xor_sync(0xffffffffu, w.t[q], sh);
+    uint32_t o[kOrdSeqs];
 #pragma unroll
-    for (int q = 0; q < kOrdSeqs; q++) o[q] = __reduce_or_sync(0xffffffffu, o[q]);
-    __shared__ u64 ts[4][kOrdSeqs];
-    __shared__ uint32_t os[4][kOrdSeqs];
-    __shared__ uint32_t ss[4][2];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) {
-        for (int q = 0; q < kOrdSeqs; q++) {
-            ts[warp][q] = t[q];
-            os[warp][q] = o[q];
-        }
-        ss[warp][0] = sr;
-        ss[warp][1] = sd;
-    }
-    __syncthreads();
-    if (threadIdx.x < kOrdSeqs) {
-        const int q = threadIdx.x;
-        const size_t slot = ((size_t)f * g.nb + b) * kOrdSeqs + q;
-        sums[slot] = ts[0][q] + ts[1][q] + ts[2][q] + ts[3][q];
-        ors[slot] = os[0][q] | os[1][q] | os[2][q] | os[3][q];
-    } else if (threadIdx.x < kOrdSeqs + 2) {
-        const int k = threadIdx.x - kOrdSeqs;
-        ssums[((size_t)f * g.nb + b) * 2 + k] = ss[0][k] + ss[1][k] + ss[2][k] + ss[3][k];
+    for (int q = 0; q < kOrdSeqs; q++) o[q] = __reduce_or_sync(0xffffffffu, w.o[q]);
+    const uint32_t sr = __reduce_add_sync(0xffffffffu, w.sr), sd = __reduce_add_sync(0xffffffffu, w.sd);
+    const size_t slot = ((size_t)f * g.nb + b) * kOrdSeqs;
+    if (lane < kOrdSeqs) {
+        sums[slot + lane] = lane == 0 ? w.t[0] : lane == 1 ? w.t[1] : w.t[2];
+        ors[slot + lane] = lane == 0 ? o[0] : lane == 1 ? o[1] : o[2];
+    } else if (lane < kOrdSeqs + 2) {
+        ssums[((size_t)f * g.nb + b) * 2 + (lane - kOrdSeqs)] = lane == kOrdSeqs ? sr : sd;
     }
 }
 

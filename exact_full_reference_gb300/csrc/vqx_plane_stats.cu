@@ -1004,7 +1004,8 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
     e = cudaMemsetAsync(n_work, 0, sizeof(int), st);
     if (e == cudaSuccess) {
         if (timed) cudaEventRecord(ev[0], st);
-        vqx::ordered_block_sums<<<dim3(nb, n_frames), 128, 0, st>>>(g, sums, ors, ssums);
+        vqx::ordered_block_sums<<<dim3((nb + vqx::kSumWarps - 1) / vqx::kSumWarps, n_frames),
+                                  32 * vqx::kSumWarps, 0, st>>>(g, sums, ors, ssums);
         e = cudaGetLastError();
         if (timed) cudaEventRecord(ev[1], st);
     }
