@@ -72,6 +72,21 @@ class VqxProfile(ctypes.Structure):
     ]
 
 
+VQX_MAX_PLANES = 4
+
+
+class PlaneDesc(ctypes.Structure):
+    """``vqx_plane_desc``: one plane of every frame (device pointers)."""
+    _fields_ = [
+        ("ref", ctypes.c_void_p),
+        ("dist", ctypes.c_void_p),
+        ("width", ctypes.c_int),
+        ("height", ctypes.c_int),
+        ("stride", ctypes.c_size_t),
+        ("frame_pitch", ctypes.c_size_t),
+    ]
+
+
 class VqxError(RuntimeError):
     def __init__(self, status, msg):
         super().__init__(msg)
@@ -103,6 +118,8 @@ def library():
             fin = getattr(lib, "vqx_plane_%s_finish" % kind)
             fin.argtypes = [vp, vp]
             fin.restype = i
+        lib.vqx_planes_stats.argtypes = [ctypes.POINTER(PlaneDesc), i, i, i, vp, vp]
+        lib.vqx_planes_stats.restype = i
         lib.vqx_psnr_cap.argtypes = [i]
         lib.vqx_psnr_cap.restype = ctypes.c_double
         lib.vqx_status_string.argtypes = [i]
@@ -286,6 +303,25 @@ def vqx_plane_stats_noalloc(ref, dist, width=None, height=None, stride=None, bpc
     on the GPU)."""
     out, rc = _call("vqx_plane_stats_noalloc", ref, dist, width, height, stride, bpc, n_frames,
                     _stream_handle(stream), out, check)
+    return out if check else (out, rc)
+
+
+def vqx_planes_stats(planes, bpc, n_frames, stream=None, check=True):
+    """Per-frame statistics of several planes of each frame (Y, Cb, Cr ...).
+
+    ``planes``: a sequence of ``(ref, dist, width, height, stride,
+    frame_pitch)``; ref/dist are CUDA tensors or device addresses of the
+    plane in frame 0, stride and frame_pitch in bytes (frame_pitch 0 or None:
+    height * stride).  Returns ``FRAME_STATS_DTYPE`` records of shape
+    (n_frames, len(planes))."""
+    descs = (PlaneDesc * max(len(planes), 1))()
+    for k, (r, d, w, h, st, fp) in enumerate(planes):
+        descs[k] = PlaneDesc(_address(r), _address(d), w, h, st, fp or 0)
+    out = np.zeros((max(n_frames, 0), len(planes)), FRAME_STATS_DTYPE)
+    rc = library().vqx_planes_stats(descs, len(planes), bpc, n_frames, _stream_handle(stream),
+                                    out.ctypes.data if out.size else None)
+    if check and rc != VQX_OK:
+        _raise("vqx_planes_stats", rc)
     return out if check else (out, rc)
 
 

@@ -107,15 +107,15 @@ cudaError_t encode_fn(PFN_cuTensorMapEncodeTiled_v12000 *out) {
 }
 
 // A width x height x frames tensor of elem_bytes-byte elements starting at
-// base, rows `stride` bytes apart and frames height * stride apart, read in
-// bx x by x 1 boxes.
+// base, rows `stride` bytes apart and frames frame_pitch bytes apart, read
+// in bx x by x 1 boxes.
 cudaError_t encode_planes(CUtensorMap *tm, const void *base, int elem_bytes, int width, int height,
-                          size_t stride, int frames, int bx, int by) {
+                          size_t stride, size_t frame_pitch, int frames, int bx, int by) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     cudaError_t e = encode_fn(&enc);
     if (e != cudaSuccess) return e;
     const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)height, (cuuint64_t)frames};
-    const cuuint64_t strides[2] = {(cuuint64_t)stride, (cuuint64_t)stride * (cuuint64_t)height};
+    const cuuint64_t strides[2] = {(cuuint64_t)stride, (cuuint64_t)frame_pitch};
     const cuuint32_t box[3] = {(cuuint32_t)bx, (cuuint32_t)by, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
     const CUtensorMapDataType type = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -329,6 +329,21 @@ int validate(const void *ref, const void *dist, int width, int height, size_t st
     return VQX_OK;
 }
 
+// One plane of vqx_planes_stats: as validate, with its own frame pitch.
+int validate_plane(const vqx_plane_desc &d, int bpc, int n_frames, size_t *pitch) {
+    int rc = validate(d.ref, d.dist, d.width, d.height, d.stride, bpc, n_frames,
+                      reinterpret_cast<const vqx_frame_stats *>(&d));
+    if (rc != VQX_OK) return rc;
+    const size_t min_pitch = (size_t)d.height * d.stride;
+    const size_t fp = d.frame_pitch ? d.frame_pitch : min_pitch;
+    if (fp < min_pitch) return VQX_EINVAL;
+    if (bytes_per_sample(bpc) == 2 && (fp & 1u)) return VQX_EINVAL;
+    const unsigned __int128 span = (unsigned __int128)fp * (unsigned __int128)n_frames;
+    if (span > (unsigned __int128)(SIZE_MAX / 2)) return VQX_EINVAL;
+    *pitch = fp;
+    return VQX_OK;
+}
+
 // ------------------------------------------------------------------ plan
 struct Plan {
     int path = kDense;
@@ -412,26 +427,27 @@ UnitShape choose_segs(long long frames, long long max_segs, long long resident, 
 
 // max_records: at most this many stage-1 records per frame (a caller with a
 // fixed scratch); units then write one record each, and if need be the
-// frames get fewer segments.
+// frames get fewer segments.  frame_pitch: bytes from one frame to the next
+// (0: height * stride, frames back to back).
 Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width, int height,
                size_t stride, int bpc, long long frames_per_launch, int kind = kStats,
-               long long max_records = 1ll << 40) {
+               long long max_records = 1ll << 40, size_t frame_pitch = 0) {
     Plan p;
     p.bpc = bpc;
     p.variant = variant_index(bpc, kind);
     p.width = width;
     p.height = height;
     p.stride = stride;
-    p.frame_pitch = (size_t)height * stride;
+    p.frame_pitch = frame_pitch ? frame_pitch : (size_t)height * stride;
     const size_t row_bytes = (size_t)width * (size_t)bytes_per_sample(bpc);
     const bool aligned = (((uintptr_t)ref | (uintptr_t)dist) & 15u) == 0;
     const size_t frame_bytes = row_bytes * (size_t)height;
-    if (aligned && stride == row_bytes && (frame_bytes & 15u) == 0) {
+    if (aligned && stride == row_bytes && p.frame_pitch == frame_bytes && (frame_bytes & 15u) == 0) {
         p.path = kDense;
         p.work = (uint32_t)(frame_bytes >> 4);
     } else {
         // copies need 16-byte aligned rows; very narrow ones take the sample path
-        const bool pitched = aligned && (stride & 15u) == 0;
+        const bool pitched = aligned && ((stride | p.frame_pitch) & 15u) == 0;
         p.path = pitched && (row_bytes & 15u) == 0 && row_bytes >= kRowsMinBytes ? kRows
                  : pitched && width >= 64                                         ? kTiles
                                                                                   : kRowsScalar;
@@ -488,10 +504,10 @@ cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned 
     const size_t first = (size_t)frame0 * p.frame_pitch;
     const int row_elems = (int)((size_t)p.width * bytes_per_sample(BPC) / (size_t)p.tile_elem);
     cudaError_t e = encode_planes(&src.tref, ref + first, p.tile_elem, row_elems, p.height, p.stride,
-                                  frames, p.tile_bx, p.tile_by);
+                                  p.frame_pitch, frames, p.tile_bx, p.tile_by);
     if (e == cudaSuccess)
         e = encode_planes(&src.tdist, dist + first, p.tile_elem, row_elems, p.height, p.stride,
-                          frames, p.tile_bx, p.tile_by);
+                          p.frame_pitch, frames, p.tile_bx, p.tile_by);
     if (e != cudaSuccess) return e;
     src.width = row_elems;
     src.height = p.height;
@@ -843,6 +859,70 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
     rc = vqx_plane_stats_submit(ref, dist, width, height, stride, bpc, n_frames, stream, &p);
     if (rc != VQX_OK) return rc;
     return vqx_plane_stats_finish(p, out);
+}
+
+int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
+                    vqx_stream_t stream, vqx_frame_stats *out) {
+    if (!planes || n_planes < 1 || n_planes > VQX_MAX_PLANES) return VQX_EINVAL;
+    if (bpc != 8 && bpc != 10 && bpc != 12 && bpc != 16) return VQX_EBPC;
+    if (n_frames < 0) return VQX_EINVAL;
+    if (n_frames == 0) return VQX_OK;
+    if (!out) return VQX_EINVAL;
+    size_t pitch[VQX_MAX_PLANES];
+    for (int p = 0; p < n_planes; p++) {
+        const int rc = validate_plane(planes[p], bpc, n_frames, &pitch[p]);
+        if (rc != VQX_OK) return rc;
+    }
+    DeviceCtx *ctx = nullptr;
+    int rc = device_ctx(&ctx);
+    if (rc != VQX_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    Plan plan[VQX_MAX_PLANES];
+    size_t off[VQX_MAX_PLANES + 1] = {0};  // record offsets of the planes, in records
+    for (int p = 0; p < n_planes; p++) {
+        const vqx_plane_desc &d = planes[p];
+        plan[p] = make_plan(*ctx, d.ref, d.dist, d.width, d.height, d.stride, bpc, n_frames, kStats,
+                            1ll << 40, pitch[p]);
+        off[p + 1] = off[p] + records_bytes(plan[p], n_frames) / sizeof(Partial);
+    }
+    PinnedBuf rec;
+    if ((rc = acquire_pinned((size_t)n_planes * n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, off[n_planes] * sizeof(Partial), ctx->pool, st);
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    Partial *partials = (Partial *)ws;
+    for (int p = 0; e == cudaSuccess && p < n_planes; p++)
+        e = launch_stage1(plan[p], planes[p].ref, planes[p].dist, 0, n_frames, partials + off[p], st, true);
+    for (int p = 0; e == cudaSuccess && p < n_planes; p++)
+        e = launch_stage2(plan[p], n_frames, partials + off[p], (Partial *)rec.dev + (size_t)p * n_frames,
+                          st);
+    const cudaError_t ef = cudaFreeAsync(ws, st);
+    const cudaError_t es = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e != cudaSuccess) {
+        release_pinned(rec);
+        return cuda_status(e);
+    }
+    t_prof.totals.calls++;
+    t_prof.totals.kernel_launches += 2 * (uint64_t)n_planes;
+    t_prof.totals.stage1_launches += (uint64_t)n_planes;
+    const Partial *sums = (const Partial *)rec.host;
+    rc = VQX_OK;
+    for (int p = 0; p < n_planes; p++) {
+        const vqx_plane_desc &d = planes[p];
+        t_prof.totals.stage1_bytes += plane_bytes(d.width, d.height, bpc, n_frames);
+        for (int f = 0; f < n_frames; f++) {
+            vqx_frame_stats &o = out[(size_t)f * n_planes + p];
+            conclude(sums[(size_t)p * n_frames + f], bpc, d.width, d.height, &o);
+            rc = merge_status(rc, o);
+        }
+    }
+    release_pinned(rec);
+    return rc;
 }
 
 int vqx_plane_stats_host(const void *ref, const void *dist, int width, int height,

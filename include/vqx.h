@@ -147,6 +147,34 @@ int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int hei
 int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out);
 
 /*
+ * Several planes of each frame in one call (Y, Cb, Cr of 4:2:0 or 4:2:2
+ * video, at most VQX_MAX_PLANES).  Each plane has its own size, row pitch and
+ * frame pitch, so the planes may live in separate buffers or interleaved in
+ * one buffer per frame.
+ */
+#define VQX_MAX_PLANES 4
+
+typedef struct {
+    const void *ref;    /* device pointer: this plane of frame 0 of the reference */
+    const void *dist;   /* the same plane of frame 0 of the distorted video */
+    int width, height;  /* samples per row, rows (>= 1; w * h <= VQX_MAX_FRAME_PIXELS) */
+    size_t stride;      /* bytes from one row to the next (>= width * bytes per sample) */
+    size_t frame_pitch; /* bytes from this plane of frame f to that of f + 1; 0 means
+                           height * stride; otherwise at least height * stride */
+} vqx_plane_desc;
+
+/*
+ * vqx_planes_stats: vqx_plane_stats for every plane of every frame; out is a
+ * host array of n_frames * n_planes records, the record of plane p of frame
+ * f at out[f * n_planes + p].  Status codes as for vqx_plane_stats
+ * (VQX_EINVAL also for n_planes outside 1 .. VQX_MAX_PLANES or a frame pitch
+ * below height * stride, or odd, at 10 to 16 bits); nothing is launched on
+ * an argument error.  Synchronous on return.
+ */
+int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
+                    vqx_stream_t stream, vqx_frame_stats *out);
+
+/*
  * Integer psnr of one frame pair: the integer sibling of float_psnr.
  * "ADR-1440: float_psnr_hip adds its squared differences as integers ..."
  * (Alternatives) names psnr_hip as keeping one uint64 per frame; the pages

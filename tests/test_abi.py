@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr",
+    for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr", "vqx_planes_stats",
               "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
               "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
         assert n in names
@@ -109,6 +109,28 @@ def test_submit_finish_empty_and_null(lib):
     assert so.vqx_plane_int_psnr(None, None, 0, 0, 0, 8, 0, None, None) == 0
     p = lib.vqx_plane_stats_submit(np.zeros((0, 4, 4), np.uint16), np.zeros((0, 4, 4), np.uint16))
     assert p.finish().size == 0
+
+
+def test_planes_argument_errors_need_no_gpu(lib):
+    so = lib.library()
+    out = (ctypes.c_char * (112 * 16))()
+
+    def call(descs, n_planes=None, bpc=16, n_frames=2):
+        arr = (lib.PlaneDesc * max(len(descs), 1))(*descs)
+        return so.vqx_planes_stats(arr, len(descs) if n_planes is None else n_planes, bpc, n_frames,
+                                   None, out)
+
+    y = lib.PlaneDesc(FAKE, FAKE, 64, 4, 128, 0)
+    c = lib.PlaneDesc(FAKE, FAKE, 32, 2, 64, 0)
+    assert call([y, c, c], n_planes=0) == -1
+    assert call([y, c, c, c, c]) == -1  # more than VQX_MAX_PLANES
+    assert call([y, c], bpc=9) == -2
+    assert call([y, lib.PlaneDesc(FAKE, FAKE, 32, 2, 64, 100)]) == -1  # pitch below height * stride
+    assert call([y, lib.PlaneDesc(FAKE, FAKE, 32, 2, 64, 129)]) == -1  # odd pitch at 16 bits
+    assert call([y, lib.PlaneDesc(FAKE + 1, FAKE, 32, 2, 64, 0)]) == -1  # odd base at 16 bits
+    assert call([y], n_frames=0) == 0
+    assert so.vqx_planes_stats(None, 1, 16, 1, None, out) == -1
+    assert ctypes.sizeof(lib.PlaneDesc) == 40
 
 
 def test_empty_batch_is_ok_without_gpu(lib):
