@@ -232,66 +232,74 @@ struct OrdWork {
 constexpr int kOrdBatch = 8;  // chunks of 32 blocks loaded at once by the one-warp kernels
 constexpr int kOrdOut = 8;    // words per frame of the ordered kernels' output
 
-// Grid (frames, 3), one warp: prefix sums over the blocks of one sequence
-// and the class of every block, cls[(f * 3 + q) * nb + b]; the q = 0 warp
-// also adds the blocks' sample sums into out[f * kOrdOut + 6, 7].  The
-// blocks go in chunks of 32 (one per lane, coalesced), the prefix by a warp
-// scan.  A single-binade block whose terms are all multiples of the
-// binade's ulp is exact.  Every tabulated block is appended to work (count
-// in *n_work, which starts at 0).
+// Grid (frames, 3), kClassThreads threads: prefix sums over the blocks of
+// one sequence and the class of every block, cls[(f * 3 + q) * nb + b]; the
+// q = 0 CTA also adds the blocks' sample sums into out[f * kOrdOut + 6, 7].
+// Thread t takes a run of consecutive blocks; the runs' sums are scanned
+// across the CTA (warp scans, then the warps' totals), and each thread walks
+// its run from its exclusive prefix.  A single-binade block whose terms are
+// all multiples of the binade's ulp is exact.  Every tabulated block is
+// appended to work (count in *n_work, which starts at 0).
+constexpr int kClassThreads = 512;
 
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kClassThreads)
     ordered_classify(const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
                      const uint32_t *__restrict__ ssums, int nb, int *__restrict__ cls,
                      OrdWork *__restrict__ work, int *__restrict__ n_work, u64 *__restrict__ out) {
-    const int f = blockIdx.x, q = blockIdx.y, lane = threadIdx.x;
-    u64 base = 0;  // prefix of the chunk's first block
-    u64 sr = 0, sd = 0;
-    for (int cb = 0; cb < nb; cb += 32 * kOrdBatch) {
-        u64 Tb[kOrdBatch];
-        uint32_t Ob[kOrdBatch];
-#pragma unroll
-        for (int u = 0; u < kOrdBatch; u++) {  // all loads first, then the chunks in order
-            const int b = cb + 32 * u + lane;
-            const size_t in = ((size_t)f * nb + b) * kOrdSeqs + q;
-            Tb[u] = b < nb ? sums[in] : 0;
-            Ob[u] = b < nb ? ors[in] : 0;
-            if (q == 0 && b < nb) {
-                sr += ssums[((size_t)f * nb + b) * 2];
-                sd += ssums[((size_t)f * nb + b) * 2 + 1];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kOrdBatch; u++) {
-            const int b = cb + 32 * u + lane;
-            const bool valid = b < nb;
-            const u64 T = Tb[u];
-            u64 incl = T;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            const u64 P = base + incl - T, P1 = P + T;
-            int c = kOrdReplay;
-            if (P1 < kTwo53) {
-                c = kOrdExact;
-            } else if (P >= kTwo53 + kOrdMargin &&
-                       binade_of(P - kOrdMargin) == binade_of(P1 + kOrdMargin)) {
-                c = binade_of(P) - 52;
-                // the running sum is a multiple of 2^c here; so are the terms?
-                if ((Ob[u] & ((1u << c) - 1)) == 0) c = kOrdExact;
-            }
-            const bool tab = valid && c != kOrdExact && c != kOrdReplay;
-            const unsigned m = __ballot_sync(0xffffffffu, tab);
-            int first = 0;
-            if (lane == 0 && m) first = atomicAdd(n_work, __popc(m));
-            first = __shfl_sync(0xffffffffu, first, 0);
-            if (valid) cls[((size_t)f * kOrdSeqs + q) * nb + b] = c;
-            if (tab) work[first + __popc(m & ((1u << lane) - 1))] = OrdWork{f, q, b};
-            base = __shfl_sync(0xffffffffu, P1, 31);
+    constexpr int kWarps = kClassThreads / 32;
+    const int f = blockIdx.x, q = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int per = (nb + kClassThreads - 1) / kClassThreads;
+    const int b0 = min(t * per, nb), b1 = min(b0 + per, nb);
+    const size_t row = (size_t)f * nb;
+    u64 mine = 0, sr = 0, sd = 0;
+    for (int b = b0; b < b1; b++) {
+        mine += sums[(row + b) * kOrdSeqs + q];
+        if (q == 0) {
+            sr += ssums[(row + b) * 2];
+            sd += ssums[(row + b) * 2 + 1];
         }
     }
+    // exclusive prefix of this thread's run
+    u64 incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const u64 v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    __shared__ u64 wsum[kWarps];
+    __shared__ int wcount[kWarps];
+    __shared__ int wbase[kWarps];
+    __shared__ u64 s2[kWarps][2];
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    u64 before = 0;
+    for (int w = 0; w < warp; w++) before += wsum[w];
+    u64 P = before + incl - mine;
+    // classify the run, counting the tabulated blocks
+    int ntab = 0;
+    for (int b = b0; b < b1; b++) {
+        const size_t in = (row + b) * kOrdSeqs + q;
+        const u64 T = sums[in], P1 = P + T;
+        int c = kOrdReplay;
+        if (P1 < kTwo53) {
+            c = kOrdExact;
+        } else if (P >= kTwo53 + kOrdMargin && binade_of(P - kOrdMargin) == binade_of(P1 + kOrdMargin)) {
+            c = binade_of(P) - 52;
+            // the running sum is a multiple of 2^c here; so are the terms?
+            if ((ors[in] & ((1u << c) - 1)) == 0) c = kOrdExact;
+        }
+        cls[((size_t)f * kOrdSeqs + q) * nb + b] = c;
+        ntab += c != kOrdExact && c != kOrdReplay;
+        P = P1;
+    }
+    // places in the work list: a scan of the counts, one atomic per CTA
+    int cincl = ntab;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, cincl, o);
+        if (lane >= o) cincl += v;
+    }
+    if (lane == 31) wcount[warp] = cincl;
     if (q == 0) {
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) {
@@ -299,9 +307,34 @@ __global__ void __launch_bounds__(32)
             sd += __shfl_xor_sync(0xffffffffu, sd, sh);
         }
         if (lane == 0) {
-            out[(size_t)f * kOrdOut + 6] = sr;
-            out[(size_t)f * kOrdOut + 7] = sd;
+            s2[warp][0] = sr;
+            s2[warp][1] = sd;
         }
+    }
+    __syncthreads();
+    if (t == 0) {
+        int total = 0;
+        for (int w = 0; w < kWarps; w++) {
+            wbase[w] = total;
+            total += wcount[w];
+        }
+        const int first = total ? atomicAdd(n_work, total) : 0;
+        for (int w = 0; w < kWarps; w++) wbase[w] += first;
+        if (q == 0) {
+            u64 a = 0, d = 0;
+            for (int w = 0; w < kWarps; w++) {
+                a += s2[w][0];
+                d += s2[w][1];
+            }
+            out[(size_t)f * kOrdOut + 6] = a;
+            out[(size_t)f * kOrdOut + 7] = d;
+        }
+    }
+    __syncthreads();
+    int slot = wbase[warp] + cincl - ntab;
+    for (int b = b0; b < b1 && ntab; b++) {
+        const int c = cls[((size_t)f * kOrdSeqs + q) * nb + b];
+        if (c != kOrdExact && c != kOrdReplay) work[slot++] = OrdWork{f, q, b};
     }
 }
 

@@ -1090,7 +1090,7 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
         if (timed) cudaEventRecord(ev[1], st);
     }
     if (e == cudaSuccess) {
-        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(
+        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), vqx::kClassThreads, 0, st>>>(
             sums, ors, ssums, nb, cls, work, n_work, (u64 *)res.dev);
         e = cudaGetLastError();
     }
