@@ -614,6 +614,39 @@ __device__ __forceinline__ void consumer_reduce_store(const u64 (&t)[6], u64 (*s
     consumer_sync<NCW>();  // scratch is reused by the next unit
 }
 
+// Many small dense frames: each warp takes whole frames (frame frame0 + k
+// for k its warp index, then every total-warps-th), reads each one as
+// frame_vecs contiguous 16-byte vectors of each plane, and writes the frame's
+// single record itself, partials[frame].  No shared memory and no block
+// barrier: a frame's end costs one warp's reduction, where a frame split
+// across a whole CTA costs sixteen.
+constexpr int kFrameWarps = 8;  // warps per CTA of fused_frames
+
+template <int BPC, class Acc = TermSums<BPC>>
+__global__ void __launch_bounds__(32 * kFrameWarps)
+    fused_frames(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
+                 size_t frame_pitch, uint32_t frame_vecs, int frames, int frame0,
+                 Partial *__restrict__ partials) {
+    allow_dependent_launch();
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * kFrameWarps;
+    for (int k = blockIdx.x * kFrameWarps + (threadIdx.x >> 5); k < frames; k += warps) {
+        const int f = frame0 + k;
+        const unsigned char *r = ref + (size_t)f * frame_pitch;
+        const unsigned char *d = dist + (size_t)f * frame_pitch;
+        Acc acc;
+        for (uint32_t c = lane; c < frame_vecs;) {
+            const uint32_t stop = min(frame_vecs, c + Acc::kFlushVecs * 32);
+#pragma unroll 4
+            for (; c < stop; c += 32) acc.vec(ld_stream16(r + 16 * (size_t)c), ld_stream16(d + 16 * (size_t)c));
+            acc.flush();
+        }
+        u64 t[6];
+        acc.totals(t);
+        warp_reduce_store(t, partials[f].v);
+    }
+}
+
 // Where the persistent pipeline's stages come from.  A source maps a unit
 // (a (frame, segment) pair) to its stages and issues a stage's two copies
 // (reference and distorted plane), arming the stage's full mbarrier with the

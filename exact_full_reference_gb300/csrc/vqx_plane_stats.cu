@@ -43,8 +43,15 @@ int cuda_status(cudaError_t e) {
 // kRows: padded rows of whole 16-byte vectors, at least kRowsMinBytes long,
 // on 16-byte aligned bases and pitch (1-D bulk copies of row pieces);
 // kTiles: other rows on 16-byte aligned bases and pitch (tensor-map boxes);
-// kRowsScalar: anything else (sample loads).
-enum Path { kDense = 0, kTiles = 1, kRowsScalar = 2, kRows = 3, kPaths = 4 };
+// kRowsScalar: anything else (sample loads);
+// kFrames: many dense frames of at most kFramesMaxVecs vectors (a warp per
+// frame, plain 16-byte loads).  Measured: 64x64 16-bit frames (512 vectors)
+// stream at 0.70 of the copy bandwidth this way from about 1200 frames on,
+// 0.38 through the TMA pipeline, whose unit ends dominate such frames; from
+// 128x128 16-bit (2048 vectors) and for every 8-bit size tried the pipeline
+// is faster.
+enum Path { kDense = 0, kTiles = 1, kRowsScalar = 2, kRows = 3, kFrames = 4, kPaths = 5 };
+constexpr uint32_t kFramesMaxVecs = 1024;  // 16 KB of each plane
 constexpr size_t kRowsMinBytes = 512;
 
 // What a call computes: the fused statistics, or the integer psnr.  Up to 12
@@ -82,6 +89,8 @@ Stage1Shape stage1_shape(int path) {
     case kRows:
         return {(const void *)stream_kernel<BPC, vqx::RowSource, Acc>(), vqx::kTmaThreads,
                 vqx::kTmaSmem};
+    case kFrames:
+        return {(const void *)vqx::fused_frames<BPC, Acc>, 32 * vqx::kFrameWarps, 0};
     default: return {(const void *)vqx::fused_rows<BPC, false, Acc>, vqx::kThreads, 0};
     }
 }
@@ -445,6 +454,8 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
     if (aligned && stride == row_bytes && p.frame_pitch == frame_bytes && (frame_bytes & 15u) == 0) {
         p.path = kDense;
         p.work = (uint32_t)(frame_bytes >> 4);
+        // many small frames (8 or more per SM): a warp per frame
+        if (p.work <= kFramesMaxVecs && frames_per_launch >= 8ll * c.sms) p.path = kFrames;
     } else {
         // copies need 16-byte aligned rows; very narrow ones take the sample path
         const bool pitched = aligned && ((stride | p.frame_pitch) & 15u) == 0;
@@ -454,6 +465,12 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
         p.work = (uint32_t)height;
     }
     p.resident = (long long)c.sms * c.resident[p.path][p.variant];
+    if (p.path == kFrames) {  // one record per frame, written by its warp
+        p.segs = 1;
+        p.seg_work = p.work;
+        p.rec_per_unit = 1;
+        return p;
+    }
     if (p.path == kTiles) {
         // rows per CTA were the batch spread over every resident CTA
         long long max_by = (long long)height * frames_per_launch / (p.resident > 0 ? p.resident : 1);
@@ -529,6 +546,14 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     memset(&cfg, 0, sizeof cfg);
     const long long units = (long long)frames * p.segs;
     cfg.stream = st;
+    if (p.path == kFrames) {
+        // no programmatic dependency here: fused_frames stores without waiting
+        const long long need = ((long long)frames + vqx::kFrameWarps - 1) / vqx::kFrameWarps;
+        cfg.gridDim = dim3((unsigned)(need < p.resident ? need : p.resident));
+        cfg.blockDim = dim3(32 * vqx::kFrameWarps);
+        return cudaLaunchKernelEx(&cfg, vqx::fused_frames<BPC, Acc>, ref, dist, p.frame_pitch, p.work,
+                                  frames, frame0, partials);
+    }
     if (p.path == kRowsScalar) {
         cfg.gridDim = dim3((unsigned)units);
         cfg.blockDim = dim3(vqx::kThreads);

@@ -281,3 +281,20 @@ def test_submit_profiles_on_the_finishing_thread(lib):
     prof = lib.profile_read(reset=True)
     lib.profile_enable(False)
     assert prof["calls"] == 4 and prof["stage1_launches"] == 4 and prof["stage1_ms"] > 0
+
+
+@pytest.mark.parametrize("bpc,w,h,n", [(16, 64, 64, 1300), (8, 96, 64, 2000), (10, 64, 32, 1500),
+                                       (12, 32, 48, 1250)])
+def test_many_tiny_dense_frames(lib, orc, bpc, w, h, n):
+    """Batches of many frames of at most 16 KB per plane: a warp per frame
+    (the many-small-frames path), each frame's record written by its warp."""
+    rng = np.random.Generator(np.random.PCG64(n + w + bpc))
+    dt = np.uint8 if bpc == 8 else np.uint16
+    ref = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    dist = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    rec, sc, un = run_case(lib, orc, ref, dist, bpc)
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    ip = lib.vqx_plane_int_psnr(pr, pd, w, h, stride, bpc, n)
+    assert [int(x) for x in ip["sse"][:50]] == [int(x) for x in orc.int_psnr(rb, db, w, h, stride, bpc, 50)["sse"]]
+    na = lib.vqx_plane_stats_noalloc(pr, pd, w, h, stride, bpc, n)
+    assert na.tobytes() == rec.tobytes()
