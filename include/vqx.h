@@ -30,8 +30,20 @@
  * and 16 = one little-endian uint16 per sample (the low bpc bits; a sample
  * of 2^bpc or more is an error, VQX_ERANGE).  Row y of frame f starts
  * f * height * stride + y * stride bytes after the plane's base pointer;
- * both planes use the same stride and the same frame pitch.  Planes of
- * uint16 samples must be 2-byte aligned (base and stride).
+ * both planes use the same stride and the same frame pitch (with
+ * vqx_planes_stats each plane descriptor gives its own, and a frame pitch).
+ * Planes of uint16 samples must be 2-byte aligned (base and stride).
+ *
+ * Entry points:
+ *   vqx_plane_stats            device planes, blocking
+ *   vqx_plane_stats_submit / _finish   the same in two halves (pipelining)
+ *   vqx_planes_stats           several planes of every frame (Y, Cb, Cr)
+ *   vqx_plane_stats_host       planes in host memory (copies overlapped)
+ *   vqx_plane_stats_ordered    doubles equal to the CPU's also past 2^53 units
+ *   vqx_plane_stats_noalloc    no allocation at call time (fixed scratch)
+ *   vqx_plane_int_psnr (+ _submit / _finish)   the integer psnr
+ *   vqx_psnr_cap, vqx_status_string, vqx_last_cuda_error,
+ *   vqx_profile_enable / vqx_profile_read      helpers and counters
  */
 #ifndef VQX_H
 #define VQX_H
@@ -257,10 +269,13 @@ const char *vqx_status_string(int status);
 int vqx_last_cuda_error(void);
 
 /* Per-thread counters of the library's work.  Calls, kernel launches and
- * bytes read are always counted (both entry points).  Device times are
- * measured only while enabled: each vqx_plane_stats call then records CUDA
- * events on the caller's stream around its fused kernel and its per-frame
- * kernel.  vqx_profile_read returns the totals since the last reset. */
+ * bytes read are always counted.  Device times are measured only while
+ * enabled: a vqx_plane_stats or vqx_plane_int_psnr batch (submitted on a
+ * thread with profiling on; counted on the thread that finishes it) then
+ * records CUDA events on the caller's stream around its fused kernel and
+ * its per-frame kernel, and vqx_plane_stats_ordered around its block-sum
+ * kernel (counted as its stage-1 launch).  vqx_profile_read returns the
+ * totals since the last reset. */
 typedef struct {
     uint64_t calls;            /* successful calls */
     uint64_t kernel_launches;  /* library kernels launched by those calls */
