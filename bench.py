@@ -382,11 +382,14 @@ def run_ours(args, wlo):
     so = vqx.library()
     out = np.zeros(n, vqx.INT_PSNR_DTYPE if args.op == "int_psnr" else vqx.FRAME_STATS_DTYPE)
     out_p = out.ctypes.data
-    submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh)
+    # the planes are written once, before any step: batches may start reading
+    # them while the batch ahead finishes
+    submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh,
+                   vqx.VQX_SUBMIT_PLANES_READY)
     if args.op == "ordered":
         # a blocking call per step: submit runs it, finish has nothing left to do
         def submit_fn(*a):
-            return so.vqx_plane_stats_ordered(*a[:-1], out_p)
+            return so.vqx_plane_stats_ordered(*a[:-2], out_p)
 
         def finish_fn(handle, out_ptr):
             return 0
@@ -568,7 +571,8 @@ def run_ours(args, wlo):
                        "pipeline": ("one blocking vqx_plane_stats_ordered call a step"
                                     if args.op == "ordered" else
                                     "batch i + 1 submitted before batch i is finished "
-                                    "(vqx_plane_%s_submit / _finish)" % args.op),
+                                    "(vqx_plane_%s_submit with VQX_SUBMIT_PLANES_READY / "
+                                    "_finish)" % args.op),
                        "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e,
             "roofline": roofline,

@@ -73,6 +73,7 @@ class VqxProfile(ctypes.Structure):
 
 
 VQX_MAX_PLANES = 4
+VQX_SUBMIT_PLANES_READY = 1
 
 
 class PlaneDesc(ctypes.Structure):
@@ -113,7 +114,7 @@ def library():
             fn.restype = i
         for kind in ("stats", "int_psnr"):
             sub = getattr(lib, "vqx_plane_%s_submit" % kind)
-            sub.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.POINTER(vp)]
+            sub.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.c_uint, ctypes.POINTER(vp)]
             sub.restype = i
             fin = getattr(lib, "vqx_plane_%s_finish" % kind)
             fin.argtypes = [vp, vp]
@@ -244,28 +245,29 @@ class Pending:
         return out if check else (out, rc)
 
 
-def _submit(kind, ref, dist, width, height, stride, bpc, n_frames, stream):
+def _submit(kind, ref, dist, width, height, stride, bpc, n_frames, stream, flags):
     width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
     handle = ctypes.c_void_p()
     name = "vqx_plane_%s_submit" % kind
     rc = getattr(library(), name)(_address(ref), _address(dist), width, height, stride, bpc,
-                                  n_frames, _stream_handle(stream), ctypes.byref(handle))
+                                  n_frames, _stream_handle(stream), flags, ctypes.byref(handle))
     if rc != VQX_OK:
         _raise(name, rc)
     return Pending(handle.value, max(n_frames, 0), (ref, dist), kind)
 
 
 def vqx_plane_stats_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
-                           n_frames=None, stream=None):
+                           n_frames=None, stream=None, flags=0):
     """Enqueue a batch of device planes without waiting; returns a
-    ``Pending`` whose ``finish()`` gives what ``vqx_plane_stats`` would."""
-    return _submit("stats", ref, dist, width, height, stride, bpc, n_frames, stream)
+    ``Pending`` whose ``finish()`` gives what ``vqx_plane_stats`` would.
+    ``flags``: 0 or ``VQX_SUBMIT_PLANES_READY``."""
+    return _submit("stats", ref, dist, width, height, stride, bpc, n_frames, stream, flags)
 
 
 def vqx_plane_int_psnr_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
-                              n_frames=None, stream=None):
+                              n_frames=None, stream=None, flags=0):
     """The same for the integer psnr (``finish()`` gives ``INT_PSNR_DTYPE``)."""
-    return _submit("int_psnr", ref, dist, width, height, stride, bpc, n_frames, stream)
+    return _submit("int_psnr", ref, dist, width, height, stride, bpc, n_frames, stream, flags)
 
 
 def vqx_plane_int_psnr(ref, dist, width=None, height=None, stride=None, bpc=16, n_frames=None,

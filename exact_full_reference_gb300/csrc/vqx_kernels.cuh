@@ -815,6 +815,10 @@ struct TileSource {
 // nothing, still writes (flagged) records for its remaining units, and the
 // producer waits (bounded) for the copies it issued before the CTA exits.
 //
+// planes_ready: the caller guarantees that no kernel ahead of this one on the
+// stream is still writing the planes when it lets this one start, so the
+// producer streams without waiting for it (record stores still wait).
+//
 // Records: with warp_records every consumer warp writes its own record of
 // each unit (record r of the source becomes records r * NCW .. r * NCW +
 // NCW - 1) and ends a unit without waiting for the others; otherwise the
@@ -822,7 +826,7 @@ struct TileSource {
 template <int BPC, int NCW, int SV, int STAGES, class Src, class Acc = TermSums<BPC>>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     fused_stream_tma(const __grid_constant__ Src src, int units, int warp_records,
-                     Partial *__restrict__ partials) {
+                     int planes_ready, Partial *__restrict__ partials) {
     constexpr uint32_t kStageBytes = SV * 16;  // per plane
     constexpr uint32_t kPerThread = SV / (NCW * 32);
     static_assert(SV % (NCW * 32) == 0, "a full stage gives every consumer thread equal work");
@@ -849,8 +853,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         if (lane != 0) return;
         // Launched as a programmatic dependent, this grid may be resident
         // before the kernel ahead of it on the stream has finished: read
-        // nothing it may still be writing (returns at once otherwise).
-        grid_dependency_wait();
+        // nothing it may still be writing (returns at once otherwise),
+        // unless the caller declared the planes complete already.
+        if (!planes_ready) grid_dependency_wait();
         bool ok = true;
         uint32_t k = 0;
         for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {

@@ -515,7 +515,7 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
 template <int BPC, class Acc>
 cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned char *ref,
                          const unsigned char *dist, int frame0, int frames, int units,
-                         Partial *partials) {
+                         Partial *partials, bool planes_ready) {
     vqx::TileSource src;
     memset(&src, 0, sizeof src);
     const size_t first = (size_t)frame0 * p.frame_pitch;
@@ -535,13 +535,13 @@ cudaError_t launch_tiles(cudaLaunchConfig_t &cfg, const Plan &p, const unsigned 
     src.by = p.tile_by;
     src.box_vecs = (uint32_t)((size_t)p.tile_bx * p.tile_by * p.tile_elem / 16);
     return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::TileSource, Acc>(), src, units,
-                              (int)(p.rec_per_unit > 1), partials);
+                              (int)(p.rec_per_unit > 1), (int)planes_ready, partials);
 }
 
 template <int BPC, class Acc>
 cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const unsigned char *dist,
                               int frame0, int frames, Partial *partials, cudaStream_t st,
-                              bool overlap) {
+                              bool overlap, bool planes_ready) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     const long long units = (long long)frames * p.segs;
@@ -582,7 +582,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.segs = p.segs;
         src.frame0 = frame0;
         return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::DenseSource, Acc>(), src, (int)units,
-                                  (int)(p.rec_per_unit > 1), partials);
+                                  (int)(p.rec_per_unit > 1), (int)planes_ready, partials);
     }
     if (p.path == kRows) {
         vqx::RowSource src;
@@ -596,24 +596,32 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
         src.segs = p.segs;
         src.frame0 = frame0;
         return cudaLaunchKernelEx(&cfg, stream_kernel<BPC, vqx::RowSource, Acc>(), src, (int)units,
-                                  (int)(p.rec_per_unit > 1), partials);
+                                  (int)(p.rec_per_unit > 1), (int)planes_ready, partials);
     }
-    return launch_tiles<BPC, Acc>(cfg, p, ref, dist, frame0, frames, (int)units, partials);
+    return launch_tiles<BPC, Acc>(cfg, p, ref, dist, frame0, frames, (int)units, partials,
+                                  planes_ready);
 }
 
 // overlap: launch the persistent kernels as programmatic dependents of the
 // kernel before them on the stream, so that their CTAs are set up while that
-// kernel finishes; they wait for it before their first load and store.
+// kernel finishes; they wait for it before their first load (unless
+// planes_ready) and before their first store.
 cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int frame0,
-                          int frames, Partial *partials, cudaStream_t st, bool overlap = false) {
+                          int frames, Partial *partials, cudaStream_t st, bool overlap = false,
+                          bool planes_ready = false) {
     const unsigned char *r = (const unsigned char *)ref;
     const unsigned char *d = (const unsigned char *)dist;
     switch (p.variant) {
-    case 0: return launch_stage1_bpc<8, vqx::TermSums<8>>(p, r, d, frame0, frames, partials, st, overlap);
-    case 1: return launch_stage1_bpc<10, vqx::TermSums<10>>(p, r, d, frame0, frames, partials, st, overlap);
-    case 2: return launch_stage1_bpc<12, vqx::TermSums<12>>(p, r, d, frame0, frames, partials, st, overlap);
-    case 3: return launch_stage1_bpc<16, vqx::TermSums<16>>(p, r, d, frame0, frames, partials, st, overlap);
-    default: return launch_stage1_bpc<16, vqx::SseSums16>(p, r, d, frame0, frames, partials, st, overlap);
+    case 0: return launch_stage1_bpc<8, vqx::TermSums<8>>(p, r, d, frame0, frames, partials, st, overlap,
+                                                       planes_ready);
+    case 1: return launch_stage1_bpc<10, vqx::TermSums<10>>(p, r, d, frame0, frames, partials, st, overlap,
+                                                       planes_ready);
+    case 2: return launch_stage1_bpc<12, vqx::TermSums<12>>(p, r, d, frame0, frames, partials, st, overlap,
+                                                       planes_ready);
+    case 3: return launch_stage1_bpc<16, vqx::TermSums<16>>(p, r, d, frame0, frames, partials, st, overlap,
+                                                       planes_ready);
+    default: return launch_stage1_bpc<16, vqx::SseSums16>(p, r, d, frame0, frames, partials, st, overlap,
+                                                       planes_ready);
     }
 }
 
@@ -751,7 +759,8 @@ void vqx_profile_read(vqx_profile *out, int reset) {
 namespace {
 
 int submit_impl(const void *ref, const void *dist, int width, int height, size_t stride, int bpc,
-                int n_frames, vqx_stream_t stream, int kind, vqx_pending **pending) {
+                int n_frames, vqx_stream_t stream, int kind, unsigned flags, vqx_pending **pending) {
+    if (flags & ~VQX_SUBMIT_PLANES_READY) return VQX_EINVAL;
     if (!pending) return VQX_EINVAL;
     *pending = nullptr;
     // out is checked by vqx_plane_stats_finish; any non-null pointer passes here
@@ -778,7 +787,8 @@ int submit_impl(const void *ref, const void *dist, int width, int height, size_t
     }
     Partial *partials = (Partial *)ws;
     if (p->timed) cudaEventRecord(p->ev[0], st);
-    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st, true);
+    e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st, true,
+                      (flags & VQX_SUBMIT_PLANES_READY) != 0);
     if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[1], st);
     if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, (Partial *)p->rec.dev, st);
     if (e == cudaSuccess && p->timed) cudaEventRecord(p->ev[2], st);
@@ -845,8 +855,9 @@ extern "C" {
 
 int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                           vqx_pending **pending) {
-    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kStats, pending);
+                           unsigned flags, vqx_pending **pending) {
+    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kStats, flags,
+                       pending);
 }
 
 int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out) {
@@ -855,8 +866,8 @@ int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out) {
 
 int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int height,
                               size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                              vqx_pending **pending) {
-    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr,
+                              unsigned flags, vqx_pending **pending) {
+    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr, flags,
                        pending);
 }
 
@@ -870,7 +881,7 @@ int vqx_plane_int_psnr(const void *ref, const void *dist, int width, int height,
                       reinterpret_cast<const vqx_frame_stats *>(out));
     if (rc != VQX_OK || n_frames == 0) return rc;
     vqx_pending *p = nullptr;
-    rc = submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr, &p);
+    rc = submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kIntPsnr, 0u, &p);
     if (rc != VQX_OK) return rc;
     return finish_impl(p, kIntPsnr, out);
 }
@@ -881,7 +892,7 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
     int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
     if (rc != VQX_OK || n_frames == 0) return rc;
     vqx_pending *p = nullptr;
-    rc = vqx_plane_stats_submit(ref, dist, width, height, stride, bpc, n_frames, stream, &p);
+    rc = vqx_plane_stats_submit(ref, dist, width, height, stride, bpc, n_frames, stream, 0u, &p);
     if (rc != VQX_OK) return rc;
     return vqx_plane_stats_finish(p, out);
 }

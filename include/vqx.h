@@ -136,11 +136,22 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
  * waits on and concludes this one).
  *
  * vqx_plane_stats_submit takes the arguments of vqx_plane_stats without
- * `out`, checks them (same status codes; on an error nothing is enqueued and
- * *pending is set to NULL), enqueues the batch's kernels on `stream` and
+ * `out`, plus flags (0 or VQX_SUBMIT_PLANES_READY), checks them (same status
+ * codes, and VQX_EINVAL for an unknown flag; on an error nothing is enqueued
+ * and *pending is set to NULL), enqueues the batch's kernels on `stream` and
  * returns without waiting.  *pending receives a library-owned handle, NULL
  * for an empty batch.  ref and dist must stay valid and unchanged until
  * vqx_plane_stats_finish on that handle has returned.
+ *
+ * The batch's main kernel is a programmatic dependent of the kernel before it
+ * on the stream: it is set up while that kernel finishes, and by default
+ * waits for it to complete before reading the planes.  VQX_SUBMIT_PLANES_READY
+ * tells it not to wait before reading (it still waits before writing
+ * anything): pass it when no kernel ahead on the stream that lets its
+ * dependents start early (programmatic dependent launch) is still writing
+ * these planes, for instance when the planes were written before the batch
+ * ahead was enqueued.  Consecutive batches then overlap one's end with the
+ * next one's start.  Results are the same either way.
  *
  * vqx_plane_stats_finish waits for the batch, writes its n_frames records to
  * out (host array, caller-owned) exactly as vqx_plane_stats would and
@@ -152,9 +163,11 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
  */
 typedef struct vqx_pending vqx_pending;
 
+#define VQX_SUBMIT_PLANES_READY 1u
+
 int vqx_plane_stats_submit(const void *ref, const void *dist, int width, int height,
                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                           vqx_pending **pending);
+                           unsigned flags, vqx_pending **pending);
 
 int vqx_plane_stats_finish(vqx_pending *pending, vqx_frame_stats *out);
 
@@ -215,7 +228,7 @@ int vqx_plane_int_psnr(const void *ref, const void *dist, int width, int height,
  * from one pair is not accepted by the other: VQX_EINVAL, handle released). */
 int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int height,
                               size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                              vqx_pending **pending);
+                              unsigned flags, vqx_pending **pending);
 
 int vqx_plane_int_psnr_finish(vqx_pending *pending, vqx_int_psnr_stats *out);
 

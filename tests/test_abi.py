@@ -92,7 +92,7 @@ def test_submit_argument_errors_need_no_gpu(lib, args, status):
     so = lib.library()
     handle = ctypes.c_void_p(1234)
     rc = so.vqx_plane_stats_submit(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
-                                   a["stride"], a["bpc"], a["n_frames"], None, ctypes.byref(handle))
+                                   a["stride"], a["bpc"], a["n_frames"], None, 0, ctypes.byref(handle))
     assert rc == status
     assert handle.value is None  # cleared on every error
 
@@ -100,11 +100,14 @@ def test_submit_argument_errors_need_no_gpu(lib, args, status):
 def test_submit_finish_empty_and_null(lib):
     so = lib.library()
     handle = ctypes.c_void_p(1234)
-    assert so.vqx_plane_stats_submit(None, None, 0, 0, 0, 16, 0, None, ctypes.byref(handle)) == 0
+    assert so.vqx_plane_stats_submit(None, None, 0, 0, 0, 16, 0, None, 0, ctypes.byref(handle)) == 0
     assert handle.value is None
     assert so.vqx_plane_stats_finish(None, None) == 0
-    assert so.vqx_plane_stats_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, None) == -1
-    assert so.vqx_plane_int_psnr_submit(None, None, 0, 0, 0, 12, 0, None, ctypes.byref(handle)) == 0
+    assert so.vqx_plane_stats_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, 0, None) == -1
+    # an unknown flag is refused before anything else
+    assert so.vqx_plane_stats_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, 2, ctypes.byref(handle)) == -1
+    assert handle.value is None
+    assert so.vqx_plane_int_psnr_submit(None, None, 0, 0, 0, 12, 0, None, 0, ctypes.byref(handle)) == 0
     assert handle.value is None and so.vqx_plane_int_psnr_finish(None, None) == 0
     assert so.vqx_plane_int_psnr(None, None, 0, 0, 0, 8, 0, None, None) == 0
     p = lib.vqx_plane_stats_submit(np.zeros((0, 4, 4), np.uint16), np.zeros((0, 4, 4), np.uint16))
