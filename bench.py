@@ -197,7 +197,7 @@ def kernel_source_digest():
 
 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "fused_stream_traffic.json")
-KERNEL_LABEL = "fused_stream_tma<%d, 16, 1536, 2, DenseSource>"
+KERNEL_LABEL = "fused_stream_tma<%d, 16, 1536, 2, DenseSource, TermSums<%d>>"
 # the capture the traffic record is taken from (the plain command runs first)
 TRAFFIC_CAPTURE = ("ncu --set full --clock-control none -k regex:fused_stream -s 3 -c 1 "
                    "-o prof_fused_stream python bench.py --steps 5 --warmup 3 --no-cpu --no-e2e")
@@ -244,7 +244,7 @@ def write_traffic_record(report, wlo):
     rd, wr = val("dram__bytes_read.sum"), val("dram__bytes_write.sum")
     bps = 1 if wlo.bpc == 8 else 2
     rec = {
-        "kernel": KERNEL_LABEL % wlo.bpc,
+        "kernel": KERNEL_LABEL % (wlo.bpc, wlo.bpc),
         "source_sha256": kernel_source_digest(),
         "per_launch_bytes": {wlo.name: rd + wr},
         "dram_bytes_read": rd,
@@ -494,7 +494,7 @@ def run_ours(args, wlo):
     bytes_per_launch = prof["stage1_bytes"] / launches
     achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
     traffic = recorded_traffic(wlo.name) if args.op == "stats" else None
-    label = KERNEL_LABEL % wlo.bpc
+    label = KERNEL_LABEL % (wlo.bpc, wlo.bpc)
     if args.op == "int_psnr" and wlo.bpc == 16:
         label = "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
     if args.op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
