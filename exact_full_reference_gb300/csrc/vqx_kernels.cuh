@@ -502,17 +502,15 @@ __device__ __forceinline__ void block_reduce_store(u64 (&t)[6], u64 *dst) {
 }
 
 // ---------------------------------------------------------------- stage 1
-// Any layout: unit u is frame frame0 + u / segs, rows [s * seg_rows,
-// min((s + 1) * seg_rows, height)).  A warp walks one row at a time.  With
-// VEC, rows start 16-byte aligned and are read as 16-byte vectors plus a
-// scalar tail; without, every sample is read on its own.
-template <int BPC, bool VEC, class Acc = TermSums<BPC>>
+// Any layout (the path of rows that are not 16-byte aligned): unit u is
+// frame frame0 + u / segs, rows [s * seg_rows, min((s + 1) * seg_rows,
+// height)).  A warp walks one row at a time, every sample read on its own.
+template <int BPC, class Acc = TermSums<BPC>>
 __global__ void __launch_bounds__(kThreads)
     fused_rows(const unsigned char *__restrict__ ref, const unsigned char *__restrict__ dist,
                size_t frame_pitch, size_t stride, int width, int height, int seg_rows, int segs,
                int frame0, Partial *__restrict__ partials) {
     allow_dependent_launch();
-    constexpr int kBps = BPC == 8 ? 1 : 2;
     const int unit = blockIdx.x;
     const int f = frame0 + unit / segs;
     const int s = unit - (unit / segs) * segs;
@@ -526,18 +524,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int y = y0 + warp; y < y1; y += kThreads / 32) {
         const unsigned char *rr = rf + (size_t)y * stride;
         const unsigned char *dr = df + (size_t)y * stride;
-        int x0 = 0;
-        if constexpr (VEC) {
-            const int nvec = (width * kBps) >> 4;
-            for (int c = lane; c < nvec;) {
-                const int stop = min(nvec, c + (int)Acc::kFlushVecs * 32);
-                for (; c < stop; c += 32)
-                    acc.vec(ld_stream16(rr + 16 * (size_t)c), ld_stream16(dr + 16 * (size_t)c));
-                acc.flush();
-            }
-            x0 = nvec * (16 / kBps);
-        }
-        for (int x = x0 + lane; x < width;) {
+        for (int x = lane; x < width;) {
             const int stop = min(width, x + (int)Acc::kFlushVecs * 32);
             for (; x < stop; x += 32) acc.sample(ld_sample<BPC>(rr, x), ld_sample<BPC>(dr, x));
             acc.flush();

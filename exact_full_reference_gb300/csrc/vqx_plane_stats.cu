@@ -91,7 +91,7 @@ Stage1Shape stage1_shape(int path) {
                 vqx::kTmaSmem};
     case kFrames:
         return {(const void *)vqx::fused_frames<BPC, Acc>, 32 * vqx::kFrameWarps, 0};
-    default: return {(const void *)vqx::fused_rows<BPC, false, Acc>, vqx::kThreads, 0};
+    default: return {(const void *)vqx::fused_rows<BPC, Acc>, vqx::kThreads, 0};
     }
 }
 
@@ -557,7 +557,7 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     if (p.path == kRowsScalar) {
         cfg.gridDim = dim3((unsigned)units);
         cfg.blockDim = dim3(vqx::kThreads);
-        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, false, Acc>, ref, dist, p.frame_pitch,
+        return cudaLaunchKernelEx(&cfg, vqx::fused_rows<BPC, Acc>, ref, dist, p.frame_pitch,
                                   p.stride, p.width, p.height, (int)p.seg_work, p.segs, frame0,
                                   partials);
     }
