@@ -39,10 +39,21 @@ METRIC = "frame pairs/s and HBM GB/s (fused PSNR+moments), 3840x2160 16-bit, 1 G
 UNIT = "frame pairs/s"
 
 
+def chroma_workloads(wlo):
+    """The two 4:2:0 chroma planes that go with the luma workload ``wlo``:
+    half the width and height, the same content recipe, their own seeds."""
+    import dataclasses
+
+    return [dataclasses.replace(wlo, name=wlo.name + "_c%d" % k, width=max(1, wlo.width // 2),
+                                height=max(1, wlo.height // 2), seed=wlo.seed + 1000 * k)
+            for k in (1, 2)]
+
+
 def metric_for(op, wlo):
     if op == "stats":
         return METRIC
-    what = "integer psnr" if op == "int_psnr" else "fused PSNR+moments, CPU-order replay"
+    what = {"int_psnr": "integer psnr", "ordered": "fused PSNR+moments, CPU-order replay",
+            "planes420": "fused PSNR+moments, 4:2:0 Y+Cb+Cr"}[op]
     return "frame pairs/s and HBM GB/s (%s), %dx%d %d-bit, 1 GB300" % (
         what, wlo.width, wlo.height, wlo.bpc)
 FALLBACK_HBM_GBS = 6800.0
@@ -59,10 +70,12 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["stats", "int_psnr", "ordered"], default="stats",
+    p.add_argument("--op", choices=["stats", "int_psnr", "ordered", "planes420"], default="stats",
                    help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
                         "the integer psnr (vqx_plane_int_psnr); ordered: the CPU-order replay "
-                        "past 2^53 units (vqx_plane_stats_ordered, one blocking call a step)")
+                        "past 2^53 units (vqx_plane_stats_ordered, one blocking call a step); "
+                        "planes420: the workload as the luma of 4:2:0 video, Y, Cb and Cr "
+                        "through one vqx_planes_stats call a step")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
                    help="write the DRAM traffic record of the fused kernel from an ncu report "
                         "(read here with ncu -i; needs no GPU) and exit")
@@ -262,10 +275,12 @@ def write_traffic_record(report, wlo):
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="stats"):
+def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="stats", extra=()):
     """Run the CPU oracle over frames (or bands of ``rows`` rows) of the batch
     on ``cores`` threads until ``seconds`` have passed.  Returns (pairs/s,
-    pairs done, elapsed s).  ctypes drops the GIL inside the C calls."""
+    pairs done, elapsed s).  ctypes drops the GIL inside the C calls.
+    ``extra``: (ref, dist) arrays of half-size planes taken with each frame
+    (the chroma of 4:2:0 video), half the rows of each band."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -282,6 +297,11 @@ def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="sta
             orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
         else:
             orc.int_psnr(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
+        for cr, cd in extra:
+            ch, cw = cr.shape[1:]
+            cb = max(1, min(ch, band // 2))
+            c0 = min(y0 // 2, ch - cb)
+            orc.batch(cr[f, c0 : c0 + cb], cd[f, c0 : c0 + cb], cw, cb, cw * cr.itemsize, wlo.bpc, 1)
         return band
 
     done_rows = 0
@@ -308,17 +328,18 @@ def run_reference(args, wlo):
     cores = host_cores()
     frames = list(range(min(wlo.n_frames, max(cores, 1))))
     ref, dist = wlo.generate(frames)
+    extra = [c.generate(frames) for c in chroma_workloads(wlo)] if args.op == "planes420" else ()
     # size one step so that warm-up plus timed steps take about two minutes
     per_step_s = min(0.5, 120.0 / max(args.steps + args.warmup, 1))
-    rate, _, _ = time_oracle(wlo, ref, dist, 0.0, 1, rows=64, op=args.op)  # one thread, calibration
+    rate, _, _ = time_oracle(wlo, ref, dist, 0.0, 1, rows=64, op=args.op, extra=extra)  # calibration
     rows_per_s = rate * wlo.height
     rows = int(max(1, min(wlo.height, rows_per_s * per_step_s)))
     for _ in range(args.warmup):
-        time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op)
+        time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op, extra=extra)
     t0 = time.perf_counter()
     pairs = 0.0
     for _ in range(args.steps):
-        _, p, _ = time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op)
+        _, p, _ = time_oracle(wlo, ref, dist, 0.0, cores, rows=rows, op=args.op, extra=extra)
         pairs += p
     el = time.perf_counter() - t0
     value = pairs / el
@@ -381,12 +402,29 @@ def run_ours(args, wlo):
 
     so = vqx.library()
     out = np.zeros(n, vqx.INT_PSNR_DTYPE if args.op == "int_psnr" else vqx.FRAME_STATS_DTYPE)
+    chroma_np, chroma_dev = [], []
+    if args.op == "planes420":
+        out = np.zeros((n, 3), vqx.FRAME_STATS_DTYPE)
+        for c in chroma_workloads(wlo):
+            cr, cd = c.generate()
+            chroma_np.append((cr, cd))
+            chroma_dev.append((torch.from_numpy(cr.reshape(-1).view(np.uint8)).to(dev),
+                               torch.from_numpy(cd.reshape(-1).view(np.uint8)).to(dev), c))
+        descs = (vqx.PlaneDesc * 3)(
+            vqx.PlaneDesc(d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, 0),
+            *[vqx.PlaneDesc(tr.data_ptr(), td.data_ptr(), c.width, c.height,
+                            c.width * c.bytes_per_sample, 0) for tr, td, c in chroma_dev])
     out_p = out.ctypes.data
     # the planes are written once, before any step: batches may start reading
     # them while the batch ahead finishes
     submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh,
                    vqx.VQX_SUBMIT_PLANES_READY)
-    if args.op == "ordered":
+    if args.op == "planes420":
+        def submit_fn(*a):
+            return so.vqx_planes_stats_submit(descs, 3, wlo.bpc, n, sh, vqx.VQX_SUBMIT_PLANES_READY, a[-1])
+
+        finish_fn = so.vqx_planes_stats_finish
+    elif args.op == "ordered":
         # a blocking call per step: submit runs it, finish has nothing left to do
         def submit_fn(*a):
             return so.vqx_plane_stats_ordered(*a[:-2], out_p)
@@ -499,6 +537,8 @@ def run_ours(args, wlo):
         label = "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
     if args.op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
         label = "ordered_block_sums"
+    if args.op == "planes420":
+        label = "fused_stream_tma, three planes (Y, Cb, Cr) timed together"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                 "timing": "CUDA events recorded by the library around each launch in a second "
@@ -538,10 +578,11 @@ def run_ours(args, wlo):
     if rank == 0 and world == 1 and not args.no_cpu:
         cores = host_cores()
         sub = list(range(min(n, cores)))
+        ex = [(cr[sub], cd[sub]) for cr, cd in chroma_np]
         rate, pairs, el = time_oracle(wlo, ref[sub], dist_np[sub], args.cpu_seconds, cores,
-                                      op=args.op)
+                                      op=args.op, extra=ex)
         rate1, pairs1, el1 = time_oracle(wlo, ref[:1], dist_np[:1], min(args.cpu_seconds, 4.0), 1,
-                                         op=args.op)
+                                         op=args.op, extra=[(cr[:1], cd[:1]) for cr, cd in chroma_np])
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%.1f frame pairs of %s (whole frames, one per thread) in %.1f s"
                          % (pairs, wlo.name, el),
@@ -563,13 +604,19 @@ def run_ours(args, wlo):
             "dtype": ("u%d samples, %s" % (8 if wlo.bpc == 8 else 16,
                       "f32 terms, u64 sums" if args.op == "stats" else "exact integer squares, u64 sums")),
             "data": "synthetic",
-            "hbm_gbs": value * wlo.pair_bytes / 1e9 / world,
+            "hbm_gbs": value * wlo.pair_bytes * (1.5 if args.op == "planes420" else 1.0) / 1e9 / world,
             "config": {"workload": wlo.name, "frames_per_gpu": n, "width": w, "height": h,
-                       "bpc": wlo.bpc, "batch_bytes": int(rbytes.nbytes + dbytes.nbytes),
+                       "bpc": wlo.bpc,
+                       "batch_bytes": int(rbytes.nbytes + dbytes.nbytes
+                                          + sum(cr.nbytes + cd.nbytes for cr, cd in chroma_np)),
                        "l2": "inputs %.2f GB per step, larger than the 129 MB L2; no flush"
                              % ((rbytes.nbytes + dbytes.nbytes) / 1e9),
                        "pipeline": ("one blocking vqx_plane_stats_ordered call a step"
                                     if args.op == "ordered" else
+                                    "batch i + 1 submitted before batch i is finished "
+                                    "(vqx_planes_stats_submit with VQX_SUBMIT_PLANES_READY / "
+                                    "_finish; Y, Cb, Cr)"
+                                    if args.op == "planes420" else
                                     "batch i + 1 submitted before batch i is finished "
                                     "(vqx_plane_%s_submit with VQX_SUBMIT_PLANES_READY / "
                                     "_finish)" % args.op),
@@ -585,6 +632,9 @@ def run_ours(args, wlo):
                                     "every step, steps timed one by one, flush excluded"
                                     % (2 * l2_bytes >> 20))
             line["config"]["pipeline"] = "none (each step timed on its own after the flush)"
+        if args.op == "planes420":
+            line["config"]["planes"] = "Y %dx%d, Cb and Cr %dx%d per frame" % (
+                w, h, max(1, w // 2), max(1, h // 2))
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -121,6 +121,11 @@ def library():
             fin.restype = i
         lib.vqx_planes_stats.argtypes = [ctypes.POINTER(PlaneDesc), i, i, i, vp, vp]
         lib.vqx_planes_stats.restype = i
+        lib.vqx_planes_stats_submit.argtypes = [ctypes.POINTER(PlaneDesc), i, i, i, vp, ctypes.c_uint,
+                                                ctypes.POINTER(vp)]
+        lib.vqx_planes_stats_submit.restype = i
+        lib.vqx_planes_stats_finish.argtypes = [vp, vp]
+        lib.vqx_planes_stats_finish.restype = i
         lib.vqx_psnr_cap.argtypes = [i]
         lib.vqx_psnr_cap.restype = ctypes.c_double
         lib.vqx_status_string.argtypes = [i]
@@ -226,18 +231,19 @@ class Pending:
     """A batch enqueued by ``vqx_plane_stats_submit``; ``finish()`` waits for
     it and returns its records (call it exactly once)."""
 
-    def __init__(self, handle, n_frames, keep, kind="stats"):
+    def __init__(self, handle, n_frames, keep, kind="stats", n_planes=None):
         self._handle = handle
         self.n_frames = n_frames
         self.kind = kind
+        self.shape = n_frames if n_planes is None else (n_frames, n_planes)
         self._keep = keep  # the planes stay referenced until the batch is finished
 
     def finish(self, out=None, check=True):
         if self._handle is False:
             raise RuntimeError("this batch was already finished")
         if out is None:
-            out = np.zeros(self.n_frames, FRAME_STATS_DTYPE if self.kind == "stats" else INT_PSNR_DTYPE)
-        name = "vqx_plane_%s_finish" % self.kind
+            out = np.zeros(self.shape, INT_PSNR_DTYPE if self.kind == "int_psnr" else FRAME_STATS_DTYPE)
+        name = "vqx_planes_stats_finish" if self.kind == "planes" else "vqx_plane_%s_finish" % self.kind
         rc = getattr(library(), name)(self._handle, out.ctypes.data if out.size else None)
         self._handle, self._keep = False, None
         if check and rc != VQX_OK:
@@ -308,6 +314,24 @@ def vqx_plane_stats_noalloc(ref, dist, width=None, height=None, stride=None, bpc
     return out if check else (out, rc)
 
 
+def _plane_descs(planes):
+    descs = (PlaneDesc * max(len(planes), 1))()
+    for k, (r, d, w, h, st, fp) in enumerate(planes):
+        descs[k] = PlaneDesc(_address(r), _address(d), w, h, st, fp or 0)
+    return descs
+
+
+def vqx_planes_stats_submit(planes, bpc, n_frames, stream=None, flags=0):
+    """Enqueue ``vqx_planes_stats`` without waiting; ``finish()`` gives the
+    (n_frames, len(planes)) records."""
+    handle = ctypes.c_void_p()
+    rc = library().vqx_planes_stats_submit(_plane_descs(planes), len(planes), bpc, n_frames,
+                                           _stream_handle(stream), flags, ctypes.byref(handle))
+    if rc != VQX_OK:
+        _raise("vqx_planes_stats_submit", rc)
+    return Pending(handle.value, max(n_frames, 0), [p[:2] for p in planes], "planes", len(planes))
+
+
 def vqx_planes_stats(planes, bpc, n_frames, stream=None, check=True):
     """Per-frame statistics of several planes of each frame (Y, Cb, Cr ...).
 
@@ -316,9 +340,7 @@ def vqx_planes_stats(planes, bpc, n_frames, stream=None, check=True):
     plane in frame 0, stride and frame_pitch in bytes (frame_pitch 0 or None:
     height * stride).  Returns ``FRAME_STATS_DTYPE`` records of shape
     (n_frames, len(planes))."""
-    descs = (PlaneDesc * max(len(planes), 1))()
-    for k, (r, d, w, h, st, fp) in enumerate(planes):
-        descs[k] = PlaneDesc(_address(r), _address(d), w, h, st, fp or 0)
+    descs = _plane_descs(planes)
     out = np.zeros((max(n_frames, 0), len(planes)), FRAME_STATS_DTYPE)
     rc = library().vqx_planes_stats(descs, len(planes), bpc, n_frames, _stream_handle(stream),
                                     out.ctypes.data if out.size else None)

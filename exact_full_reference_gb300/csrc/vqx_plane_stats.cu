@@ -57,10 +57,10 @@ constexpr size_t kRowsMinBytes = 512;
 // What a call computes: the fused statistics, or the integer psnr.  Up to 12
 // bits the integer psnr's SSE is the fused pass's noise sum (its squares are
 // exact), so only 16 bits has a kernel variant of its own.
-enum Kind { kStats = 0, kIntPsnr = 1 };
+enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2 };
 constexpr int kVariants = 5;  // fused 8, 10, 12, 16 bits; integer psnr 16 bits
 
-int variant_index(int bpc, int kind) {
+int variant_index(int bpc, int kind) {  // kPlanes runs the fused statistics
     if (kind == kIntPsnr && bpc == 16) return 4;
     return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3;
 }
@@ -276,6 +276,8 @@ struct vqx_pending {
     DeviceCtx *ctx = nullptr;
     int kind = 0;  // Kind: what the batch computes
     int n_frames = 0, bpc = 0, width = 0, height = 0;
+    int n_planes = 1;                                    // kPlanes: the planes' sizes
+    int pw[VQX_MAX_PLANES] = {}, ph[VQX_MAX_PLANES] = {};
 };
 
 namespace {
@@ -803,6 +805,7 @@ int submit_impl(const void *ref, const void *dist, int width, int height, size_t
         return cuda_status(e);
     }
     p->kind = kind;
+    p->n_planes = 1;
     p->n_frames = n_frames;
     p->bpc = bpc;
     p->width = width;
@@ -823,9 +826,13 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
         rc = VQX_EINVAL;
     } else {
         t_prof.totals.calls++;
-        t_prof.totals.kernel_launches += 2;
-        t_prof.totals.stage1_launches += 1;
-        t_prof.totals.stage1_bytes += plane_bytes(p->width, p->height, p->bpc, p->n_frames);
+        t_prof.totals.kernel_launches += 2 * (uint64_t)p->n_planes;
+        t_prof.totals.stage1_launches += (uint64_t)p->n_planes;
+        if (kind == kPlanes)
+            for (int q = 0; q < p->n_planes; q++)
+                t_prof.totals.stage1_bytes += plane_bytes(p->pw[q], p->ph[q], p->bpc, p->n_frames);
+        else
+            t_prof.totals.stage1_bytes += plane_bytes(p->width, p->height, p->bpc, p->n_frames);
         if (p->timed) {
             float a = 0.f, b = 0.f;
             cudaEventElapsedTime(&a, p->ev[0], p->ev[1]);
@@ -836,6 +843,14 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
         const Partial *sums = (const Partial *)p->rec.host;
         if (kind == kStats) {
             rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
+        } else if (kind == kPlanes) {
+            vqx_frame_stats *o = (vqx_frame_stats *)out;
+            for (int q = 0; q < p->n_planes; q++)
+                for (int f = 0; f < p->n_frames; f++) {
+                    vqx_frame_stats &r = o[(size_t)f * p->n_planes + q];
+                    conclude(sums[(size_t)q * p->n_frames + f], p->bpc, p->pw[q], p->ph[q], &r);
+                    rc = merge_status(rc, r);
+                }
         } else {
             vqx_int_psnr_stats *o = (vqx_int_psnr_stats *)out;
             for (int f = 0; f < p->n_frames; f++) {
@@ -897,13 +912,15 @@ int vqx_plane_stats(const void *ref, const void *dist, int width, int height, si
     return vqx_plane_stats_finish(p, out);
 }
 
-int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
-                    vqx_stream_t stream, vqx_frame_stats *out) {
+int vqx_planes_stats_submit(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
+                           vqx_stream_t stream, unsigned flags, vqx_pending **pending) {
+    if (!pending) return VQX_EINVAL;
+    *pending = nullptr;
+    if (flags & ~VQX_SUBMIT_PLANES_READY) return VQX_EINVAL;
     if (!planes || n_planes < 1 || n_planes > VQX_MAX_PLANES) return VQX_EINVAL;
     if (bpc != 8 && bpc != 10 && bpc != 12 && bpc != 16) return VQX_EBPC;
     if (n_frames < 0) return VQX_EINVAL;
     if (n_frames == 0) return VQX_OK;
-    if (!out) return VQX_EINVAL;
     size_t pitch[VQX_MAX_PLANES];
     for (int p = 0; p < n_planes; p++) {
         const int rc = validate_plane(planes[p], bpc, n_frames, &pitch[p]);
@@ -918,47 +935,66 @@ int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_
     size_t off[VQX_MAX_PLANES + 1] = {0};  // record offsets of the planes, in records
     for (int p = 0; p < n_planes; p++) {
         const vqx_plane_desc &d = planes[p];
-        plan[p] = make_plan(*ctx, d.ref, d.dist, d.width, d.height, d.stride, bpc, n_frames, kStats,
+        plan[p] = make_plan(*ctx, d.ref, d.dist, d.width, d.height, d.stride, bpc, n_frames, kPlanes,
                             1ll << 40, pitch[p]);
         off[p + 1] = off[p] + records_bytes(plan[p], n_frames) / sizeof(Partial);
     }
-    PinnedBuf rec;
-    if ((rc = acquire_pinned((size_t)n_planes * n_frames * sizeof(Partial), &rec)) != VQX_OK) return rc;
+    vqx_pending *pd = nullptr;
+    if ((rc = acquire_pending(ctx, t_prof.on, &pd)) != VQX_OK) return rc;
+    if ((rc = acquire_pinned((size_t)n_planes * n_frames * sizeof(Partial), &pd->rec)) != VQX_OK) {
+        release_pending(pd);
+        return rc;
+    }
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, off[n_planes] * sizeof(Partial), ctx->pool, st);
     if (e != cudaSuccess) {
-        release_pinned(rec);
+        release_pinned(pd->rec);
+        release_pending(pd);
         return cuda_status(e);
     }
     Partial *partials = (Partial *)ws;
+    const bool ready = (flags & VQX_SUBMIT_PLANES_READY) != 0;
+    if (pd->timed) cudaEventRecord(pd->ev[0], st);
     for (int p = 0; e == cudaSuccess && p < n_planes; p++)
-        e = launch_stage1(plan[p], planes[p].ref, planes[p].dist, 0, n_frames, partials + off[p], st, true);
+        e = launch_stage1(plan[p], planes[p].ref, planes[p].dist, 0, n_frames, partials + off[p], st,
+                          true, ready);
+    if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[1], st);
     for (int p = 0; e == cudaSuccess && p < n_planes; p++)
-        e = launch_stage2(plan[p], n_frames, partials + off[p], (Partial *)rec.dev + (size_t)p * n_frames,
-                          st);
+        e = launch_stage2(plan[p], n_frames, partials + off[p],
+                          (Partial *)pd->rec.dev + (size_t)p * n_frames, st);
+    if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[2], st);
     const cudaError_t ef = cudaFreeAsync(ws, st);
-    const cudaError_t es = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaEventRecord(pd->done, st);
     if (e != cudaSuccess) {
-        release_pinned(rec);
+        cudaStreamSynchronize(st);  // whatever was enqueued finishes first
+        release_pinned(pd->rec);
+        release_pending(pd);
         return cuda_status(e);
     }
-    t_prof.totals.calls++;
-    t_prof.totals.kernel_launches += 2 * (uint64_t)n_planes;
-    t_prof.totals.stage1_launches += (uint64_t)n_planes;
-    const Partial *sums = (const Partial *)rec.host;
-    rc = VQX_OK;
+    pd->kind = kPlanes;
+    pd->n_frames = n_frames;
+    pd->bpc = bpc;
+    pd->n_planes = n_planes;
     for (int p = 0; p < n_planes; p++) {
-        const vqx_plane_desc &d = planes[p];
-        t_prof.totals.stage1_bytes += plane_bytes(d.width, d.height, bpc, n_frames);
-        for (int f = 0; f < n_frames; f++) {
-            vqx_frame_stats &o = out[(size_t)f * n_planes + p];
-            conclude(sums[(size_t)p * n_frames + f], bpc, d.width, d.height, &o);
-            rc = merge_status(rc, o);
-        }
+        pd->pw[p] = planes[p].width;
+        pd->ph[p] = planes[p].height;
     }
-    release_pinned(rec);
-    return rc;
+    *pending = pd;
+    return VQX_OK;
+}
+
+int vqx_planes_stats_finish(vqx_pending *pending, vqx_frame_stats *out) {
+    return finish_impl(pending, kPlanes, out);
+}
+
+int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
+                    vqx_stream_t stream, vqx_frame_stats *out) {
+    if (n_frames > 0 && !out) return VQX_EINVAL;
+    vqx_pending *p = nullptr;
+    const int rc = vqx_planes_stats_submit(planes, n_planes, bpc, n_frames, stream, 0u, &p);
+    if (rc != VQX_OK || !p) return rc;
+    return finish_impl(p, kPlanes, out);
 }
 
 int vqx_plane_stats_host(const void *ref, const void *dist, int width, int height,

@@ -199,6 +199,14 @@ typedef struct {
 int vqx_planes_stats(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
                     vqx_stream_t stream, vqx_frame_stats *out);
 
+/* The same in two halves, as vqx_plane_stats_submit / _finish (flags, the
+ * planes' lifetime and the handle's rules alike); the descriptors themselves
+ * are read during the submit only. */
+int vqx_planes_stats_submit(const vqx_plane_desc *planes, int n_planes, int bpc, int n_frames,
+                            vqx_stream_t stream, unsigned flags, vqx_pending **pending);
+
+int vqx_planes_stats_finish(vqx_pending *pending, vqx_frame_stats *out);
+
 /*
  * Integer psnr of one frame pair: the integer sibling of float_psnr.
  * "ADR-1440: float_psnr_hip adds its squared differences as integers ..."

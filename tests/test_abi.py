@@ -26,6 +26,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr", "vqx_planes_stats",
+              "vqx_planes_stats_submit", "vqx_planes_stats_finish",
               "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
               "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
         assert n in names
@@ -134,6 +135,13 @@ def test_planes_argument_errors_need_no_gpu(lib):
     assert call([y], n_frames=0) == 0
     assert so.vqx_planes_stats(None, 1, 16, 1, None, out) == -1
     assert ctypes.sizeof(lib.PlaneDesc) == 40
+    handle = ctypes.c_void_p(99)
+    arr = (lib.PlaneDesc * 2)(y, c)
+    assert so.vqx_planes_stats_submit(arr, 2, 9, 2, None, 0, ctypes.byref(handle)) == -2
+    assert handle.value is None
+    assert so.vqx_planes_stats_submit(arr, 2, 16, 2, None, 4, ctypes.byref(handle)) == -1
+    assert so.vqx_planes_stats_submit(arr, 2, 16, 0, None, 0, ctypes.byref(handle)) == 0
+    assert handle.value is None and so.vqx_planes_stats_finish(None, None) == 0
 
 
 def test_empty_batch_is_ok_without_gpu(lib):

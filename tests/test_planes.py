@@ -106,3 +106,25 @@ def test_one_plane_is_vqx_plane_stats(lib, orc):
     keep, pr, pd, stride, _ = parity.place(ref, dist)
     rec = lib.vqx_planes_stats([(pr, pd, 480, 270, stride, None)], 12, 4)
     assert rec[:, 0].tobytes() == lib.vqx_plane_stats(pr, pd, 480, 270, stride, 12, 4).tobytes()
+
+
+def test_planes_submit_finish(lib, orc):
+    """The two-half form: batches enqueued back to back (with and without
+    VQX_SUBMIT_PLANES_READY) give the blocking call's records; a handle of
+    another kind is refused."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    planes = yuv_frames(rng, 4, 576, 324, 288, 162, 10)
+    keep, descs = [], []
+    for ref, dist in planes:
+        k, pr, pd, stride, _ = parity.place(ref, dist)
+        keep.append(k)
+        descs.append((pr, pd, ref.shape[2], ref.shape[1], stride, 0))
+    want = lib.vqx_planes_stats(descs, 10, 4)
+    for flags in (0, lib.VQX_SUBMIT_PLANES_READY):
+        pend = [lib.vqx_planes_stats_submit(descs, 10, 4, flags=flags) for _ in range(3)]
+        for p in reversed(pend):
+            assert p.finish().tobytes() == want.tobytes()
+    p = lib.vqx_planes_stats_submit(descs, 10, 4)
+    p.kind, p.shape = "stats", 4
+    out, rc = p.finish(check=False)
+    assert rc == lib.VQX_EINVAL
