@@ -73,7 +73,7 @@ def parse_args():
     p.add_argument("--op", choices=["stats", "int_psnr", "ordered", "planes420"], default="stats",
                    help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
                         "the integer psnr (vqx_plane_int_psnr); ordered: the CPU-order replay "
-                        "past 2^53 units (vqx_plane_stats_ordered, one blocking call a step); "
+                        "past 2^53 units (vqx_plane_stats_ordered_submit / _finish); "
                         "planes420: the workload as the luma of 4:2:0 video, Y, Cb and Cr "
                         "through one vqx_planes_stats call a step")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
@@ -425,12 +425,8 @@ def run_ours(args, wlo):
 
         finish_fn = so.vqx_planes_stats_finish
     elif args.op == "ordered":
-        # a blocking call per step: submit runs it, finish has nothing left to do
-        def submit_fn(*a):
-            return so.vqx_plane_stats_ordered(*a[:-2], out_p)
-
-        def finish_fn(handle, out_ptr):
-            return 0
+        submit_fn = so.vqx_plane_stats_ordered_submit
+        finish_fn = so.vqx_plane_stats_ordered_finish
     else:
         submit_fn = getattr(so, "vqx_plane_%s_submit" % args.op)
         finish_fn = getattr(so, "vqx_plane_%s_finish" % args.op)
@@ -611,7 +607,9 @@ def run_ours(args, wlo):
                                           + sum(cr.nbytes + cd.nbytes for cr, cd in chroma_np)),
                        "l2": "inputs %.2f GB per step, larger than the 129 MB L2; no flush"
                              % ((rbytes.nbytes + dbytes.nbytes) / 1e9),
-                       "pipeline": ("one blocking vqx_plane_stats_ordered call a step"
+                       "pipeline": ("batch i + 1 submitted before batch i is finished "
+                                    "(vqx_plane_stats_ordered_submit with VQX_SUBMIT_PLANES_READY "
+                                    "/ _finish)"
                                     if args.op == "ordered" else
                                     "batch i + 1 submitted before batch i is finished "
                                     "(vqx_planes_stats_submit with VQX_SUBMIT_PLANES_READY / "

@@ -112,7 +112,7 @@ def library():
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
-        for kind in ("stats", "int_psnr"):
+        for kind in ("stats", "int_psnr", "stats_ordered"):
             sub = getattr(lib, "vqx_plane_%s_submit" % kind)
             sub.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.c_uint, ctypes.POINTER(vp)]
             sub.restype = i
@@ -268,6 +268,13 @@ def vqx_plane_stats_submit(ref, dist, width=None, height=None, stride=None, bpc=
     ``Pending`` whose ``finish()`` gives what ``vqx_plane_stats`` would.
     ``flags``: 0 or ``VQX_SUBMIT_PLANES_READY``."""
     return _submit("stats", ref, dist, width, height, stride, bpc, n_frames, stream, flags)
+
+
+def vqx_plane_stats_ordered_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
+                                   n_frames=None, stream=None, flags=0):
+    """The same for ``vqx_plane_stats_ordered`` (its workspace is held until
+    ``finish()``)."""
+    return _submit("stats_ordered", ref, dist, width, height, stride, bpc, n_frames, stream, flags)
 
 
 def vqx_plane_int_psnr_submit(ref, dist, width=None, height=None, stride=None, bpc=16,

@@ -173,9 +173,16 @@ struct OrdWordSums {
 
 constexpr int kSumWarps = 4;  // blocks (one per warp) per CTA of ordered_block_sums
 
+//
+// Launched as a programmatic dependent of the batch ahead, the kernel writes
+// only its own batch's workspace (which the batch ahead does not hold) and,
+// unless planes_ready, waits for the kernel ahead before reading the planes.
+// It also zeroes the work-list count that ordered_classify appends to.
 __global__ void __launch_bounds__(32 * kSumWarps)
     ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
-                       uint32_t *__restrict__ ssums) {
+                       uint32_t *__restrict__ ssums, int *__restrict__ n_work, int planes_ready) {
+    if (!planes_ready) grid_dependency_wait();
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *n_work = 0;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kSumWarps + (threadIdx.x >> 5), f = blockIdx.y;
     if (b >= g.nb) return;
@@ -504,6 +511,7 @@ __global__ void __launch_bounds__(32)
     ordered_walk(const OrdPlanes g, const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
                  const int *__restrict__ cls, const OrdTable *__restrict__ tables,
                  u64 *__restrict__ out) {
+    allow_dependent_launch();  // the next batch's block sums may start on free SMs
     const int f = blockIdx.x, q = blockIdx.y, lane = threadIdx.x;
     __shared__ uint32_t terms[kOrdBlock];
     const int nb = g.nb;

@@ -57,7 +57,7 @@ constexpr size_t kRowsMinBytes = 512;
 // What a call computes: the fused statistics, or the integer psnr.  Up to 12
 // bits the integer psnr's SSE is the fused pass's noise sum (its squares are
 // exact), so only 16 bits has a kernel variant of its own.
-enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2 };
+enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2, kOrdered = 3 };
 constexpr int kVariants = 5;  // fused 8, 10, 12, 16 bits; integer psnr 16 bits
 
 int variant_index(int bpc, int kind) {  // kPlanes runs the fused statistics
@@ -278,6 +278,7 @@ struct vqx_pending {
     int n_frames = 0, bpc = 0, width = 0, height = 0;
     int n_planes = 1;                                    // kPlanes: the planes' sizes
     int pw[VQX_MAX_PLANES] = {}, ph[VQX_MAX_PLANES] = {};
+    void *ws = nullptr;  // kOrdered: the workspace, held until finished
 };
 
 namespace {
@@ -826,7 +827,7 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
         rc = VQX_EINVAL;
     } else {
         t_prof.totals.calls++;
-        t_prof.totals.kernel_launches += 2 * (uint64_t)p->n_planes;
+        t_prof.totals.kernel_launches += kind == kOrdered ? 4 : 2 * (uint64_t)p->n_planes;
         t_prof.totals.stage1_launches += (uint64_t)p->n_planes;
         if (kind == kPlanes)
             for (int q = 0; q < p->n_planes; q++)
@@ -841,7 +842,22 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
             t_prof.totals.stage2_ms += b;
         }
         const Partial *sums = (const Partial *)p->rec.host;
-        if (kind == kStats) {
+        if (kind == kOrdered) {
+            const u64 *w = (const u64 *)p->rec.host;
+            for (int f = 0; f < p->n_frames; f++) {
+                const u64 *o = w + (size_t)f * vqx::kOrdOut;
+                Partial s_f;
+                s_f.v[0] = o[3];  // exact noise units
+                s_f.v[1] = o[6];  // sample sums
+                s_f.v[2] = o[7];
+                s_f.v[3] = o[4];  // exact squares
+                s_f.v[4] = o[5];
+                s_f.v[5] = 0;  // 16 bits: no sample out of range; no device wait to time out
+                vqx_frame_stats &r = ((vqx_frame_stats *)out)[f];
+                conclude(s_f, p->bpc, p->width, p->height, &r, o);
+                rc = merge_status(rc, r);
+            }
+        } else if (kind == kStats) {
             rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
         } else if (kind == kPlanes) {
             vqx_frame_stats *o = (vqx_frame_stats *)out;
@@ -858,6 +874,12 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
                 rc = merge_status_flags(rc, o[f].flags);
             }
         }
+    }
+    if (p->ws) {
+        // the batch is over (its event completed, or the wait failed and the
+        // context is gone): the workspace goes back to the pool
+        cudaFreeAsync(p->ws, p->ctx->copy_stream);
+        p->ws = nullptr;
     }
     release_pinned(p->rec);
     release_pending(p);
@@ -1092,16 +1114,22 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
 }  // extern "C"
 
 // ====================================================================== CPU-order replay
-extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
-                                       size_t stride, int bpc, int n_frames, vqx_stream_t stream,
-                                       vqx_frame_stats *out) {
-    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+extern "C" int vqx_plane_stats_ordered_submit(const void *ref, const void *dist, int width,
+                                              int height, size_t stride, int bpc, int n_frames,
+                                              vqx_stream_t stream, unsigned flags,
+                                              vqx_pending **pending) {
+    if (!pending) return VQX_EINVAL;
+    *pending = nullptr;
+    if (flags & ~VQX_SUBMIT_PLANES_READY) return VQX_EINVAL;
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames,
+                      reinterpret_cast<const vqx_frame_stats *>(pending));
     if (rc != VQX_OK || n_frames == 0) return rc;
     const uint64_t pixels = (uint64_t)width * (uint64_t)height;
     // Below 16 bits, or up to 2^21 pixels, no CPU sum can reach 2^53 units:
     // the exact sums are the CPU's sums.
     if (bpc != 16 || pixels <= (1u << 21))
-        return vqx_plane_stats(ref, dist, width, height, stride, bpc, n_frames, stream, out);
+        return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kStats, flags,
+                           pending);
     if (n_frames > 65535) return VQX_EINVAL;
     // The replay kernels produce every integer sum as well (the blocks' exact
     // sums), so the plain pass is not run here.
@@ -1114,13 +1142,18 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
                  tab_b = cells * sizeof(vqx::OrdTable), ors_b = cells * sizeof(uint32_t),
                  work_b = cells * sizeof(vqx::OrdWork),
                  ssum_b = (size_t)n_frames * nb * 2 * sizeof(uint32_t);
-    PinnedBuf res;
-    if ((rc = acquire_pinned((size_t)n_frames * vqx::kOrdOut * sizeof(u64), &res)) != VQX_OK) return rc;
+    vqx_pending *pd = nullptr;
+    if ((rc = acquire_pending(ctx, t_prof.on, &pd)) != VQX_OK) return rc;
+    if ((rc = acquire_pinned((size_t)n_frames * vqx::kOrdOut * sizeof(u64), &pd->rec)) != VQX_OK) {
+        release_pending(pd);
+        return rc;
+    }
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, sums_b + cls_b + tab_b + ors_b + work_b + ssum_b + 256,
                                             ctx->pool, st);
     if (e != cudaSuccess) {
-        release_pinned(res);
+        release_pinned(pd->rec);
+        release_pending(pd);
         return cuda_status(e);
     }
     // sums and tables (8-byte aligned), then the 4-byte arrays
@@ -1141,29 +1174,26 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
     g.nb = nb;
     g.dense = stride == (size_t)width * 2 && (pixels & 7u) == 0 &&
               (((uintptr_t)ref | (uintptr_t)dist) & 15u) == 0;
-    // with profiling on, the block-sum kernel (the pass over every pixel) is
-    // timed as this call's stage-1 launch
-    struct Events {  // destroyed on every return
-        cudaEvent_t e[2] = {nullptr, nullptr};
-        ~Events() {
-            for (cudaEvent_t x : e)
-                if (x) cudaEventDestroy(x);
-        }
-    } evs;
-    cudaEvent_t *ev = evs.e;
-    const bool timed = t_prof.on && cudaEventCreate(&ev[0]) == cudaSuccess &&
-                       cudaEventCreate(&ev[1]) == cudaSuccess;
-    e = cudaMemsetAsync(n_work, 0, sizeof(int), st);
-    if (e == cudaSuccess) {
-        if (timed) cudaEventRecord(ev[0], st);
-        vqx::ordered_block_sums<<<dim3((nb + vqx::kSumWarps - 1) / vqx::kSumWarps, n_frames),
-                                  32 * vqx::kSumWarps, 0, st>>>(g, sums, ors, ssums);
-        e = cudaGetLastError();
-        if (timed) cudaEventRecord(ev[1], st);
-    }
+    // The block sums are a programmatic dependent of the kernel ahead (the
+    // batch ahead's walk, when batches follow each other): they start while
+    // it runs and write only this batch's workspace.
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((nb + vqx::kSumWarps - 1) / vqx::kSumWarps, n_frames);
+    cfg.blockDim = dim3(32 * vqx::kSumWarps);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int ready = (flags & VQX_SUBMIT_PLANES_READY) ? 1 : 0;
+    if (pd->timed) cudaEventRecord(pd->ev[0], st);
+    e = cudaLaunchKernelEx(&cfg, vqx::ordered_block_sums, g, sums, ors, ssums, n_work, ready);
+    if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[1], st);
     if (e == cudaSuccess) {
         vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), vqx::kClassThreads, 0, st>>>(
-            sums, ors, ssums, nb, cls, work, n_work, (u64 *)res.dev);
+            sums, ors, ssums, nb, cls, work, n_work, (u64 *)pd->rec.dev);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
@@ -1175,41 +1205,44 @@ extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int wi
     }
     if (e == cudaSuccess) {
         vqx::ordered_walk<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(g, sums, ors, cls, tables,
-                                                                         (u64 *)res.dev);
+                                                                         (u64 *)pd->rec.dev);
         e = cudaGetLastError();
     }
-    const cudaError_t ef = cudaFreeAsync(ws, st);
-    const cudaError_t es = cudaStreamSynchronize(st);
-    if (e == cudaSuccess) e = ef != cudaSuccess ? ef : es;
+    if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[2], st);
+    if (e == cudaSuccess) e = cudaEventRecord(pd->done, st);
     if (e != cudaSuccess) {
-        release_pinned(res);
+        cudaStreamSynchronize(st);  // whatever was enqueued finishes first
+        cudaFreeAsync(ws, st);
+        cudaStreamSynchronize(st);
+        release_pinned(pd->rec);
+        release_pending(pd);
         return cuda_status(e);
     }
-    t_prof.totals.calls++;
-    t_prof.totals.kernel_launches += 4;  // and one memset
-    t_prof.totals.stage1_launches += 1;
-    t_prof.totals.stage1_bytes += plane_bytes(width, height, bpc, n_frames);
-    if (timed) {
-        float ms = 0.f;
-        cudaEventElapsedTime(&ms, ev[0], ev[1]);
-        t_prof.totals.stage1_ms += ms;
-    }
-    const u64 *w = (const u64 *)res.host;
-    rc = VQX_OK;
-    for (int f = 0; f < n_frames; f++) {
-        const u64 *o = w + (size_t)f * vqx::kOrdOut;
-        Partial s_f;
-        s_f.v[0] = o[3];  // exact noise units
-        s_f.v[1] = o[6];  // sample sums
-        s_f.v[2] = o[7];
-        s_f.v[3] = o[4];  // exact squares
-        s_f.v[4] = o[5];
-        s_f.v[5] = 0;  // 16 bits: no sample is out of range; no device wait to time out
-        conclude(s_f, bpc, width, height, &out[f], o);
-        rc = merge_status(rc, out[f]);
-    }
-    release_pinned(res);
-    return rc;
+    pd->kind = kOrdered;
+    pd->n_planes = 1;
+    pd->n_frames = n_frames;
+    pd->bpc = bpc;
+    pd->width = width;
+    pd->height = height;
+    pd->ws = ws;
+    *pending = pd;
+    return VQX_OK;
+}
+
+extern "C" int vqx_plane_stats_ordered_finish(vqx_pending *pending, vqx_frame_stats *out) {
+    // a batch that needed no replay was submitted as a plain one
+    return finish_impl(pending, pending && pending->kind == kStats ? kStats : kOrdered, out);
+}
+
+extern "C" int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
+                                       size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                                       vqx_frame_stats *out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    vqx_pending *p = nullptr;
+    rc = vqx_plane_stats_ordered_submit(ref, dist, width, height, stride, bpc, n_frames, stream, 0u, &p);
+    if (rc != VQX_OK) return rc;
+    return vqx_plane_stats_ordered_finish(p, out);
 }
 
 // ====================================================================== no-allocation variant

@@ -39,7 +39,8 @@
  *   vqx_plane_stats_submit / _finish   the same in two halves (pipelining)
  *   vqx_planes_stats           several planes of every frame (Y, Cb, Cr)
  *   vqx_plane_stats_host       planes in host memory (copies overlapped)
- *   vqx_plane_stats_ordered    doubles equal to the CPU's also past 2^53 units
+ *   vqx_plane_stats_ordered (+ _submit / _finish)   doubles equal to the CPU's
+ *                              also past 2^53 units
  *   vqx_plane_stats_noalloc    no allocation at call time (fixed scratch)
  *   vqx_plane_int_psnr (+ _submit / _finish)   the integer psnr
  *   vqx_psnr_cap, vqx_status_string, vqx_last_cuda_error,
@@ -276,6 +277,15 @@ int vqx_plane_stats_host(const void *ref, const void *dist, int width, int heigh
 int vqx_plane_stats_ordered(const void *ref, const void *dist, int width, int height,
                             size_t stride, int bpc, int n_frames, vqx_stream_t stream,
                             vqx_frame_stats *out);
+
+/* The same in two halves, as vqx_plane_stats_submit / _finish (flags, the
+ * planes' lifetime and the handle's rules alike).  A batch's device
+ * workspace is held until its handle is finished. */
+int vqx_plane_stats_ordered_submit(const void *ref, const void *dist, int width, int height,
+                                   size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                                   unsigned flags, vqx_pending **pending);
+
+int vqx_plane_stats_ordered_finish(vqx_pending *pending, vqx_frame_stats *out);
 
 /* The PSNR cap in dB for a bit depth (6 * bpc + 12: 60, 72, 84, 108), or a
  * NaN for an unsupported bpc.  ADR-1440 (Consequences) shows that a cap

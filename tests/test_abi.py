@@ -27,6 +27,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("vqx_plane_stats", "vqx_plane_stats_host", "vqx_plane_int_psnr", "vqx_planes_stats",
               "vqx_planes_stats_submit", "vqx_planes_stats_finish",
+              "vqx_plane_stats_ordered_submit", "vqx_plane_stats_ordered_finish",
               "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
               "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
         assert n in names

@@ -72,3 +72,23 @@ def test_ordered_is_plain_below_the_limit(lib):
     a = lib.vqx_plane_stats(pr, pd, w.width, w.height, stride, w.bpc, 2)
     b = lib.vqx_plane_stats_ordered(pr, pd, w.width, w.height, stride, w.bpc, 2)
     assert a.tobytes() == b.tobytes()
+
+
+def test_ordered_submit_finish_pipelined(lib, orc):
+    """Replay batches enqueued back to back, with and without
+    VQX_SUBMIT_PLANES_READY, give the blocking call's records; so does a
+    batch that needs no replay (submitted as a plain one)."""
+    w = wl.WORKLOADS["stress_full_range_4k16"]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    want = lib.vqx_plane_stats_ordered(pr, pd, w.width, w.height, stride, 16, 2)
+    for flags in (0, lib.VQX_SUBMIT_PLANES_READY):
+        pend = [lib.vqx_plane_stats_ordered_submit(pr, pd, w.width, w.height, stride, 16, 2, flags=flags)
+                for _ in range(4)]
+        for p in pend[::-1]:
+            assert p.finish().tobytes() == want.tobytes()
+    small = wl.WORKLOADS["1920x1080_10bit_x48"]
+    r2, d2 = small.generate([0, 1])
+    k2, p2, q2, s2, _ = parity.place(r2, d2)
+    p = lib.vqx_plane_stats_ordered_submit(p2, q2, small.width, small.height, s2, 10, 2)
+    assert p.finish().tobytes() == lib.vqx_plane_stats(p2, q2, small.width, small.height, s2, 10, 2).tobytes()
