@@ -303,3 +303,52 @@ def test_many_tiny_dense_frames(lib, orc, bpc, w, h, n):
     assert [int(x) for x in ip["sse"][:50]] == [int(x) for x in orc.int_psnr(rb, db, w, h, stride, bpc, 50)["sse"]]
     na = lib.vqx_plane_stats_noalloc(pr, pd, w, h, stride, bpc, n)
     assert na.tobytes() == rec.tobytes()
+
+
+def test_every_kind_from_four_threads(lib, orc):
+    """Four threads, four streams, each submitting and finishing its own kind
+    of batch (fused, integer psnr, multi-plane, replay) 15 times over; every
+    result equals the blocking call's."""
+    rng = np.random.Generator(np.random.PCG64(44))
+    r16 = rng.integers(0, 65536, (2, 1200, 2000)).astype(np.uint16)  # past 2^21 px: replay
+    d16 = rng.integers(0, 65536, (2, 1200, 2000)).astype(np.uint16)
+    k16, p16, q16, s16, _ = parity.place(r16, d16)
+    r10 = rng.integers(0, 1024, (3, 270, 480)).astype(np.uint16)
+    d10 = rng.integers(0, 1024, (3, 270, 480)).astype(np.uint16)
+    k10, p10, q10, s10, _ = parity.place(r10, d10)
+    descs = [(p10, q10, 480, 270, s10, None), (q10, p10, 480, 270, s10, None)]
+    jobs = {
+        "stats": (lambda st: lib.vqx_plane_stats_submit(p10, q10, 480, 270, s10, 10, 3, stream=st),
+                  lib.vqx_plane_stats(p10, q10, 480, 270, s10, 10, 3)),
+        "int_psnr": (lambda st: lib.vqx_plane_int_psnr_submit(p16, q16, 2000, 1200, s16, 16, 2, stream=st),
+                     lib.vqx_plane_int_psnr(p16, q16, 2000, 1200, s16, 16, 2)),
+        "planes": (lambda st: lib.vqx_planes_stats_submit(descs, 10, 3, stream=st),
+                   lib.vqx_planes_stats(descs, 10, 3)),
+        "ordered": (lambda st: lib.vqx_plane_stats_ordered_submit(p16, q16, 2000, 1200, s16, 16, 2,
+                                                                  stream=st),
+                    lib.vqx_plane_stats_ordered(p16, q16, 2000, 1200, s16, 16, 2)),
+    }
+    torch.cuda.synchronize()
+    bad = []
+
+    def worker(name):
+        submit, want = jobs[name]
+        st = torch.cuda.Stream()
+        pend = []
+        for i in range(15):
+            pend.append(submit(st))
+            if i % 3 == 2:  # keep a few in flight, finish out of order
+                for p in pend[::-1]:
+                    if p.finish().tobytes() != want.tobytes():
+                        bad.append(name)
+                pend = []
+        for p in pend:
+            if p.finish().tobytes() != want.tobytes():
+                bad.append(name)
+
+    th = [threading.Thread(target=worker, args=(k,)) for k in jobs]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not bad, bad
