@@ -206,6 +206,160 @@ WORKLOADS = {
 HEADLINE = "3840x2160_16bit_x32"
 
 
+# ---------------------------------------------------------------- psnr_hvs terms
+# "ADR-1397: GPU psnr_hvs twins reproduce the CPU's running float sum bit for
+# bit" gives 64 terms per 8x8 block and 10 802 176 terms for a 3840x2160 luma
+# plane (Context), of which 15 to 32 % are nonzero (Consequences).  Blocks
+# every 7 samples in each direction give exactly that count (548 x 308 blocks
+# at 3840x2160), so term counts of other sizes follow the same grid.  The
+# terms themselves (transform, CSF and masking) are not on the pages: the
+# stand-in below draws non-negative float32 values of the same shape.
+
+
+def hvs_blocks(width, height):
+    """8x8 blocks at a step of 7 samples: ((w - 8) // 7 + 1) * ((h - 8) // 7 + 1)."""
+    if width < 8 or height < 8:
+        return 0
+    return ((width - 8) // 7 + 1) * ((height - 8) // 7 + 1)
+
+
+def hvs_term_count(width, height):
+    return 64 * hvs_blocks(width, height)
+
+
+# A fixed stand-in for a frequency weighting of the 64 positions of a block:
+# 1 / (1 + (u + v) / 2) for coefficient (u, v), row order.  Not a CSF table.
+_HVS_POS_WEIGHT = np.array([1.0 / (1.0 + (u + v) / 2.0) for v in range(8) for u in range(8)],
+                           np.float32)
+
+
+def _hvs_masked(wl, rng, n):
+    """Masked-coefficient-error stand-in: the nonzero share q is drawn from
+    U[0.15, 0.32] per plane; a nonzero term is fl(fl(e * w)^2) with e =
+    fl(k - thr), k an integer error 1 + Geometric(0.3) scaled by 2^(bpc-8),
+    thr ~ U[0, 1), and w the block position's weight times U[0.5, 1)."""
+    q = rng.uniform(0.15, 0.32)
+    nz = rng.random(n) < q
+    k = (1 + rng.geometric(0.3, n)).astype(np.float32) * np.float32(1 << (wl.bpc - 8))
+    thr = rng.random(n, dtype=np.float32)
+    e = (k - thr).astype(np.float32)
+    pos = np.arange(n) % 64
+    w = (_HVS_POS_WEIGHT[pos] * rng.uniform(0.5, 1.0, n).astype(np.float32)).astype(np.float32)
+    ew = (e * w).astype(np.float32)
+    t = (ew * ew).astype(np.float32)
+    return np.where(nz, t, np.float32(0)).astype(np.float32)
+
+
+def _hvs_ones(_wl, _rng, n):
+    """Every term 1.0: the running float sum stops at 2^24."""
+    return np.ones(n, np.float32)
+
+
+def _hvs_ties(_wl, rng, n):
+    """Terms from {0.5, 1, 1.5, 2, 3} times a power of two drawn from
+    2^-2..2^2: many additions land exactly halfway between two floats."""
+    base = rng.choice(np.array([0.5, 1.0, 1.5, 2.0, 3.0], np.float32), n)
+    return (base * np.exp2(rng.integers(-2, 3, n)).astype(np.float32)).astype(np.float32)
+
+
+def _hvs_drift(_wl, rng, n):
+    """2000 terms from U[16000, 16600] (a sum near 1.94 * 2^24, where the
+    float sum's ulp is 2), then terms from U[0.8, 0.999], below half that ulp:
+    the float sum stalls under 2^25 while the exact sum passes it."""
+    head = min(2000, n)
+    t = np.empty(n, np.float32)
+    t[:head] = rng.uniform(16000.0, 16600.0, head).astype(np.float32)
+    t[head:] = rng.uniform(0.8, 0.999, n - head).astype(np.float32)
+    return t
+
+
+def _hvs_subnormal(_wl, rng, n):
+    """Subnormal terms (multiples of 2^-149 below 2^-126): the sum starts in
+    the subnormal range and crosses into the normal one."""
+    return (rng.integers(0, 1 << 10, n).astype(np.float64) * 2.0 ** -149).astype(np.float32)
+
+
+def _hvs_wide(_wl, rng, n):
+    """Log-uniform magnitudes over 2^-40..2^40, a third of them zero: jumps
+    over many binades at once."""
+    t = np.exp2(rng.uniform(-40.0, 40.0, n)).astype(np.float32)
+    t[rng.random(n) < 1.0 / 3.0] = 0.0
+    return t
+
+
+def _hvs_zeros(_wl, _rng, n):
+    return np.zeros(n, np.float32)
+
+
+_HVS_MAKERS = {
+    "masked": _hvs_masked,
+    "ones": _hvs_ones,
+    "ties": _hvs_ties,
+    "drift": _hvs_drift,
+    "subnormal": _hvs_subnormal,
+    "wide": _hvs_wide,
+    "zeros": _hvs_zeros,
+}
+
+
+@dataclass(frozen=True)
+class HvsWorkload:
+    """``n_planes`` planes of psnr_hvs terms of a width x height luma plane
+    (or ``n_terms`` terms when given).  Plane p draws from child p of
+    ``SeedSequence(seed)``."""
+
+    name: str
+    width: int
+    height: int
+    bpc: int
+    n_planes: int
+    seed: int
+    kind: str
+    n_terms_override: int = 0
+    note: str = ""
+
+    @property
+    def n_terms(self):
+        return self.n_terms_override or hvs_term_count(self.width, self.height)
+
+    @property
+    def plane_bytes(self):
+        return 4 * self.n_terms
+
+    def generate(self, planes=None):
+        """float32 array (len(planes), n_terms)."""
+        idx = range(self.n_planes) if planes is None else list(planes)
+        children = np.random.SeedSequence(self.seed).spawn(self.n_planes)
+        out = np.empty((len(idx), self.n_terms), np.float32)
+        for k, p in enumerate(idx):
+            rng = np.random.Generator(np.random.PCG64(children[p]))
+            out[k] = _HVS_MAKERS[self.kind](self, rng, self.n_terms)
+        return out
+
+
+HVS_WORKLOADS = {
+    "hvs_576x324_8bit_x4": HvsWorkload("hvs_576x324_8bit_x4", 576, 324, 8, 4, 31, "masked",
+                                       note="Netflix 576x324 luma stand-in"),
+    "hvs_1920x1080_10bit_x4": HvsWorkload("hvs_1920x1080_10bit_x4", 1920, 1080, 10, 4, 32,
+                                          "masked", note="1920x1080 10-bit luma stand-in"),
+    "hvs_3840x2160_8bit_x32": HvsWorkload("hvs_3840x2160_8bit_x32", 3840, 2160, 8, 32, 33,
+                                          "masked", note="3840x2160 luma batch (BBB stand-in)"),
+    "hvs_3840x2160_10bit_x2": HvsWorkload("hvs_3840x2160_10bit_x2", 3840, 2160, 10, 2, 34,
+                                          "masked", note="3840x2160 10-bit luma"),
+    "hvs_ones_2e24": HvsWorkload("hvs_ones_2e24", 0, 0, 8, 1, 35, "ones",
+                                 n_terms_override=(1 << 24) + 4096 + 77,
+                                 note="stalls at 2^24"),
+    "hvs_ties": HvsWorkload("hvs_ties", 0, 0, 8, 2, 36, "ties", n_terms_override=3_000_017),
+    "hvs_drift": HvsWorkload("hvs_drift", 0, 0, 8, 2, 37, "drift", n_terms_override=2_000_003),
+    "hvs_subnormal": HvsWorkload("hvs_subnormal", 0, 0, 8, 2, 38, "subnormal",
+                                 n_terms_override=1_000_033),
+    "hvs_wide": HvsWorkload("hvs_wide", 0, 0, 8, 2, 39, "wide", n_terms_override=1_500_007),
+    "hvs_zeros": HvsWorkload("hvs_zeros", 0, 0, 8, 1, 40, "zeros", n_terms_override=70_001),
+}
+
+HVS_HEADLINE = "hvs_3840x2160_8bit_x32"
+
+
 def with_layout(planes, stride_bytes=None, offset_bytes=0):
     """Copy dense planes (n, h, w) into a flat byte buffer with row pitch
     ``stride_bytes`` and ``offset_bytes`` of lead-in, the layout the library

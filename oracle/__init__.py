@@ -1,5 +1,5 @@
-"""CPU oracle for the fused float_psnr noise and float_moment statistics, and
-for the integer psnr.
+"""CPU oracle for the fused float_psnr noise and float_moment statistics, for
+the integer psnr and for the psnr_hvs plane sum.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference leg of ``bench.py`` may import this package.  The GPU
@@ -65,6 +65,9 @@ class Oracle:
         lib.vqx_oracle_batch.restype = i
         lib.vqx_oracle_int_psnr_batch.argtypes = [vp, vp, i, i, sz, i, i, vp]
         lib.vqx_oracle_int_psnr_batch.restype = i
+        i64 = ctypes.c_int64
+        lib.vqx_oracle_hvs_batch.argtypes = [vp, i64, i64, i, i, vp, vp]
+        lib.vqx_oracle_hvs_batch.restype = i
         lib.vqx_oracle_psnr_cap.argtypes = [i]
         lib.vqx_oracle_psnr_cap.restype = ctypes.c_double
         self._lib = lib
@@ -129,6 +132,34 @@ class Oracle:
             dist = dist[None]
         n, h, w = ref.shape
         return self.int_psnr(ref, dist, w, h, w * ref.itemsize, bpc, n)
+
+    def hvs(self, terms, bpc, n_terms=None, pitch=None, n_planes=None):
+        """psnr_hvs plane sums and scores of float32 terms.
+
+        ``terms`` is a float32 array: shape (n_planes, pitch) or (n,) for one
+        plane; ``n_terms`` (default: the last axis) terms of each plane are
+        added.  Returns ``(sums, scores)``, float32 arrays of n_planes."""
+        terms = np.ascontiguousarray(terms)
+        if terms.dtype != np.float32:
+            raise ValueError("terms must be float32")
+        if terms.ndim == 1:
+            terms = terms[None]
+        if pitch is None:
+            pitch = terms.shape[-1]
+        if n_planes is None:
+            n_planes = terms.size // pitch if pitch else 0
+        if n_terms is None:
+            n_terms = pitch
+        if n_planes > 0 and (n_planes - 1) * pitch + n_terms > terms.size:
+            raise ValueError("term buffer smaller than the planes need")
+        sums = np.zeros(n_planes, np.float32)
+        scores = np.zeros(n_planes, np.float32)
+        rc = self._lib.vqx_oracle_hvs_batch(terms.ctypes.data, n_terms, pitch, n_planes, bpc,
+                                            sums.ctypes.data if n_planes else None,
+                                            scores.ctypes.data if n_planes else None)
+        if rc != 0:
+            raise ValueError("oracle rejected the arguments (status %d)" % rc)
+        return sums, scores
 
     def frames(self, ref, dist, bpc, scores=True, units=True):
         """Convenience form for dense arrays of shape (n, h, w) or (h, w)."""

@@ -38,8 +38,8 @@
  * (Decision) and ADR-1447 (Decision) state that these integers, divided by
  * scaler^2 (or scaler), are the CPU's terms and sums.
  *
- * The integer psnr (vqx_oracle_int_psnr_frame) is stated beside them, with
- * its own readings.
+ * The integer psnr (vqx_oracle_int_psnr_frame) and the psnr_hvs plane sum
+ * (vqx_oracle_hvs_plane) are stated beside them, with their own readings.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -fno-tree-vectorize.
  * Contraction must stay off: the pages' CPU reference is a strict build.
@@ -241,6 +241,49 @@ int vqx_oracle_batch(const void *ref, const void *dist, int w, int h, size_t str
         if (scores) rc = vqx_oracle_scores_frame(r, d, w, h, stride, bpc, &scores[f]);
         if (rc == VQX_ORACLE_OK && units)
             rc = vqx_oracle_units_frame(r, d, w, h, stride, bpc, &units[f]);
+        if (rc != VQX_ORACLE_OK) return rc;
+    }
+    return VQX_ORACLE_OK;
+}
+
+/* psnr_hvs plane score, summation step.
+ *
+ * "ADR-1397: GPU psnr_hvs twins reproduce the CPU's running float sum bit for
+ * bit", sections Context and Decision ("Sum on the host"): every masked
+ * coefficient error of a plane (64 per 8x8 block, the block's values in row
+ * order, blocks in raster order) is added, one after another, into a single
+ * float that starts at zero; the total is then divided, in float, by the
+ * number of terms and by the squared sample maximum.  The strict build of the
+ * CPU reference means every addition and division is one IEEE single
+ * operation, rounded to nearest even, subnormals kept.
+ *
+ * The terms themselves (transform, CSF and masking) are not on the pages;
+ * here they are the input.  Readings taken (also listed in the design notes):
+ *  - the two divisions happen in the order the page names them: first by the
+ *    term count converted to float, then by the squared maximum;
+ *  - the squared maximum is the float product of (2^bpc - 1) with itself.
+ */
+int vqx_oracle_hvs_plane(const float *terms, int64_t n_terms, int bpc, float *sum, float *score) {
+    if (!terms || !sum || !score || n_terms < 1 || !valid_bpc(bpc)) return VQX_ORACLE_EINVAL;
+    float s = 0.0f;
+    for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];
+    const float peak = (float)((1u << bpc) - 1u);
+    float q = s / (float)n_terms;
+    q = q / (peak * peak);
+    *sum = s;
+    *score = q;
+    return VQX_ORACLE_OK;
+}
+
+/* n_planes planes of n_terms terms, plane p starting p * pitch floats after
+ * the base.  Planes are independent. */
+int vqx_oracle_hvs_batch(const float *terms, int64_t n_terms, int64_t pitch, int n_planes, int bpc,
+                         float *sums, float *scores) {
+    if (n_planes < 0 || pitch < n_terms || (n_planes > 0 && (!sums || !scores)))
+        return VQX_ORACLE_EINVAL;
+    for (int p = 0; p < n_planes; p++) {
+        const int rc = vqx_oracle_hvs_plane(terms + (size_t)p * (size_t)pitch, n_terms, bpc,
+                                            &sums[p], &scores[p]);
         if (rc != VQX_ORACLE_OK) return rc;
     }
     return VQX_ORACLE_OK;

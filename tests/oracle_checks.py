@@ -12,6 +12,9 @@ Nothing here re-types the oracle's arithmetic.  The independent facts used are:
   (``rne24``), which never touches the float hardware;
 - correctly rounded conversions of exact rationals (``float(Fraction)``);
 - closed forms (identical planes, swaps, hand-derived one-pixel values);
+- for the psnr_hvs plane sum: exact rationals rounded to binary32 by an
+  integer-only rule (``f32_round``), numpy's sequential float32 running sum,
+  and hand-worked sums (``tests/golden/hvs_sums.txt``);
 - the figures the pages print (``tests/golden/page_figures.txt``).
 """
 import math
@@ -394,7 +397,147 @@ def check_int_psnr_layout(orc):
             assert out[f].tobytes() == alone.tobytes()
 
 
+# ---------------------------------------------------------------- psnr_hvs plane sum
+def f32_round(x):
+    """Round an exact rational to IEEE-754 binary32, to nearest with ties to
+    the even significand, subnormals kept (exponent floor -126), in integer
+    arithmetic only."""
+    x = Fraction(x)
+    if x == 0:
+        return Fraction(0)
+    sign = -1 if x < 0 else 1
+    x = abs(x)
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    if Fraction(2) ** e > x:
+        e -= 1
+    e = max(e, -126)
+    ulp = Fraction(2) ** (e - 23)
+    q = x / ulp
+    n = q.numerator // q.denominator
+    r = q - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def _hvs_value(tok):
+    """A golden-file token: a decimal, or m*s<k> / s<k> for m * 2^k.  The
+    decimals are rounded to float32 exactly as a C float literal is."""
+    if "s" in tok:
+        m, _, k = tok.partition("s")
+        m = int(m.rstrip("*")) if m else 1
+        return Fraction(m) * Fraction(2) ** int(k)
+    return f32_round(Fraction(tok))
+
+
+def _exact_running_sum(terms):
+    s = Fraction(0)
+    for t in terms:
+        s = f32_round(s + Fraction(float(t)))
+    return s
+
+
+def _hvs_sets(n=3000):
+    """Seeded term sets of several shapes (small, for the rational reference)."""
+    out = []
+    for kind in ("masked", "ties", "subnormal", "wide", "drift"):
+        w = wl.HvsWorkload("pin_" + kind, 0, 0, 10, 1, 90 + len(out), kind, n_terms_override=n)
+        out.append(w.generate()[0])
+    return out
+
+
+def check_hvs_sum_exact_rounding(orc):
+    """The oracle's plane sum equals the running sum taken with exact
+    rationals and an explicit binary32 rounding after every addition."""
+    for t in _hvs_sets():
+        s, _ = orc.hvs(t, 10)
+        assert Fraction(float(s[0])) == _exact_running_sum(t)
+
+
+def check_hvs_sum_matches_numpy_accumulate(orc):
+    """The plane sum is the last element of numpy's float32 running sum
+    (``np.add.accumulate``, a strictly sequential float32 loop), on larger
+    sets and on a 4:2:0-sized plane of the masked stand-in."""
+    sets = [wl.HvsWorkload("acc_" + k, 0, 0, 8, 1, 70 + i, k, n_terms_override=200_003).generate()[0]
+            for i, k in enumerate(("masked", "ties", "wide", "subnormal", "drift"))]
+    sets.append(wl.HVS_WORKLOADS["hvs_576x324_8bit_x4"].generate([1])[0])
+    for t in sets:
+        s, _ = orc.hvs(t, 8)
+        ref = np.add.accumulate(t, dtype=np.float32)[-1]
+        assert s[0].tobytes() == ref.tobytes(), (s[0], ref)
+
+
+def check_hvs_golden_sums(orc):
+    """Hand-worked running sums (ties to even, lost quarter-ulps, order,
+    subnormals, 0.1 + 0.2): ``tests/golden/hvs_sums.txt``."""
+    for row in read_table("hvs_sums.txt"):
+        want = _hvs_value(row[0])
+        terms = np.array([float(_hvs_value(x)) for x in row[1:]], np.float32)
+        s, _ = orc.hvs(terms, 8)
+        assert Fraction(float(s[0])) == want, (row, float(s[0]))
+
+
+def check_hvs_ones_stall_at_2_24(orc):
+    """A plane of ones: the float sum reaches 2^24 and stays there (every
+    later addition is a tie resolved to the even 2^24)."""
+    n = (1 << 24) + 77
+    s, sc = orc.hvs(np.ones(n, np.float32), 8)
+    assert float(s[0]) == 2.0 ** 24
+
+
+def check_hvs_score_closed_forms(orc):
+    """score = (sum / count) / peak^2 in float.  Terms equal to peak^2 give
+    exactly 1 at 8, 10 and 12 bits (every step exact); a plane whose sum is
+    3 and count 3 gives the float nearest 1 / 65025 at 8 bits; and on
+    sums where the order of the two divisions matters, the count comes first."""
+    for bpc in (8, 10, 12):
+        peak = (1 << bpc) - 1
+        n = 5 if bpc < 12 else 1
+        s, sc = orc.hvs(np.full(n, peak * peak, np.float32), bpc)
+        assert float(s[0]) == n * peak * peak and float(sc[0]) == 1.0, (bpc, s, sc)
+    s, sc = orc.hvs(np.ones(3, np.float32), 8)
+    assert Fraction(float(sc[0])) == f32_round(Fraction(1, 65025))
+    rng = np.random.default_rng(5)
+    found = 0
+    for _ in range(4000):
+        v = f32_round(Fraction(int(rng.integers(1, 1 << 24))) / int(rng.integers(1, 1 << 10)))
+        n = int(rng.integers(2, 2000))
+        count_first = f32_round(f32_round(v / n) / 65025)
+        one_division = f32_round(v / f32_round(Fraction(n * 65025)))
+        if count_first == one_division:
+            continue
+        terms = np.zeros(n, np.float32)
+        terms[0] = float(v)
+        s, sc = orc.hvs(terms, 8)
+        assert Fraction(float(sc[0])) == count_first, (v, n)
+        found += 1
+        if found == 8:
+            break
+    assert found == 8
+
+
+def check_hvs_batch_layout(orc):
+    """Planes sit ``pitch`` floats apart; only the first n_terms of each are
+    added (the padding holds values that would change any sum), and each
+    plane's result equals the plane taken alone."""
+    rng = np.random.default_rng(11)
+    n, pitch, planes = 1001, 1100, 3
+    buf = np.full((planes, pitch), 1.0e6, np.float32)
+    buf[:, :n] = rng.uniform(0, 100, (planes, n)).astype(np.float32)
+    s, sc = orc.hvs(buf, 10, n_terms=n, pitch=pitch, n_planes=planes)
+    for p in range(planes):
+        s1, sc1 = orc.hvs(np.ascontiguousarray(buf[p, :n]), 10)
+        assert s[p].tobytes() == s1[0].tobytes() and sc[p].tobytes() == sc1[0].tobytes()
+        assert Fraction(float(s1[0])) == _exact_running_sum(buf[p, :n])
+
+
 ALL_CHECKS = [
+    check_hvs_sum_exact_rounding,
+    check_hvs_sum_matches_numpy_accumulate,
+    check_hvs_golden_sums,
+    check_hvs_ones_stall_at_2_24,
+    check_hvs_score_closed_forms,
+    check_hvs_batch_layout,
     check_int_psnr_closed_forms,
     check_int_psnr_identical_and_swap,
     check_int_psnr_against_float_units,

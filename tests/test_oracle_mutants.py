@@ -84,6 +84,30 @@ MUTANTS = [
     ("integer psnr: distorted plane read as the reference",
      "(int64_t)sample_at(rrow, x, bpc) - (int64_t)sample_at(drow, x, bpc)",
      "(int64_t)sample_at(rrow, x, bpc) - (int64_t)sample_at(rrow, x, bpc)"),
+    ("hvs: double accumulator",
+     "float s = 0.0f;\n    for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];",
+     "double s = 0.0;\n    for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];"),
+    ("hvs: terms added last to first",
+     "for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];",
+     "for (int64_t i = n_terms - 1; i >= 0; i--) s = s + terms[i];"),
+    ("hvs: two halves summed apart",
+     "for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];",
+     "float s2 = 0.0f;\n    for (int64_t i = 0; i < n_terms; i++) { if (i < n_terms / 2) s = s + terms[i]; else s2 = s2 + terms[i]; }\n    s = s + s2;"),
+    ("hvs: first term skipped",
+     "for (int64_t i = 0; i < n_terms; i++) s = s + terms[i];",
+     "for (int64_t i = 1; i < n_terms; i++) s = s + terms[i];"),
+    ("hvs: one division by count times peak^2",
+     "float q = s / (float)n_terms;\n    q = q / (peak * peak);",
+     "float q = s / ((float)n_terms * (peak * peak));"),
+    ("hvs: divided by the block count",
+     "float q = s / (float)n_terms;",
+     "float q = s / (float)(n_terms / 64 > 0 ? n_terms / 64 : 1);"),
+    ("hvs: peak 2^bpc",
+     "const float peak = (float)((1u << bpc) - 1u);",
+     "const float peak = (float)(1u << bpc);"),
+    ("hvs: plane pitch ignored",
+     "terms + (size_t)p * (size_t)pitch, n_terms",
+     "terms + (size_t)p * (size_t)n_terms, n_terms"),
     ("sample byte order swapped",
      "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return v;",
      "memcpy(&v, row + 2 * (size_t)x, sizeof v);\n    return (uint16_t)((v >> 8) | (v << 8));"),

@@ -51,3 +51,21 @@ def test_page_figures_bound():
     assert two_digits(oracle.moment_bound(n4k, 53)) == float(f["bound_3840x2160_full_range"])
     assert two_digits(oracle.moment_bound(2560 * 1440, 53)) == float(f["bound_2560x1440"])
     assert oracle.mse_bound(n4k, 2 ** 53 - 1) == 0.0
+
+
+def test_hvs_workload_matches_page_figures():
+    """ADR-1397: the term count of a 3840x2160 plane and the share of nonzero
+    terms that the synthetic psnr_hvs planes are built to."""
+    import numpy as np
+
+    from exact_full_reference_gb300 import workloads as wl
+
+    f = oc.page_figures()
+    assert wl.hvs_term_count(3840, 2160) == int(f["hvs_terms_3840x2160"])
+    assert wl.hvs_term_count(3840, 2160) % int(f["hvs_terms_per_block"]) == 0
+    lo, hi = float(f["hvs_nonzero_min"]), float(f["hvs_nonzero_max"])
+    for name in ("hvs_576x324_8bit_x4", "hvs_1920x1080_10bit_x4"):
+        w = wl.HVS_WORKLOADS[name]
+        for t in w.generate():
+            share = np.count_nonzero(t) / t.size
+            assert lo - 0.01 <= share <= hi + 0.01, (name, share)
