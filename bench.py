@@ -70,12 +70,14 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["stats", "int_psnr", "ordered", "planes420"], default="stats",
+    p.add_argument("--op", choices=["stats", "int_psnr", "ordered", "planes420", "hvs"],
+                   default="stats",
                    help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
                         "the integer psnr (vqx_plane_int_psnr); ordered: the CPU-order replay "
                         "past 2^53 units (vqx_plane_stats_ordered_submit / _finish); "
                         "planes420: the workload as the luma of 4:2:0 video, Y, Cb and Cr "
-                        "through one vqx_planes_stats call a step")
+                        "through one vqx_planes_stats call a step; hvs: psnr_hvs plane sums "
+                        "of a batch of term planes (vqx_psnr_hvs_sum_submit / _finish)")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
                    help="write the DRAM traffic record of the fused kernel from an ncu report "
                         "(read here with ncu -i; needs no GPU) and exit")
@@ -639,10 +641,241 @@ def run_ours(args, wlo):
     return 0
 
 
+# ---------------------------------------------------------------- psnr_hvs plane sums
+HVS_UNIT = "planes/s"
+
+
+def hvs_metric(hw):
+    return "planes/s and HBM GB/s (psnr_hvs plane sums), %d terms a plane (%dx%d luma), 1 GB300" % (
+        hw.n_terms, hw.width, hw.height)
+
+
+def time_oracle_hvs(hw, terms, seconds, cores, n_terms=None):
+    """The oracle's plane sums of ``terms`` (one plane, or its first
+    ``n_terms`` terms, per thread) until ``seconds`` have passed.  Returns
+    (planes/s, planes done, elapsed s)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    orc = oracle.load()
+    n = terms.shape[1] if n_terms is None else n_terms
+
+    def one(k):
+        orc.hvs(terms[k % terms.shape[0], :n], hw.bpc)
+        return n
+
+    done = 0
+    k = 0
+    t0 = time.perf_counter()
+    while True:
+        with ThreadPoolExecutor(cores) as ex:
+            done += sum(ex.map(one, range(k, k + cores)))
+        k += cores
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    planes = done / terms.shape[1]
+    return planes / el, planes, el
+
+
+def run_hvs_reference(args, hw):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    terms = hw.generate(range(min(hw.n_planes, max(cores, 1))))
+    per_step_s = min(0.5, 120.0 / max(args.steps + args.warmup, 1))
+    rate, _, _ = time_oracle_hvs(hw, terms[:1], 0.0, 1, n_terms=min(hw.n_terms, 1 << 20))
+    n = int(max(1, min(hw.n_terms, rate * hw.n_terms * per_step_s)))
+    for _ in range(args.warmup):
+        time_oracle_hvs(hw, terms, 0.0, cores, n_terms=n)
+    t0 = time.perf_counter()
+    planes = 0.0
+    for _ in range(args.steps):
+        _, p, _ = time_oracle_hvs(hw, terms, 0.0, cores, n_terms=n)
+        planes += p
+    el = time.perf_counter() - t0
+    value = planes / el
+    line = {
+        "impl": "reference", "metric": hvs_metric(hw), "value": value, "unit": HVS_UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": hw.name, "planes": hw.n_planes, "terms_per_plane": hw.n_terms,
+                   "oracle": "plain C, one float running sum per plane"},
+        "cpu_baseline": {"value": value, "unit": HVS_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d planes' first %d terms per step, one plane per thread"
+                                   % (cores, n)},
+        "e2e": {"value": value, "unit": HVS_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_hvs(args, hw):
+    """One step = one batch of term planes resident in HBM through
+    vqx_psnr_hvs_sum_submit + _finish (tables, walk, read-back, score),
+    pipelined one deep like the plane statistics."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    __import__("__graft_entry__").build()
+    import exact_full_reference_gb300 as vqx
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    terms = hw.generate()
+    n_planes, n_terms = terms.shape
+    d_terms = torch.from_numpy(terms).to(dev)
+    torch.cuda.synchronize()
+    so = vqx.library()
+    out = np.zeros(n_planes, vqx.HVS_PLANE_DTYPE)
+    out_p = out.ctypes.data
+
+    def submit(ptr=None):
+        handle = ctypes.c_void_p()
+        rc = so.vqx_psnr_hvs_sum_submit(ptr or d_terms.data_ptr(), n_terms, n_terms, n_planes,
+                                        hw.bpc, sh, vqx.VQX_SUBMIT_PLANES_READY if ptr is None else 0,
+                                        ctypes.byref(handle))
+        if rc != 0:
+            raise RuntimeError("submit: %s" % vqx.status_string(rc))
+        return handle
+
+    def finish(handle):
+        rc = so.vqx_psnr_hvs_sum_finish(handle, out_p)
+        if rc != 0:
+            raise RuntimeError("finish: %s" % vqx.status_string(rc))
+
+    def steps(k):
+        prev = None
+        for _ in range(k):
+            cur = submit()
+            if prev is not None:
+                finish(prev)
+            prev = cur
+        if prev is not None:
+            finish(prev)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    steps(max(args.warmup, 3))
+    torch.cuda.synchronize()
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
+    if terms.nbytes < 2 * l2_bytes:
+        raise SystemExit("psnr_hvs bench batches must be larger than twice the L2")
+
+    def timed_region(instrumented):
+        barrier()
+        torch.cuda.synchronize()
+        vqx.profile_enable(instrumented)
+        vqx.profile_read(reset=True)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        ev0.record(stream)
+        steps(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier()
+        prof = vqx.profile_read(reset=True)
+        vqx.profile_enable(False)
+        return reduce_max(ev0.elapsed_time(ev1), pg, dev), prof, t0, t1
+
+    clocks = ClockSampler(gpu_smi_id(torch, dev))
+    time.sleep(0.3)
+    elapsed_ms, counted, t_wall0, t_wall1 = timed_region(False)
+    inst_ms, prof, _, _ = timed_region(True)
+    time.sleep(0.2)
+    clocks.stop()
+    value = job_throughput(world, n_planes, args.steps, elapsed_ms / 1e3)
+    peak, peak_kind = measured_peak()
+    launches = max(prof["stage1_launches"], 1)
+    avg_ms = prof["stage1_ms"] / launches
+    bytes_per_launch = prof["stage1_bytes"] / launches
+    achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                "timing": "CUDA events recorded by the library around each launch in a second "
+                          "timed region of the same %d steps" % args.steps,
+                "instrumented_region_ms_per_step": inst_ms / args.steps,
+                "kernel": "hvs_tables", "avg_launch_us": avg_ms * 1e3,
+                "bytes_per_launch": bytes_per_launch,
+                "walk_avg_us": prof["stage2_ms"] / launches * 1e3}
+
+    e2e = None
+    if not args.no_e2e:
+        h_terms = torch.from_numpy(terms).pin_memory()
+        d_e2e = torch.empty_like(d_terms)
+        k = max(1, min(args.e2e_steps, args.steps))
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(k):
+            with torch.cuda.stream(stream):
+                d_e2e.copy_(h_terms, non_blocking=True)
+            finish(submit(d_e2e.data_ptr()))
+        torch.cuda.synchronize()
+        el = reduce_max(time.perf_counter() - t0, pg, dev)
+        e2e = {"value": job_throughput(world, n_planes, k, el), "unit": HVS_UNIT, "steps": k,
+               "h2d_bytes_per_step": int(terms.nbytes),
+               "d2h_bytes_per_step": int(n_planes * 16),
+               "api": "copy of pinned host terms on the call's stream, then vqx_psnr_hvs_sum_submit / _finish"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cores = host_cores()
+        sub = terms[: min(n_planes, cores)]
+        rate, planes, el = time_oracle_hvs(hw, sub, args.cpu_seconds, cores)
+        cpu = {"value": rate, "unit": HVS_UNIT, "cores": cores, "kind": "oracle",
+               "sample": "%.1f whole planes of %s (one per thread) in %.1f s" % (planes, hw.name, el)}
+
+    if rank == 0:
+        line = {
+            "metric": hvs_metric(hw), "value": value, "unit": HVS_UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "hbm_gbs": value * 4 * n_terms / 1e9 / world,
+            "config": {"workload": hw.name, "planes_per_gpu": n_planes, "terms_per_plane": n_terms,
+                       "bpc": hw.bpc, "batch_bytes": int(terms.nbytes),
+                       "l2": "terms %.2f GB per step, larger than the 129 MB L2; no flush"
+                             % (terms.nbytes / 1e9),
+                       "pipeline": "batch i + 1 submitted before batch i is finished "
+                                   "(vqx_psnr_hvs_sum_submit with VQX_SUBMIT_PLANES_READY / _finish)",
+                       "parallelism": "planes independent per GPU" if world > 1 else "1 GPU"},
+            "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu,
+            "clocks": clocks.summary(t_wall0, t_wall1),
+            "gpu_launches": int(counted["kernel_launches"]),
+            "replayed_leaves_max": int(out["replayed_leaves"].max()),
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     from exact_full_reference_gb300 import workloads as wl
 
+    if args.op == "hvs":
+        hw = wl.HVS_WORKLOADS[args.workload or wl.HVS_HEADLINE]
+        return run_hvs_reference(args, hw) if args.impl == "reference" else run_hvs(args, hw)
     wlo = wl.WORKLOADS[args.workload or wl.HEADLINE]
     if args.record_traffic:
         return write_traffic_record(args.record_traffic, wlo)

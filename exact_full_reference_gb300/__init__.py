@@ -60,6 +60,15 @@ INT_PSNR_DTYPE = np.dtype(
     ]
 )
 
+HVS_PLANE_DTYPE = np.dtype(
+    [
+        ("sum", "<f4"),
+        ("score", "<f4"),
+        ("flags", "<u4"),
+        ("replayed_leaves", "<u4"),
+    ]
+)
+
 
 class VqxProfile(ctypes.Structure):
     _fields_ = [
@@ -126,6 +135,14 @@ def library():
         lib.vqx_planes_stats_submit.restype = i
         lib.vqx_planes_stats_finish.argtypes = [vp, vp]
         lib.vqx_planes_stats_finish.restype = i
+        i64 = ctypes.c_int64
+        lib.vqx_psnr_hvs_sum.argtypes = [vp, i64, i64, i, i, vp, vp]
+        lib.vqx_psnr_hvs_sum.restype = i
+        lib.vqx_psnr_hvs_sum_submit.argtypes = [vp, i64, i64, i, i, vp, ctypes.c_uint,
+                                                ctypes.POINTER(vp)]
+        lib.vqx_psnr_hvs_sum_submit.restype = i
+        lib.vqx_psnr_hvs_sum_finish.argtypes = [vp, vp]
+        lib.vqx_psnr_hvs_sum_finish.restype = i
         lib.vqx_psnr_cap.argtypes = [i]
         lib.vqx_psnr_cap.restype = ctypes.c_double
         lib.vqx_status_string.argtypes = [i]
@@ -242,8 +259,10 @@ class Pending:
         if self._handle is False:
             raise RuntimeError("this batch was already finished")
         if out is None:
-            out = np.zeros(self.shape, INT_PSNR_DTYPE if self.kind == "int_psnr" else FRAME_STATS_DTYPE)
-        name = "vqx_planes_stats_finish" if self.kind == "planes" else "vqx_plane_%s_finish" % self.kind
+            dtype = {"int_psnr": INT_PSNR_DTYPE, "hvs": HVS_PLANE_DTYPE}.get(self.kind, FRAME_STATS_DTYPE)
+            out = np.zeros(self.shape, dtype)
+        name = {"planes": "vqx_planes_stats_finish", "hvs": "vqx_psnr_hvs_sum_finish"}.get(
+            self.kind, "vqx_plane_%s_finish" % self.kind)
         rc = getattr(library(), name)(self._handle, out.ctypes.data if out.size else None)
         self._handle, self._keep = False, None
         if check and rc != VQX_OK:
@@ -364,3 +383,45 @@ def profile_read(reset=False):
     p = VqxProfile()
     library().vqx_profile_read(ctypes.byref(p), 1 if reset else 0)
     return {k: getattr(p, k) for k, _ in VqxProfile._fields_}
+
+
+def _hvs_geometry(terms, n_terms, pitch, n_planes):
+    shape = tuple(getattr(terms, "shape", ()))
+    if pitch is None:
+        if not shape:
+            raise ValueError("plane_pitch is needed for a flat address")
+        pitch = int(shape[-1])
+    if n_terms is None:
+        n_terms = pitch
+    if n_planes is None:
+        n_planes = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    return int(n_terms), int(pitch), int(n_planes)
+
+
+def vqx_psnr_hvs_sum(terms, n_terms=None, pitch=None, n_planes=None, bpc=8, stream=None,
+                     out=None, check=True):
+    """psnr_hvs plane sums of device-resident float32 terms: shape
+    (n_planes, pitch) or (n,) for one plane, or an address with explicit
+    sizes.  Returns ``HVS_PLANE_DTYPE`` records (the sequential float sum and
+    the plane score); with ``check=False``, ``(records, status)``."""
+    n_terms, pitch, n_planes = _hvs_geometry(terms, n_terms, pitch, n_planes)
+    if out is None:
+        out = np.zeros(max(n_planes, 0), HVS_PLANE_DTYPE)
+    rc = library().vqx_psnr_hvs_sum(_address(terms), n_terms, pitch, n_planes, bpc,
+                                    _stream_handle(stream), out.ctypes.data if out.size else None)
+    if check and rc != VQX_OK:
+        _raise("vqx_psnr_hvs_sum", rc)
+    return out if check else (out, rc)
+
+
+def vqx_psnr_hvs_sum_submit(terms, n_terms=None, pitch=None, n_planes=None, bpc=8, stream=None,
+                            flags=0):
+    """The same without waiting: a ``Pending`` whose ``finish()`` gives the
+    records."""
+    n_terms, pitch, n_planes = _hvs_geometry(terms, n_terms, pitch, n_planes)
+    handle = ctypes.c_void_p()
+    rc = library().vqx_psnr_hvs_sum_submit(_address(terms), n_terms, pitch, n_planes, bpc,
+                                           _stream_handle(stream), flags, ctypes.byref(handle))
+    if rc != VQX_OK:
+        _raise("vqx_psnr_hvs_sum_submit", rc)
+    return Pending(handle.value, max(n_planes, 0), terms, "hvs")

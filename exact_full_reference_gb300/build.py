@@ -21,6 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD_DIR, "libvqx.so")
 SOURCES = [os.path.join(CSRC, "vqx_plane_stats.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "vqx_kernels.cuh"), os.path.join(CSRC, "vqx_ordered.cuh"),
+                     os.path.join(CSRC, "vqx_hvs.cuh"),
                      os.path.join(INCLUDE, "vqx.h"),
                      os.path.abspath(__file__)]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

@@ -1,0 +1,516 @@
+// psnr_hvs plane sum: the CPU's running float sum of a plane's terms,
+// reproduced on the device.
+//
+// "ADR-1397: GPU psnr_hvs twins reproduce the CPU's running float sum bit for
+// bit" (Context, Decision): the CPU adds every masked coefficient error of a
+// plane, one after another, into one float, so the rounding of each addition
+// depends on the sum so far.  The page's twin stores the terms and adds them
+// on the host; its Alternatives leave an order-preserving device reduction as
+// the open design.  This is one.
+//
+// - The terms are non-negative, so the running sum s never decreases.  While
+//   s stays in one binade b (the floats of biased exponent b; for b = 1 also
+//   the subnormals, which share its ulp), s = m u with u = 2^(b - 150), and
+//   fl(s + t) = (m + k) u, k being t / u rounded to nearest with a tie going
+//   to the even m + k.  The increment depends on s only through the parity of
+//   m, so a run of additions is a function of one bit: (K[p], p'[p]) for
+//   p = 0, 1, its transfer.  In float bits m u is the word ((b - 1) << 23) + m,
+//   so a state is its own bit pattern, its parity is bit 0, and applying K is
+//   an integer add to the bits, valid while they stay at or below
+//   (b + 1) << 23 (the top of the binade, 2^(b - 126), is reached exactly).
+// - A run's transfer for binade b comes from performing its additions (the
+//   float add, round to nearest even, subnormals kept) from the representative
+//   state m = 2^23 + p (m = p for b = 1), the smallest state of its parity:
+//   from any larger state of the same parity that stays in the binade every
+//   addition rounds the same way.  A run that leaves the binade from there has
+//   no transfer for b.
+// - The binade a run starts in is guessed from the sum of the terms before it
+//   (the float sum stays within a few per cent of it), and every run keeps
+//   transfers for two candidate binades.  Runs are leaves of kHvsLeaf terms (a
+//   warp, kHvsLane per lane) and nodes of kHvsLeaves leaves (a CTA).
+// - One warp per plane walks: windows of 32 nodes, composed by a warp scan and
+//   applied to the state; a node without a transfer for the state's binade, or
+//   one that would leave it, is walked leaf by leaf, and such a leaf lane by
+//   lane: the lanes' runs for the state's binade are composed, and the lane
+//   whose run would leave the binade adds its terms one by one with float adds
+//   from the true state.
+// Correctness does not depend on the guess: a wrong guess only sends more of
+// the walk down to single terms.
+//
+// The prefix the guess needs comes from a decoupled look-back (Merrill and
+// Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back", 2016)
+// across the CTAs of one launch: each CTA takes its node in block order,
+// publishes the node's sum, then adds its predecessors' published sums.  Its
+// wait is bounded; a CTA that gives up guesses from what it has.  The CTA
+// reads its node once, coalesced, into shared memory (summing and checking
+// the terms on the way); after the look-back each lane takes its own run
+// from there.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "vqx_kernels.cuh"
+
+namespace vqx {
+
+constexpr int kHvsLane = 32;                     // terms per lane
+constexpr int kHvsLeaf = 32 * kHvsLane;          // terms per leaf (a warp)
+constexpr int kHvsLeaves = 8;                    // leaves per node (warps per CTA)
+constexpr int kHvsNode = kHvsLeaf * kHvsLeaves;  // terms per node
+constexpr int kHvsThreads = 32 * kHvsLeaves;
+// A leaf in shared memory: its 256 vectors of 4 terms, vector q at q + q / 8
+// (16 bytes of padding after every 128), so that both the coalesced writes
+// and each lane's reads of its own run of 8 vectors are free of bank
+// conflicts.
+constexpr int kHvsLeafVecs = kHvsLeaf / 4;
+constexpr int kHvsLeafSlots = kHvsLeafVecs + kHvsLeafVecs / 8;
+constexpr size_t kHvsTablesSmem = (size_t)kHvsLeaves * kHvsLeafSlots * sizeof(float4);
+
+// A transfer word: K in bits 0-24 (at most 2^24), "no transfer" in bit 30,
+// the parity after the run in bit 31.
+constexpr uint32_t kHvsKMask = 0x01FFFFFFu;
+constexpr uint32_t kHvsBad = 0x40000000u;
+constexpr uint32_t kHvsPar = 0x80000000u;
+// Terms must lie in [0, 2^95) (-0 allowed): then no plane of up to 2^31 terms
+// can reach 2^127, as the float sum is below twice the exact sum.
+constexpr uint32_t kHvsTermLimit = 0x6F000000u;
+
+// Flags of a node record (the walk reports the range flag for the plane).
+constexpr uint32_t kHvsFlagRange = 1u;
+constexpr uint32_t kHvsFlagGuess = 4u;  // a look-back gave up (guesses only)
+
+// Look-back status words: the call's epoch in bits 34-63, the state in bits
+// 32-33, float bits in the low half.  Nothing clears them between calls: a
+// word of another epoch reads as empty.
+constexpr u64 kHvsAgg = 1ull << 32;
+constexpr u64 kHvsPrefix = 2ull << 32;
+constexpr uint32_t kHvsEpochMask = (1u << 30) - 1u;
+constexpr long long kHvsLookbackCycles = 20000000ll;  // about 10 ms
+
+struct HvsFn {
+    uint32_t k0, k1;  // transfer words for input parity 0 and 1
+};
+
+// Two candidate binades b and b + 1 of a run.
+struct __align__(16) HvsRec {
+    uint4 k;  // (b: k0, k1), (b + 1: k0, k1)
+    uint32_t b;
+    uint32_t pad[3];
+};
+
+struct HvsArgs {
+    const float *terms;
+    long long n_terms;  // per plane
+    long long pitch;    // floats from one plane to the next
+    int n_planes;
+    int n_leaves, n_nodes;  // per plane
+    int vec;                // 16-byte loads (base 16-byte aligned, pitch % 4 == 0)
+    int terms_ready;        // the terms were written before the launch ahead started
+    uint32_t epoch;         // this call's tag of its status words (1 .. 2^30 - 1)
+    HvsRec *leaves;         // [plane][leaf]
+    HvsRec *nodes;          // [plane][node]; pad[0] holds the node's flags
+    u64 *status;            // [plane][node]
+};
+
+// What the walk leaves per plane.
+struct HvsOut {
+    uint32_t sum_bits;
+    uint32_t flags;
+    uint32_t replayed_leaves;  // leaves walked lane by lane
+    uint32_t replayed_runs;    // lane runs added term by term
+};
+
+__device__ __forceinline__ HvsFn hvs_identity() { return {0u, kHvsPar}; }
+
+// Word of "a then b" for one input parity, given a's word.
+__device__ __forceinline__ uint32_t hvs_then(uint32_t ka, HvsFn b) {
+    if (ka & kHvsBad) return kHvsBad;
+    const uint32_t kb = (ka & kHvsPar) ? b.k1 : b.k0;
+    if (kb & kHvsBad) return kHvsBad;
+    const uint32_t k = (ka & kHvsKMask) + (kb & kHvsKMask);
+    return k > (1u << 24) ? kHvsBad : (k | (kb & kHvsPar));
+}
+
+__device__ __forceinline__ HvsFn hvs_compose(HvsFn a, HvsFn b) {
+    return {hvs_then(a.k0, b), hvs_then(a.k1, b)};
+}
+
+// Binade of a state (float bits): 1 for zero and the subnormals.
+__device__ __forceinline__ uint32_t hvs_binade(uint32_t s) { return max(s >> 23, 1u); }
+
+// Lower candidate binade for a run whose preceding terms add up to about x:
+// the binade of x (1 - 1/64), so that a float sum up to 1.6 % below the
+// estimate, or up to twice as far above, still has a transfer.
+__device__ __forceinline__ uint32_t hvs_guess(float x) {
+    return hvs_binade(__float_as_uint(__fmul_rn(x, 0.984375f)));
+}
+
+__device__ __forceinline__ bool hvs_bad_term(float t) {
+    const uint32_t u = __float_as_uint(t);
+    return u >= kHvsTermLimit && u != 0x80000000u;
+}
+
+// Transfer of adding t[0..kHvsLane) for binade b (1 <= b <= 253), found by
+// adding them from the two representative states.
+__device__ __forceinline__ HvsFn hvs_run_fn(const float (&t)[kHvsLane], uint32_t b) {
+    const uint32_t s0 = ((b - 1u) << 23) + (b == 1u ? 0u : (1u << 23));
+    float x0 = __uint_as_float(s0), x1 = __uint_as_float(s0 + 1u);
+#pragma unroll
+    for (int i = 0; i < kHvsLane; i++) {
+        x0 = __fadd_rn(x0, t[i]);
+        x1 = __fadd_rn(x1, t[i]);
+    }
+    const uint32_t lim = (b + 1u) << 23;
+    const uint32_t e0 = __float_as_uint(x0), e1 = __float_as_uint(x1);
+    HvsFn f;
+    f.k0 = e0 > lim ? kHvsBad : ((e0 - s0) | (e0 << 31));
+    f.k1 = e1 > lim ? kHvsBad : ((e1 - s0 - 1u) | (e1 << 31));
+    return f;
+}
+
+// Transfers of adding a lane's run (its 8 vectors at run[0..8) of a leaf in
+// shared memory) for binades b and b + 1.
+__device__ __forceinline__ void hvs_run_fns2(const float4 *run, uint32_t b, HvsFn &fb, HvsFn &fb1) {
+    const uint32_t s0 = ((b - 1u) << 23) + (b == 1u ? 0u : (1u << 23));
+    const uint32_t u0 = (b << 23) + (1u << 23);  // binade b + 1 (never 1)
+    float x0 = __uint_as_float(s0), x1 = __uint_as_float(s0 + 1u);
+    float y0 = __uint_as_float(u0), y1 = __uint_as_float(u0 + 1u);
+#pragma unroll
+    for (int i = 0; i < kHvsLane / 4; i++) {
+        const float4 v = run[i];
+        const float t[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            x0 = __fadd_rn(x0, t[c]);
+            x1 = __fadd_rn(x1, t[c]);
+            y0 = __fadd_rn(y0, t[c]);
+            y1 = __fadd_rn(y1, t[c]);
+        }
+    }
+    const uint32_t lim = (b + 1u) << 23, lim1 = (b + 2u) << 23;
+    const uint32_t e0 = __float_as_uint(x0), e1 = __float_as_uint(x1);
+    const uint32_t g0 = __float_as_uint(y0), g1 = __float_as_uint(y1);
+    fb.k0 = e0 > lim ? kHvsBad : ((e0 - s0) | (e0 << 31));
+    fb.k1 = e1 > lim ? kHvsBad : ((e1 - s0 - 1u) | (e1 << 31));
+    fb1.k0 = g0 > lim1 ? kHvsBad : ((g0 - u0) | (g0 << 31));
+    fb1.k1 = g1 > lim1 ? kHvsBad : ((g1 - u0 - 1u) | (g1 << 31));
+}
+
+// Ordered reduction: lane 0 gets lanes 0..31 composed in lane order.
+__device__ __forceinline__ HvsFn hvs_reduce(HvsFn f) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        HvsFn o;
+        o.k0 = __shfl_down_sync(0xffffffffu, f.k0, off);
+        o.k1 = __shfl_down_sync(0xffffffffu, f.k1, off);
+        f = hvs_compose(f, o);
+    }
+    return f;
+}
+
+// Inclusive scan: lane j gets lanes 0..j composed in order.
+__device__ __forceinline__ HvsFn hvs_scan(HvsFn f, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        HvsFn o;
+        o.k0 = __shfl_up_sync(0xffffffffu, f.k0, off);
+        o.k1 = __shfl_up_sync(0xffffffffu, f.k1, off);
+        if (lane >= off) f = hvs_compose(o, f);
+    }
+    return f;
+}
+
+__device__ __forceinline__ HvsFn hvs_select(const HvsRec &r, uint32_t b) {
+    if (b == r.b) return {r.k.x, r.k.y};
+    if (b == r.b + 1u) return {r.k.z, r.k.w};
+    return {kHvsBad, kHvsBad};
+}
+
+// Apply the scanned transfers of a window to the state s (uniform across the
+// warp): the lanes below `valid` that keep s in its binade form a prefix; s
+// moves past them and their count is returned.
+__device__ __forceinline__ int hvs_take(HvsFn scanned, int valid, int lane, uint32_t &s) {
+    const uint32_t lim = (hvs_binade(s) + 1u) << 23;
+    const uint32_t w = (s & 1u) ? scanned.k1 : scanned.k0;
+    const bool ok = lane < valid && !(w & kHvsBad) && s + (w & kHvsKMask) <= lim;
+    const int took = __popc(__ballot_sync(0xffffffffu, ok));
+    if (took > 0) s += __shfl_sync(0xffffffffu, w & kHvsKMask, took - 1);
+    return took;
+}
+
+// The lane's kHvsLane terms starting at p, with `avail` of them inside the
+// plane; the rest read as +0, which adds nothing.
+__device__ __forceinline__ void hvs_load(const float *p, long long avail, bool vec,
+                                         float (&t)[kHvsLane]) {
+    if (vec && avail >= kHvsLane) {
+        const float4 *q = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+        for (int i = 0; i < kHvsLane / 4; i++) {
+            const float4 v = __ldg(q + i);
+            t[4 * i] = v.x;
+            t[4 * i + 1] = v.y;
+            t[4 * i + 2] = v.z;
+            t[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kHvsLane; i++) t[i] = i < avail ? __ldg(p + i) : 0.0f;
+    }
+}
+
+// A status word carries everything it means (state and value in one 64-bit
+// word, written and read whole), so relaxed accesses at GPU scope suffice.
+__device__ __forceinline__ void st_relaxed_u64(u64 *p, u64 v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ u64 ld_relaxed_u64(const u64 *p) {
+    u64 v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// Sum of the nodes before `node` of one plane (warp-wide; status = the
+// plane's status words, tag = the call's epoch in place).  Returns false if
+// it gave up waiting.
+__device__ __forceinline__ bool hvs_lookback(const u64 *status, int node, int lane, u64 tag,
+                                             float &excl) {
+    excl = 0.0f;
+    int j = node - 1;
+    const long long t0 = clock64();
+    while (j >= 0) {
+        const int idx = j - lane;
+        u64 w = 0;
+        unsigned pre = 0;
+        for (;;) {
+            if (idx >= 0 && (w >> 34) != (tag >> 34)) w = ld_relaxed_u64(status + idx);
+            const bool mine = idx >= 0 && (w >> 34) == (tag >> 34);
+            // needed: every lane up to the nearest published prefix (or all)
+            pre = __ballot_sync(0xffffffffu, mine && (w & (3ull << 32)) == kHvsPrefix);
+            const unsigned empty = __ballot_sync(0xffffffffu, idx >= 0 && !mine);
+            const unsigned need = pre ? ((pre & (0u - pre)) - 1u) : 0xffffffffu;
+            if ((empty & need) == 0) break;
+            if (clock64() - t0 > kHvsLookbackCycles) return false;
+            __nanosleep(32);
+        }
+        const int stop = pre ? __ffs(pre) - 1 : 32;
+        const float v = (idx >= 0 && lane <= stop) ? __uint_as_float((uint32_t)w) : 0.0f;
+        excl = __fadd_rn(excl, warp_sum_f(v));
+        if (pre) return true;
+        j -= 32;
+    }
+    return true;
+}
+
+// One CTA per node: loads the node's terms once, checks them, publishes the
+// node's sum, learns the sum before it, and writes the transfers of its
+// leaves and of itself for their candidate binades.  Launched as a
+// programmatic dependent of the kernel ahead (the previous call's walk): it
+// touches only this call's workspace, and reads the terms after that kernel
+// has finished unless they were ready before it started.
+__global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
+    extern __shared__ float4 s_terms[];  // kHvsLeaves leaves, kHvsLeafSlots each
+    __shared__ float s_leaf_sum[kHvsLeaves];
+    __shared__ float s_excl;
+    __shared__ unsigned s_flags;
+    __shared__ HvsRec s_leaf[kHvsLeaves];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (!a.terms_ready) grid_dependency_wait();
+    // CTAs start in block order, and blocks go round the planes (block t:
+    // plane t mod n_planes, node t / n_planes), so that a plane has few nodes
+    // in flight at a time and a look-back seldom needs more than one window.
+    // (Were the order ever different, only the guesses would suffer.)
+    const unsigned g = blockIdx.x;
+    const int plane = (int)(g % (unsigned)a.n_planes), node = (int)(g / (unsigned)a.n_planes);
+    const u64 tag = (u64)a.epoch << 34;
+    const float *pt = a.terms + (size_t)plane * (size_t)a.pitch;
+    const long long leaf = (long long)node * kHvsLeaves + warp;
+    const float *lb = pt + leaf * kHvsLeaf;
+    const long long avail = a.n_terms - leaf * kHvsLeaf;
+
+    // The leaf is read once, coalesced, into shared memory, with its sum (an
+    // estimate only) and the check of every term on the way.
+    float4 *sl = s_terms + (size_t)warp * kHvsLeafSlots;
+    float ls = 0.0f;
+    bool bad = false;
+    if (a.vec && avail >= kHvsLeaf) {
+#pragma unroll
+        for (int k = 0; k < kHvsLeafVecs / 32; k++) {
+            const int q = lane + 32 * k;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(lb) + q);
+            sl[q + (q >> 3)] = v;
+            ls = __fadd_rn(ls, __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)));
+            bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) | hvs_bad_term(v.w);
+        }
+    } else {
+        float *sf = reinterpret_cast<float *>(sl);
+        for (int k = 0; k < kHvsLeaf / 32; k++) {
+            const int i = lane + 32 * k;
+            const float v = i < avail ? __ldg(lb + i) : 0.0f;
+            const int q = i >> 2;
+            sf[4 * (q + (q >> 3)) + (i & 3)] = v;
+            ls = __fadd_rn(ls, v);
+            bad |= hvs_bad_term(v);
+        }
+    }
+    ls = warp_sum_f(ls);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) s_leaf_sum[warp] = ls;
+    if (threadIdx.x == 0) s_flags = 0u;
+    __syncthreads();
+    if (bad && lane == 0) atomicOr(&s_flags, kHvsFlagRange);
+
+    if (warp == 0) {
+        const float node_sum = warp_sum_f(lane < kHvsLeaves ? s_leaf_sum[lane] : 0.0f);
+        u64 *st = a.status + (size_t)plane * (size_t)a.n_nodes;
+        float excl = 0.0f;
+        if (node == 0) {
+            if (lane == 0) st_relaxed_u64(st, tag | kHvsPrefix | __float_as_uint(node_sum));
+        } else {
+            if (lane == 0) st_relaxed_u64(st + node, tag | kHvsAgg | __float_as_uint(node_sum));
+            const bool ok = hvs_lookback(st, node, lane, tag, excl);
+            if (lane == 0) {
+                if (!ok) atomicOr(&s_flags, kHvsFlagGuess);
+                st_relaxed_u64(st + node,
+                               tag | kHvsPrefix | __float_as_uint(__fadd_rn(excl, node_sum)));
+            }
+        }
+        if (lane == 0) s_excl = excl;
+    }
+    __syncthreads();
+
+    // Second pass: each lane's run of kHvsLane terms, for the two candidate
+    // binades of this leaf's estimate.
+    float lp = s_excl;
+    for (int j = 0; j < warp; j++) lp = __fadd_rn(lp, s_leaf_sum[j]);
+    const uint32_t bl = hvs_guess(lp);
+    HvsFn f0, f1;
+    hvs_run_fns2(sl + 9 * lane, bl, f0, f1);  // vectors 8 lane .. 8 lane + 7
+    f0 = hvs_reduce(f0);
+    f1 = hvs_reduce(f1);
+    if (lane == 0) {
+        HvsRec r;
+        r.k = make_uint4(f0.k0, f0.k1, f1.k0, f1.k1);
+        r.b = bl;
+        r.pad[0] = r.pad[1] = r.pad[2] = 0;
+        s_leaf[warp] = r;
+        if (leaf < a.n_leaves) a.leaves[(size_t)plane * (size_t)a.n_leaves + (size_t)leaf] = r;
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        const uint32_t bn = hvs_guess(s_excl);
+        const long long nl = (long long)a.n_leaves - (long long)node * kHvsLeaves;
+        const bool in = lane < kHvsLeaves && lane < nl;
+        const HvsFn g0 = hvs_reduce(in ? hvs_select(s_leaf[lane], bn) : hvs_identity());
+        const HvsFn g1 = hvs_reduce(in ? hvs_select(s_leaf[lane], bn + 1u) : hvs_identity());
+        if (lane == 0) {
+            HvsRec r;
+            r.k = make_uint4(g0.k0, g0.k1, g1.k0, g1.k1);
+            r.b = bn;
+            r.pad[0] = s_flags;
+            r.pad[1] = r.pad[2] = 0;
+            a.nodes[(size_t)plane * (size_t)a.n_nodes + (size_t)node] = r;
+        }
+    }
+}
+
+__device__ __forceinline__ HvsRec hvs_load_rec(const HvsRec *p) {
+    HvsRec r;
+    r.k = __ldcg(reinterpret_cast<const uint4 *>(p));
+    r.b = __ldcg(&p->b);
+    r.pad[0] = __ldcg(&p->pad[0]);
+    r.pad[1] = r.pad[2] = 0;
+    return r;
+}
+
+// One leaf, lane by lane, from state s.
+__device__ __forceinline__ void hvs_walk_leaf(const HvsArgs &a, const float *pt, long long leaf,
+                                              int lane, uint32_t &s, uint32_t &runs) {
+    const long long first = leaf * kHvsLeaf + (long long)lane * kHvsLane;
+    float t[kHvsLane];
+    hvs_load(pt + first, a.n_terms - first, a.vec != 0, t);
+    int start = 0;
+    while (start < 32) {
+        const HvsFn f = lane >= start ? hvs_run_fn(t, hvs_binade(s)) : hvs_identity();
+        const int took = hvs_take(hvs_scan(f, lane), 32, lane, s);
+        if (took >= 32) break;
+        // lane `took` leaves the binade: its terms one by one, as the CPU adds them
+        uint32_t ns = s;
+        if (lane == took) {
+            float x = __uint_as_float(s);
+#pragma unroll
+            for (int i = 0; i < kHvsLane; i++) x = __fadd_rn(x, t[i]);
+            ns = __float_as_uint(x);
+        }
+        s = __shfl_sync(0xffffffffu, ns, took);
+        runs++;
+        start = took + 1;
+    }
+}
+
+// One warp per plane: the walk over nodes, leaves and terms.  Writes the
+// plane's result (into host-mapped memory).  A node whose terms were not all
+// in [0, 2^95) ends the plane's walk before any of its terms are used: the
+// plane's sum is NaN and its flags say why.
+__global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
+    allow_dependent_launch();  // the next call's tables may start on free SMs
+    const int plane = blockIdx.x, lane = threadIdx.x;
+    HvsOut o;
+    o.flags = 0;
+    o.replayed_leaves = 0;
+    o.replayed_runs = 0;
+    const float *pt = a.terms + (size_t)plane * (size_t)a.pitch;
+    const HvsRec *nodes = a.nodes + (size_t)plane * (size_t)a.n_nodes;
+    const HvsRec *leaves = a.leaves + (size_t)plane * (size_t)a.n_leaves;
+    uint32_t s = 0u;  // the running sum, as float bits
+    int nd = 0;
+    while (nd < a.n_nodes) {
+        const int cnt = min(32, a.n_nodes - nd);
+        const uint32_t b = hvs_binade(s);
+        HvsFn f = hvs_identity();
+        uint32_t nf = 0;
+        if (lane < cnt) {
+            const HvsRec r = hvs_load_rec(nodes + nd + lane);
+            f = hvs_select(r, b);
+            nf = r.pad[0];
+        }
+        o.flags |= __reduce_or_sync(0xffffffffu, nf) & kHvsFlagGuess;
+        if (__any_sync(0xffffffffu, nf & kHvsFlagRange)) {
+            o.flags |= kHvsFlagRange;
+            break;
+        }
+        const int took = hvs_take(hvs_scan(f, lane), cnt, lane, s);
+        nd += took;
+        if (took == cnt) continue;
+        // node nd, leaf by leaf
+        const long long l0 = (long long)nd * kHvsLeaves;
+        const int nl = (int)min((long long)kHvsLeaves, (long long)a.n_leaves - l0);
+        int lf = 0;
+        while (lf < nl) {
+            const int c2 = nl - lf;
+            const uint32_t bb = hvs_binade(s);
+            const HvsFn g =
+                lane < c2 ? hvs_select(hvs_load_rec(leaves + l0 + lf + lane), bb) : hvs_identity();
+            lf += hvs_take(hvs_scan(g, lane), c2, lane, s);
+            if (lf < nl) {
+                hvs_walk_leaf(a, pt, l0 + lf, lane, s, o.replayed_runs);
+                o.replayed_leaves++;
+                lf++;
+            }
+        }
+        nd++;
+    }
+    if (lane == 0) {
+        o.sum_bits = (o.flags & kHvsFlagRange) ? 0x7FC00000u : s;
+        out[plane] = o;
+    }
+}
+
+}  // namespace vqx

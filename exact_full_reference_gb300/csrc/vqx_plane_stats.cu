@@ -18,12 +18,14 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "vqx.h"
 #include "vqx_kernels.cuh"
+#include "vqx_hvs.cuh"
 #include "vqx_ordered.cuh"
 
 namespace {
@@ -57,7 +59,7 @@ constexpr size_t kRowsMinBytes = 512;
 // What a call computes: the fused statistics, or the integer psnr.  Up to 12
 // bits the integer psnr's SSE is the fused pass's noise sum (its squares are
 // exact), so only 16 bits has a kernel variant of its own.
-enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2, kOrdered = 3 };
+enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2, kOrdered = 3, kHvs = 4 };
 constexpr int kVariants = 5;  // fused 8, 10, 12, 16 bits; integer psnr 16 bits
 
 int variant_index(int bpc, int kind) {  // kPlanes runs the fused statistics
@@ -179,6 +181,7 @@ struct DeviceCtx {
     int resident[kPaths][kVariants] = {};
     cudaMemPool_t pool = nullptr;
     cudaStream_t copy_stream = nullptr;
+    std::atomic<uint32_t> hvs_epoch{0};  // tags of the psnr_hvs look-back words
 };
 
 constexpr int kMaxDevices = 64;
@@ -188,6 +191,9 @@ cudaError_t init_device(DeviceCtx &c, int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if ((e = prepare_stage1(c.resident)) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(vqx::hvs_tables, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)vqx::kHvsTablesSmem);
+    if (e != cudaSuccess) return e;
     cudaMemPoolProps props;
     memset(&props, 0, sizeof props);
     props.allocType = cudaMemAllocationTypePinned;
@@ -278,7 +284,8 @@ struct vqx_pending {
     int n_frames = 0, bpc = 0, width = 0, height = 0;
     int n_planes = 1;                                    // kPlanes: the planes' sizes
     int pw[VQX_MAX_PLANES] = {}, ph[VQX_MAX_PLANES] = {};
-    void *ws = nullptr;  // kOrdered: the workspace, held until finished
+    long long n_terms = 0;  // kHvs: terms per plane (n_frames counts the planes)
+    void *ws = nullptr;     // kOrdered: the workspace, held until finished
 };
 
 namespace {
@@ -761,6 +768,26 @@ void vqx_profile_read(vqx_profile *out, int reset) {
 
 namespace {
 
+// The plane score of "ADR-1397: GPU psnr_hvs twins reproduce the CPU's
+// running float sum bit for bit" (Decision): the sum divided in float by the
+// term count, then by the float square of the largest sample (compiled with
+// contraction off; every operation is one IEEE single operation).
+void conclude_hvs(const vqx::HvsOut &w, int bpc, long long n_terms, vqx_hvs_plane *o) {
+    o->flags = w.flags & (VQX_FLAG_RANGE | VQX_FLAG_TIMEOUT);
+    o->replayed_leaves = w.replayed_leaves;
+    if (o->flags & VQX_FLAG_RANGE) {
+        o->sum = o->score = std::nanf("");
+        return;
+    }
+    float sum;
+    memcpy(&sum, &w.sum_bits, sizeof sum);
+    const float peak = (float)((1u << bpc) - 1u);
+    float q = sum / (float)n_terms;
+    q = q / (peak * peak);
+    o->sum = sum;
+    o->score = q;
+}
+
 int submit_impl(const void *ref, const void *dist, int width, int height, size_t stride, int bpc,
                 int n_frames, vqx_stream_t stream, int kind, unsigned flags, vqx_pending **pending) {
     if (flags & ~VQX_SUBMIT_PLANES_READY) return VQX_EINVAL;
@@ -829,7 +856,9 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
         t_prof.totals.calls++;
         t_prof.totals.kernel_launches += kind == kOrdered ? 4 : 2 * (uint64_t)p->n_planes;
         t_prof.totals.stage1_launches += (uint64_t)p->n_planes;
-        if (kind == kPlanes)
+        if (kind == kHvs)
+            t_prof.totals.stage1_bytes += 4ull * (uint64_t)p->n_terms * (uint64_t)p->n_frames;
+        else if (kind == kPlanes)
             for (int q = 0; q < p->n_planes; q++)
                 t_prof.totals.stage1_bytes += plane_bytes(p->pw[q], p->ph[q], p->bpc, p->n_frames);
         else
@@ -856,6 +885,13 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
                 vqx_frame_stats &r = ((vqx_frame_stats *)out)[f];
                 conclude(s_f, p->bpc, p->width, p->height, &r, o);
                 rc = merge_status(rc, r);
+            }
+        } else if (kind == kHvs) {
+            const vqx::HvsOut *w = (const vqx::HvsOut *)p->rec.host;
+            vqx_hvs_plane *o = (vqx_hvs_plane *)out;
+            for (int q = 0; q < p->n_frames; q++) {
+                conclude_hvs(w[q], p->bpc, p->n_terms, &o[q]);
+                rc = merge_status_flags(rc, o[q].flags);
             }
         } else if (kind == kStats) {
             rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
@@ -1320,4 +1356,124 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
         rc = merge_status(rc, out[f]);
     }
     return rc;
+}
+
+// ====================================================================== psnr_hvs plane sum
+namespace {
+
+int validate_hvs(const float *terms, int64_t n_terms, int64_t plane_pitch, int n_planes, int bpc) {
+    if (bpc != 8 && bpc != 10 && bpc != 12 && bpc != 16) return VQX_EBPC;
+    if (n_planes < 0) return VQX_EINVAL;
+    if (n_planes == 0) return VQX_OK;
+    if (!terms || ((uintptr_t)terms & 3u) != 0) return VQX_EINVAL;
+    if (n_terms < 1 || n_terms > 0x7FFFFFFFll || plane_pitch < n_terms) return VQX_EINVAL;
+    const long long nodes = (n_terms + vqx::kHvsNode - 1) / vqx::kHvsNode;
+    if ((long long)n_planes * nodes > 0x7FFFFFFFll) return VQX_EINVAL;
+    return VQX_OK;
+}
+
+}  // namespace
+
+extern "C" int vqx_psnr_hvs_sum_submit(const float *terms, int64_t n_terms, int64_t plane_pitch,
+                                       int n_planes, int bpc, vqx_stream_t stream, unsigned flags,
+                                       vqx_pending **pending) {
+    if (!pending) return VQX_EINVAL;
+    *pending = nullptr;
+    if (flags & ~VQX_SUBMIT_PLANES_READY) return VQX_EINVAL;
+    int rc = validate_hvs(terms, n_terms, plane_pitch, n_planes, bpc);
+    if (rc != VQX_OK || n_planes == 0) return rc;
+    DeviceCtx *ctx = nullptr;
+    if ((rc = device_ctx(&ctx)) != VQX_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    vqx::HvsArgs a;
+    a.terms = terms;
+    a.n_terms = n_terms;
+    a.pitch = plane_pitch;
+    a.n_planes = n_planes;
+    a.n_leaves = (int)((n_terms + vqx::kHvsLeaf - 1) / vqx::kHvsLeaf);
+    a.n_nodes = (a.n_leaves + vqx::kHvsLeaves - 1) / vqx::kHvsLeaves;
+    a.vec = ((uintptr_t)terms & 15u) == 0 && (plane_pitch & 3) == 0;
+    a.terms_ready = (flags & VQX_SUBMIT_PLANES_READY) ? 1 : 0;
+    uint32_t ep = 0;
+    while (ep == 0) ep = (ctx->hvs_epoch.fetch_add(1u) + 1u) & vqx::kHvsEpochMask;
+    a.epoch = ep;
+    const size_t recs = (size_t)n_planes * ((size_t)a.n_leaves + (size_t)a.n_nodes);
+    const size_t rec_b = recs * sizeof(vqx::HvsRec);
+    const size_t status_b = (size_t)n_planes * a.n_nodes * sizeof(u64);
+
+    vqx_pending *pd = nullptr;
+    if ((rc = acquire_pending(ctx, t_prof.on, &pd)) != VQX_OK) return rc;
+    if ((rc = acquire_pinned((size_t)n_planes * sizeof(vqx::HvsOut), &pd->rec)) != VQX_OK) {
+        release_pending(pd);
+        return rc;
+    }
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, rec_b + status_b, ctx->pool, st);
+    if (e != cudaSuccess) {
+        release_pinned(pd->rec);
+        release_pending(pd);
+        return cuda_status(e);
+    }
+    // records (16-byte aligned), then the look-back words; nothing needs
+    // clearing (the words carry this call's epoch)
+    a.leaves = (vqx::HvsRec *)ws;
+    a.nodes = a.leaves + (size_t)n_planes * a.n_leaves;
+    a.status = (u64 *)((unsigned char *)ws + rec_b);
+    // The tables are a programmatic dependent of the kernel ahead (the batch
+    // ahead's walk, when batches follow each other): they start while it
+    // runs and write only this call's workspace, which is held until finish
+    // so that no later call is given the same memory while this one may run.
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((size_t)n_planes * a.n_nodes));
+    cfg.blockDim = dim3(vqx::kHvsThreads);
+    cfg.dynamicSmemBytes = vqx::kHvsTablesSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (pd->timed) e = cudaEventRecord(pd->ev[0], st);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, vqx::hvs_tables, a);
+    if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[1], st);
+    if (e == cudaSuccess) {
+        vqx::hvs_walk<<<(unsigned)n_planes, 32, 0, st>>>(a, (vqx::HvsOut *)pd->rec.dev);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[2], st);
+    if (e == cudaSuccess) e = cudaEventRecord(pd->done, st);
+    if (e != cudaSuccess) {
+        cudaStreamSynchronize(st);  // whatever was enqueued finishes first
+        cudaFreeAsync(ws, st);
+        cudaStreamSynchronize(st);
+        release_pinned(pd->rec);
+        release_pending(pd);
+        return cuda_status(e);
+    }
+    pd->kind = kHvs;
+    pd->n_planes = 1;
+    pd->n_frames = n_planes;
+    pd->bpc = bpc;
+    pd->width = pd->height = 0;
+    pd->n_terms = n_terms;
+    pd->ws = ws;
+    *pending = pd;
+    return VQX_OK;
+}
+
+extern "C" int vqx_psnr_hvs_sum_finish(vqx_pending *pending, vqx_hvs_plane *out) {
+    return finish_impl(pending, kHvs, out);
+}
+
+extern "C" int vqx_psnr_hvs_sum(const float *terms, int64_t n_terms, int64_t plane_pitch,
+                                int n_planes, int bpc, vqx_stream_t stream, vqx_hvs_plane *out) {
+    int rc = validate_hvs(terms, n_terms, plane_pitch, n_planes, bpc);
+    if (rc != VQX_OK || n_planes == 0) return rc;
+    if (!out) return VQX_EINVAL;
+    vqx_pending *p = nullptr;
+    if ((rc = vqx_psnr_hvs_sum_submit(terms, n_terms, plane_pitch, n_planes, bpc, stream, 0u, &p)) !=
+        VQX_OK)
+        return rc;
+    return vqx_psnr_hvs_sum_finish(p, out);
 }

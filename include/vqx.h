@@ -43,6 +43,8 @@
  *                              also past 2^53 units
  *   vqx_plane_stats_noalloc    no allocation at call time (fixed scratch)
  *   vqx_plane_int_psnr (+ _submit / _finish)   the integer psnr
+ *   vqx_psnr_hvs_sum (+ _submit / _finish)     psnr_hvs plane sums of given
+ *                              terms, the CPU's sequential float sum
  *   vqx_psnr_cap, vqx_status_string, vqx_last_cuda_error,
  *   vqx_profile_enable / vqx_profile_read      helpers and counters
  */
@@ -357,6 +359,58 @@ void vqx_profile_read(vqx_profile *out, int reset);
 int vqx_plane_stats_noalloc(const void *ref, const void *dist, int width, int height,
                             size_t stride, int bpc, int n_frames, vqx_stream_t stream,
                             vqx_frame_stats *out);
+
+/*
+ * psnr_hvs plane sum ("ADR-1397: GPU psnr_hvs twins reproduce the CPU's
+ * running float sum bit for bit", Context and Decision).
+ *
+ * The CPU adds a plane's terms, the masked coefficient errors (64 per 8x8
+ * block, a block's values in row order, blocks in raster order), one after
+ * another into a single float that starts at zero, then divides that sum in
+ * float by the number of terms and then by the float square of the sample
+ * maximum 2^bpc - 1 (the plane score).  vqx_psnr_hvs_sum returns both, the
+ * sum equal bit for bit to that sequential float sum, computed on the device
+ * from transfer tables of runs of additions instead of a sequential pass.
+ * The terms are the input: their transform, CSF and masking are not part of
+ * this call.
+ *
+ * terms: device memory, float32; plane p's n_terms terms start
+ *   p * plane_pitch floats after `terms`.  4-byte aligned (a 16-byte aligned
+ *   base with plane_pitch a multiple of 4 is read with wider loads).  Read
+ *   only, not retained after the call.
+ * Every term must be a non-negative float below 2^95 (-0 counts as 0).  A
+ *   plane holding anything else (a negative value, NaN, infinity, 2^95 or
+ *   more) gets VQX_FLAG_RANGE and NaN sum and score; the call fills every
+ *   record and then returns VQX_ERANGE.
+ * n_terms: 1 .. 2^31 - 1; plane_pitch >= n_terms; n_planes >= 0 (0 does
+ *   nothing); bpc: 8, 10, 12 or 16 (the score's peak); n_planes times
+ *   ceil(n_terms / 8192) at most 2^31 - 1.
+ * out: host memory for n_planes records.  Synchronous, like
+ *   vqx_plane_stats.  The _submit / _finish pair splits it in two as
+ *   vqx_plane_stats_submit / _finish do, with the same rules; flags is 0 or
+ *   VQX_SUBMIT_PLANES_READY, which here means that the terms are ready (the
+ *   batch's first kernel is a programmatic dependent of the kernel ahead and
+ *   then reads the terms without waiting for it).  A submitted batch holds
+ *   its device workspace (about 1 % of its terms' size) until finished.
+ * Errors: VQX_EINVAL, VQX_EBPC, VQX_ERANGE, VQX_ENOMEM, VQX_ECUDA.
+ */
+typedef struct {
+    float sum;                /* the sequential float sum of the plane's terms */
+    float score;              /* (sum / n_terms) / peak^2, each step in float */
+    uint32_t flags;           /* VQX_FLAG_RANGE: a term outside [0, 2^95) */
+    uint32_t replayed_leaves; /* leaves of 1024 terms the device walked run by
+                                 run rather than from their tables (where the
+                                 sum crosses a power of two): diagnostic */
+} vqx_hvs_plane;
+
+int vqx_psnr_hvs_sum(const float *terms, int64_t n_terms, int64_t plane_pitch, int n_planes,
+                     int bpc, vqx_stream_t stream, vqx_hvs_plane *out);
+
+int vqx_psnr_hvs_sum_submit(const float *terms, int64_t n_terms, int64_t plane_pitch,
+                            int n_planes, int bpc, vqx_stream_t stream, unsigned flags,
+                            vqx_pending **pending);
+
+int vqx_psnr_hvs_sum_finish(vqx_pending *pending, vqx_hvs_plane *out);
 
 #ifdef __cplusplus
 }

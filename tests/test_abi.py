@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
               "vqx_planes_stats_submit", "vqx_planes_stats_finish",
               "vqx_plane_stats_ordered_submit", "vqx_plane_stats_ordered_finish",
               "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
-              "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read"):
+              "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read",
+              "vqx_psnr_hvs_sum", "vqx_psnr_hvs_sum_submit", "vqx_psnr_hvs_sum_finish"):
         assert n in names
 
 
@@ -178,3 +179,41 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(vqx, "_lib", None)
     with pytest.raises(ImportError):
         vqx.library()
+
+
+@pytest.mark.parametrize(
+    "args,status",
+    [
+        (dict(bpc=9), -2),
+        (dict(n_planes=-1), -1),
+        (dict(terms=0), -1),
+        (dict(terms=FAKE + 2), -1),  # not 4-byte aligned
+        (dict(n_terms=0), -1),
+        (dict(n_terms=1 << 31, pitch=1 << 31), -1),  # over 2^31 - 1 terms
+        (dict(pitch=999), -1),  # pitch below n_terms
+        (dict(n_planes=1 << 20, n_terms=(1 << 31) - 1, pitch=(1 << 31) - 1), -1),  # grid too large
+    ],
+)
+def test_hvs_argument_errors_need_no_gpu(lib, args, status):
+    a = dict(terms=FAKE, n_terms=1000, pitch=1000, n_planes=2, bpc=8)
+    a.update(args)
+    so = lib.library()
+    out = np.zeros(max(a["n_planes"], 1), lib.HVS_PLANE_DTYPE)
+    rc = so.vqx_psnr_hvs_sum(a["terms"], a["n_terms"], a["pitch"], a["n_planes"], a["bpc"], None,
+                             out.ctypes.data)
+    assert rc == status
+    h = ctypes.c_void_p(123)
+    rc = so.vqx_psnr_hvs_sum_submit(a["terms"], a["n_terms"], a["pitch"], a["n_planes"], a["bpc"],
+                                    None, 0, ctypes.byref(h))
+    assert rc == status and h.value is None
+
+
+def test_hvs_no_planes_and_flags_need_no_gpu(lib):
+    so = lib.library()
+    out = np.zeros(1, lib.HVS_PLANE_DTYPE)
+    assert so.vqx_psnr_hvs_sum(FAKE, 1000, 1000, 0, 8, None, out.ctypes.data) == 0
+    assert so.vqx_psnr_hvs_sum(FAKE, 1000, 1000, 0, 8, None, None) == 0
+    h = ctypes.c_void_p()
+    assert so.vqx_psnr_hvs_sum_submit(FAKE, 1000, 1000, 1, 8, None, 2, ctypes.byref(h)) == -1
+    assert so.vqx_psnr_hvs_sum_submit(FAKE, 1000, 1000, 1, 8, None, 0, None) == -1
+    assert so.vqx_psnr_hvs_sum_finish(None, out.ctypes.data) == 0
