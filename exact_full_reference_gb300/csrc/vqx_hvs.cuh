@@ -25,9 +25,10 @@
 //   addition rounds the same way.  A run that leaves the binade from there has
 //   no transfer for b.
 // - The binade a run starts in is guessed from the sum of the terms before it
-//   (the float sum stays within a few per cent of it), and every run keeps
-//   transfers for two candidate binades.  Runs are leaves of kHvsLeaf terms (a
-//   warp, kHvsLane per lane) and nodes of kHvsLeaves leaves (a CTA).
+//   (the float sum stays within a few per cent of it).  A node keeps
+//   transfers for two candidate binades, a leaf for one, or for two where its
+//   estimate lies close below a power of two.  Runs are leaves of kHvsLeaf
+//   terms (a warp, kHvsLane per lane) and nodes of kHvsLeaves leaves (a CTA).
 // - One warp per plane walks: windows of 32 nodes, composed by a warp scan and
 //   applied to the state; a node without a transfer for the state's binade, or
 //   one that would leave it, is walked leaf by leaf, and such a leaf lane by
@@ -66,12 +67,16 @@ constexpr int kHvsThreads = 32 * kHvsLeaves;
 constexpr int kHvsLeafVecs = kHvsLeaf / 4;
 constexpr int kHvsLeafSlots = kHvsLeafVecs + kHvsLeafVecs / 8;
 constexpr size_t kHvsTablesSmem = (size_t)kHvsLeaves * kHvsLeafSlots * sizeof(float4);
+// Windows of 32 node records the walk loads at once.
+constexpr int kHvsWalkWindows = 4;
 
-// A transfer word: K in bits 0-24 (at most 2^24), "no transfer" in bit 30,
-// the parity after the run in bit 31.
-constexpr uint32_t kHvsKMask = 0x01FFFFFFu;
-constexpr uint32_t kHvsBad = 0x40000000u;
-constexpr uint32_t kHvsPar = 0x80000000u;
+// A transfer word is K itself.  The parity after a run needs no bit of its
+// own: from a state of parity p the run ends at m + K, whose parity is that
+// of p + K.  K <= 2^24 is a transfer; kHvsBad (2^24 + 1) means "none".  The
+// sum of two words stays far below 2^32, so min(sum, kHvsBad) keeps "none"
+// absorbing under composition, and a state plus kHvsBad always lies above
+// the top of the state's binade, so hvs_take never applies it.
+constexpr uint32_t kHvsBad = (1u << 24) + 1u;
 // Terms must lie in [0, 2^95) (-0 allowed): then no plane of up to 2^31 terms
 // can reach 2^127, as the float sum is below twice the exact sum.
 constexpr uint32_t kHvsTermLimit = 0x6F000000u;
@@ -121,19 +126,21 @@ struct HvsOut {
     uint32_t replayed_runs;    // lane runs added term by term
 };
 
-__device__ __forceinline__ HvsFn hvs_identity() { return {0u, kHvsPar}; }
+__device__ __forceinline__ HvsFn hvs_identity() { return {0u, 0u}; }
 
-// Word of "a then b" for one input parity, given a's word.
-__device__ __forceinline__ uint32_t hvs_then(uint32_t ka, HvsFn b) {
-    if (ka & kHvsBad) return kHvsBad;
-    const uint32_t kb = (ka & kHvsPar) ? b.k1 : b.k0;
-    if (kb & kHvsBad) return kHvsBad;
-    const uint32_t k = (ka & kHvsKMask) + (kb & kHvsKMask);
-    return k > (1u << 24) ? kHvsBad : (k | (kb & kHvsPar));
+// "a then b": a.k0 starts from an even state and ends odd iff a.k0 is odd;
+// a.k1 starts odd and ends odd iff a.k1 is even.
+__device__ __forceinline__ HvsFn hvs_compose(HvsFn a, HvsFn b) {
+    const uint32_t n0 = (a.k0 & 1u) ? b.k1 : b.k0;
+    const uint32_t n1 = (a.k1 & 1u) ? b.k0 : b.k1;
+    return {min(a.k0 + n0, kHvsBad), min(a.k1 + n1, kHvsBad)};
 }
 
-__device__ __forceinline__ HvsFn hvs_compose(HvsFn a, HvsFn b) {
-    return {hvs_then(a.k0, b), hvs_then(a.k1, b)};
+// Word of a run that took the representative state s to e, lim being the
+// top of the binade: none if e left the binade (or, for terms outside the
+// domain, fell below s).
+__device__ __forceinline__ uint32_t hvs_word(uint32_t e, uint32_t s, uint32_t lim) {
+    return e <= lim ? min(e - s, kHvsBad) : kHvsBad;
 }
 
 // Binade of a state (float bits): 1 for zero and the subnormals.
@@ -141,7 +148,8 @@ __device__ __forceinline__ uint32_t hvs_binade(uint32_t s) { return max(s >> 23,
 
 // Lower candidate binade for a run whose preceding terms add up to about x:
 // the binade of x (1 - 1/64), so that a float sum up to 1.6 % below the
-// estimate, or up to twice as far above, still has a transfer.
+// estimate still has a transfer (and, with the next binade as the second
+// candidate, one up to twice as far above).
 __device__ __forceinline__ uint32_t hvs_guess(float x) {
     return hvs_binade(__float_as_uint(__fmul_rn(x, 0.984375f)));
 }
@@ -151,10 +159,16 @@ __device__ __forceinline__ bool hvs_bad_term(float t) {
     return u >= kHvsTermLimit && u != 0x80000000u;
 }
 
-// Transfer of adding t[0..kHvsLane) for binade b (1 <= b <= 253), found by
-// adding them from the two representative states.
+// Representative state of binade b (1 <= b <= 253) for parity 0: the
+// smallest even state, 2^23 in the significand (0 for b = 1).
+__device__ __forceinline__ uint32_t hvs_rep(uint32_t b) {
+    return ((b - 1u) << 23) + (b == 1u ? 0u : (1u << 23));
+}
+
+// Transfer of adding t[0..kHvsLane) for binade b, found by adding them from
+// the two representative states.
 __device__ __forceinline__ HvsFn hvs_run_fn(const float (&t)[kHvsLane], uint32_t b) {
-    const uint32_t s0 = ((b - 1u) << 23) + (b == 1u ? 0u : (1u << 23));
+    const uint32_t s0 = hvs_rep(b);
     float x0 = __uint_as_float(s0), x1 = __uint_as_float(s0 + 1u);
 #pragma unroll
     for (int i = 0; i < kHvsLane; i++) {
@@ -162,18 +176,34 @@ __device__ __forceinline__ HvsFn hvs_run_fn(const float (&t)[kHvsLane], uint32_t
         x1 = __fadd_rn(x1, t[i]);
     }
     const uint32_t lim = (b + 1u) << 23;
-    const uint32_t e0 = __float_as_uint(x0), e1 = __float_as_uint(x1);
-    HvsFn f;
-    f.k0 = e0 > lim ? kHvsBad : ((e0 - s0) | (e0 << 31));
-    f.k1 = e1 > lim ? kHvsBad : ((e1 - s0 - 1u) | (e1 << 31));
-    return f;
+    return {hvs_word(__float_as_uint(x0), s0, lim), hvs_word(__float_as_uint(x1), s0 + 1u, lim)};
 }
 
-// Transfers of adding a lane's run (its 8 vectors at run[0..8) of a leaf in
-// shared memory) for binades b and b + 1.
+// The same for a lane's run held in shared memory (its 8 vectors at
+// run[0..8) of a padded leaf).
+__device__ __forceinline__ HvsFn hvs_run_fn_smem(const float4 *run, uint32_t b) {
+    const uint32_t s0 = hvs_rep(b);
+    float x0 = __uint_as_float(s0), x1 = __uint_as_float(s0 + 1u);
+#pragma unroll
+    for (int i = 0; i < kHvsLane / 4; i++) {
+        const float4 v = run[i];
+        x0 = __fadd_rn(x0, v.x);
+        x1 = __fadd_rn(x1, v.x);
+        x0 = __fadd_rn(x0, v.y);
+        x1 = __fadd_rn(x1, v.y);
+        x0 = __fadd_rn(x0, v.z);
+        x1 = __fadd_rn(x1, v.z);
+        x0 = __fadd_rn(x0, v.w);
+        x1 = __fadd_rn(x1, v.w);
+    }
+    const uint32_t lim = (b + 1u) << 23;
+    return {hvs_word(__float_as_uint(x0), s0, lim), hvs_word(__float_as_uint(x1), s0 + 1u, lim)};
+}
+
+// Transfers of a lane's run in shared memory for binades b and b + 1.
 __device__ __forceinline__ void hvs_run_fns2(const float4 *run, uint32_t b, HvsFn &fb, HvsFn &fb1) {
-    const uint32_t s0 = ((b - 1u) << 23) + (b == 1u ? 0u : (1u << 23));
-    const uint32_t u0 = (b << 23) + (1u << 23);  // binade b + 1 (never 1)
+    const uint32_t s0 = hvs_rep(b);
+    const uint32_t u0 = hvs_rep(b + 1u);
     float x0 = __uint_as_float(s0), x1 = __uint_as_float(s0 + 1u);
     float y0 = __uint_as_float(u0), y1 = __uint_as_float(u0 + 1u);
 #pragma unroll
@@ -189,18 +219,16 @@ __device__ __forceinline__ void hvs_run_fns2(const float4 *run, uint32_t b, HvsF
         }
     }
     const uint32_t lim = (b + 1u) << 23, lim1 = (b + 2u) << 23;
-    const uint32_t e0 = __float_as_uint(x0), e1 = __float_as_uint(x1);
-    const uint32_t g0 = __float_as_uint(y0), g1 = __float_as_uint(y1);
-    fb.k0 = e0 > lim ? kHvsBad : ((e0 - s0) | (e0 << 31));
-    fb.k1 = e1 > lim ? kHvsBad : ((e1 - s0 - 1u) | (e1 << 31));
-    fb1.k0 = g0 > lim1 ? kHvsBad : ((g0 - u0) | (g0 << 31));
-    fb1.k1 = g1 > lim1 ? kHvsBad : ((g1 - u0 - 1u) | (g1 << 31));
+    fb = {hvs_word(__float_as_uint(x0), s0, lim), hvs_word(__float_as_uint(x1), s0 + 1u, lim)};
+    fb1 = {hvs_word(__float_as_uint(y0), u0, lim1), hvs_word(__float_as_uint(y1), u0 + 1u, lim1)};
 }
 
-// Ordered reduction: lane 0 gets lanes 0..31 composed in lane order.
+// Ordered reduction: lane 0 gets lanes 0..kLanes-1 composed in lane order
+// (kLanes a power of two; the other lanes' values are not used).
+template <int kLanes = 32>
 __device__ __forceinline__ HvsFn hvs_reduce(HvsFn f) {
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
+    for (int off = 1; off < kLanes; off <<= 1) {
         HvsFn o;
         o.k0 = __shfl_down_sync(0xffffffffu, f.k0, off);
         o.k1 = __shfl_down_sync(0xffffffffu, f.k1, off);
@@ -233,9 +261,9 @@ __device__ __forceinline__ HvsFn hvs_select(const HvsRec &r, uint32_t b) {
 __device__ __forceinline__ int hvs_take(HvsFn scanned, int valid, int lane, uint32_t &s) {
     const uint32_t lim = (hvs_binade(s) + 1u) << 23;
     const uint32_t w = (s & 1u) ? scanned.k1 : scanned.k0;
-    const bool ok = lane < valid && !(w & kHvsBad) && s + (w & kHvsKMask) <= lim;
+    const bool ok = lane < valid && s + w <= lim;
     const int took = __popc(__ballot_sync(0xffffffffu, ok));
-    if (took > 0) s += __shfl_sync(0xffffffffu, w & kHvsKMask, took - 1);
+    if (took > 0) s += __shfl_sync(0xffffffffu, w, took - 1);
     return took;
 }
 
@@ -335,20 +363,43 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
     const long long avail = a.n_terms - leaf * kHvsLeaf;
 
     // The leaf is read once, coalesced, into shared memory, with its sum (an
-    // estimate only) and the check of every term on the way.
+    // estimate only, in two packed float pairs) and the largest term bits on
+    // the way.  Every term in the domain has bits below kHvsTermLimit except
+    // -0; a larger maximum (a term outside the domain, or a -0) sends the
+    // lane to the exact check of its terms.
     float4 *sl = s_terms + (size_t)warp * kHvsLeafSlots;
-    float ls = 0.0f;
+    float ls;
     bool bad = false;
     if (a.vec && avail >= kHvsLeaf) {
+        f32x2 acc_a = 0ull, acc_b = 0ull;
+        uint32_t mx = 0u;
 #pragma unroll
         for (int k = 0; k < kHvsLeafVecs / 32; k++) {
             const int q = lane + 32 * k;
             const float4 v = __ldg(reinterpret_cast<const float4 *>(lb) + q);
             sl[q + (q >> 3)] = v;
-            ls = __fadd_rn(ls, __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w)));
-            bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) | hvs_bad_term(v.w);
+            const uint32_t ux = __float_as_uint(v.x), uy = __float_as_uint(v.y);
+            const uint32_t uz = __float_as_uint(v.z), uw = __float_as_uint(v.w);
+            acc_a = f2_add(acc_a, f2_pack(ux, uy));
+            acc_b = f2_add(acc_b, f2_pack(uz, uw));
+            mx = max(mx, max(max(ux, uy), max(uz, uw)));
+        }
+        uint32_t a0, a1, b0, b1;
+        f2_unpack(acc_a, a0, a1);
+        f2_unpack(acc_b, b0, b1);
+        ls = __fadd_rn(__fadd_rn(__uint_as_float(a0), __uint_as_float(a1)),
+                       __fadd_rn(__uint_as_float(b0), __uint_as_float(b1)));
+        if (mx >= kHvsTermLimit) {
+#pragma unroll 1
+            for (int k = 0; k < kHvsLeafVecs / 32; k++) {
+                const int q = lane + 32 * k;
+                const float4 v = sl[q + (q >> 3)];
+                bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) |
+                       hvs_bad_term(v.w);
+            }
         }
     } else {
+        ls = 0.0f;
         float *sf = reinterpret_cast<float *>(sl);
         for (int k = 0; k < kHvsLeaf / 32; k++) {
             const int i = lane + 32 * k;
@@ -385,15 +436,24 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
     }
     __syncthreads();
 
-    // Second pass: each lane's run of kHvsLane terms, for the two candidate
-    // binades of this leaf's estimate.
+    // Second pass: each lane's run of kHvsLane terms, for the binade of this
+    // leaf's estimate and, where the estimate lies within 1/16 of the top of
+    // that binade, for the next one as well (a float sum running that far
+    // ahead of its estimate is only walked more slowly, never wrongly).
     float lp = s_excl;
     for (int j = 0; j < warp; j++) lp = __fadd_rn(lp, s_leaf_sum[j]);
     const uint32_t bl = hvs_guess(lp);
+    const bool two = hvs_binade(__float_as_uint(__fmul_rn(lp, 1.0625f))) != bl;  // warp-uniform
+    const float4 *run = sl + 9 * lane;  // vectors 8 lane .. 8 lane + 7
     HvsFn f0, f1;
-    hvs_run_fns2(sl + 9 * lane, bl, f0, f1);  // vectors 8 lane .. 8 lane + 7
-    f0 = hvs_reduce(f0);
-    f1 = hvs_reduce(f1);
+    if (two) {
+        hvs_run_fns2(run, bl, f0, f1);
+        f0 = hvs_reduce(f0);
+        f1 = hvs_reduce(f1);
+    } else {
+        f0 = hvs_reduce(hvs_run_fn_smem(run, bl));
+        f1 = {kHvsBad, kHvsBad};
+    }
     if (lane == 0) {
         HvsRec r;
         r.k = make_uint4(f0.k0, f0.k1, f1.k0, f1.k1);
@@ -408,8 +468,10 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
         const uint32_t bn = hvs_guess(s_excl);
         const long long nl = (long long)a.n_leaves - (long long)node * kHvsLeaves;
         const bool in = lane < kHvsLeaves && lane < nl;
-        const HvsFn g0 = hvs_reduce(in ? hvs_select(s_leaf[lane], bn) : hvs_identity());
-        const HvsFn g1 = hvs_reduce(in ? hvs_select(s_leaf[lane], bn + 1u) : hvs_identity());
+        const HvsFn g0 = hvs_reduce<kHvsLeaves>(in ? hvs_select(s_leaf[lane & (kHvsLeaves - 1)], bn)
+                                                   : hvs_identity());
+        const HvsFn g1 = hvs_reduce<kHvsLeaves>(
+            in ? hvs_select(s_leaf[lane & (kHvsLeaves - 1)], bn + 1u) : hvs_identity());
         if (lane == 0) {
             HvsRec r;
             r.k = make_uint4(g0.k0, g0.k1, g1.k0, g1.k1);
@@ -471,24 +533,42 @@ __global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
     const HvsRec *leaves = a.leaves + (size_t)plane * (size_t)a.n_leaves;
     uint32_t s = 0u;  // the running sum, as float bits
     int nd = 0;
-    while (nd < a.n_nodes) {
-        const int cnt = min(32, a.n_nodes - nd);
-        const uint32_t b = hvs_binade(s);
-        HvsFn f = hvs_identity();
-        uint32_t nf = 0;
-        if (lane < cnt) {
-            const HvsRec r = hvs_load_rec(nodes + nd + lane);
-            f = hvs_select(r, b);
-            nf = r.pad[0];
+    bool range = false;
+    while (nd < a.n_nodes && !range) {
+        // The records of the next kHvsWalkWindows windows of 32 nodes, loaded
+        // together (the selection waits for the state; the loads need not).
+        HvsRec r[kHvsWalkWindows];
+#pragma unroll
+        for (int j = 0; j < kHvsWalkWindows; j++) {
+            const int i = nd + 32 * j + lane;
+            if (i < a.n_nodes) r[j] = hvs_load_rec(nodes + i);
         }
-        o.flags |= __reduce_or_sync(0xffffffffu, nf) & kHvsFlagGuess;
-        if (__any_sync(0xffffffffu, nf & kHvsFlagRange)) {
-            o.flags |= kHvsFlagRange;
-            break;
+        bool partial = false;
+#pragma unroll
+        for (int j = 0; j < kHvsWalkWindows; j++) {
+            const int cnt = min(32, a.n_nodes - nd);  // window j starts at node nd
+            if (cnt <= 0) break;
+            const uint32_t b = hvs_binade(s);
+            HvsFn f = hvs_identity();
+            uint32_t nf = 0;
+            if (lane < cnt) {
+                f = hvs_select(r[j], b);
+                nf = r[j].pad[0];
+            }
+            o.flags |= __reduce_or_sync(0xffffffffu, nf) & kHvsFlagGuess;
+            if (__any_sync(0xffffffffu, nf & kHvsFlagRange)) {
+                o.flags |= kHvsFlagRange;
+                range = true;
+                break;
+            }
+            const int took = hvs_take(hvs_scan(f, lane), cnt, lane, s);
+            nd += took;
+            if (took < cnt) {
+                partial = true;
+                break;
+            }
         }
-        const int took = hvs_take(hvs_scan(f, lane), cnt, lane, s);
-        nd += took;
-        if (took == cnt) continue;
+        if (range || !partial) continue;
         // node nd, leaf by leaf
         const long long l0 = (long long)nd * kHvsLeaves;
         const int nl = (int)min((long long)kHvsLeaves, (long long)a.n_leaves - l0);
