@@ -83,6 +83,7 @@ constexpr uint32_t kHvsTermLimit = 0x6F000000u;
 
 // Flags of a node record (the walk reports the range flag for the plane).
 constexpr uint32_t kHvsFlagRange = 1u;
+constexpr uint32_t kHvsFlagTimeout = 2u;  // a bounded wait gave up: no result
 constexpr uint32_t kHvsFlagGuess = 4u;  // a look-back gave up (guesses only)
 
 // Look-back status words: the call's epoch in bits 34-63, the state in bits
@@ -483,6 +484,333 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- persistent form
+// hvs_tables_tma: the same tables for planes whose terms are 16-byte aligned
+// with a pitch of whole vectors (at least 32 terms), as a persistent
+// pipeline.  CTA c takes nodes g = c, c + gridDim.x, ... (g in the launch
+// order of hvs_tables: plane g mod n_planes, node g / n_planes).
+// - A producer lane streams each node (256 rows of 32 terms, one box of a
+//   tensor map over full rows, zero-filled past a plane's last full row)
+//   into a ring of kHvsTmaStages shared-memory buffers, 128-byte swizzled:
+//   chunk c (16 bytes) of row r lies at chunk c ^ (r mod 8), so a lane
+//   reading its own row (its run) and eight lanes reading eight rows hit
+//   eight different bank groups.
+// - Summer warp w sums leaf w (rows 32 w .. 32 w + 31) of every node as soon
+//   as it lands (any order) and checks its terms; the last of the eight adds
+//   the leaf sums and publishes the node's sum at once (its status word).
+// - kHvsTmaLookback look-back warps take nodes in turn: the look-back of
+//   hvs_tables, giving the prefix estimate of the node.
+// - Table warp w then tabulates each lane's run of leaf w in order and
+//   writes the leaf's record.
+// - The node's look-back warp, once the eight leaf records are in, composes
+//   the node's record and releases the buffer (all eight table warps do the
+//   same work, so none falls behind the others and holds the ring).
+// The summers run up to kHvsTmaStages nodes ahead of the table warps, so the
+// look-back's latency hides behind the ring instead of stalling it.
+// Terms of a plane's last, partial row (fewer than 32) are not in any box:
+// the lane whose run they are reads them itself.
+// Stage k of a CTA uses buffer k mod kHvsTmaStages; each of its mbarriers
+// (full: bytes landed; sums: the eight leaf sums written; excl: the prefix
+// estimate written; empty: the eight warps done with the buffer) completes
+// one phase per use, parity (k / kHvsTmaStages) & 1.  Every wait is
+// bounded; a warp whose wait gives up waits for nothing more, and every node
+// record written after it carries kHvsFlagTimeout.
+constexpr int kHvsTmaStages = 6;
+constexpr int kHvsTmaLookback = 4;
+constexpr int kHvsTmaSummers = kHvsLeaves;       // warps kHvsLeaves .. 2 kHvsLeaves - 1
+constexpr int kHvsTmaProducer = 2 * kHvsLeaves;  // warp index
+constexpr int kHvsTmaThreads = (2 * kHvsLeaves + 1 + kHvsTmaLookback) * 32;
+static_assert(kHvsTmaLookback <= kHvsTmaStages, "a look-back warp's previous node bounds its wait");
+constexpr uint32_t kHvsNodeBytes = kHvsNode * 4;
+constexpr int kHvsNodeRows = kHvsNode / 32;
+constexpr size_t kHvsTmaSmem = (size_t)kHvsTmaStages * kHvsNodeBytes + 1024;  // + alignment
+
+struct HvsTmaArgs {
+    long long rows_full;  // full rows of 32 terms per plane
+    int tail;             // terms in the partial row (0 .. 31)
+};
+
+// A wait that sleeps: try_wait with a suspend-time hint lets the thread be
+// suspended until the phase completes (or the hint runs out) instead of
+// polling, so the warps that wait (for data, for a prefix, for a free
+// buffer) leave the issue slots to the warps that compute.  Bounded like
+// mbar_wait: false after `limit` SM clock cycles.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                long long limit = kWaitCycles) {
+    const long long t0 = clock64();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000000u)
+            : "memory");
+        if (ok) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+}
+
+__global__ void __launch_bounds__(kHvsTmaThreads, 1)
+    hvs_tables_tma(const __grid_constant__ CUtensorMap tm, HvsArgs a, HvsTmaArgs t) {
+    constexpr int S = kHvsTmaStages;
+    extern __shared__ unsigned char hvs_raw[];
+    __shared__ __align__(8) u64 full[S], empty[S], sums[S], exclb[S], leafb[S];
+    __shared__ float s_leaf_sum[S][kHvsLeaves];
+    __shared__ float s_excl[S];
+    __shared__ unsigned s_flags[S], s_summed[S];
+    __shared__ float s_node_sum[S];
+    __shared__ unsigned s_err;
+    __shared__ HvsRec s_leaf[S][kHvsLeaves];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring0 = (smem_u32(hvs_raw) + 1023u) & ~1023u;
+    unsigned char *ring = hvs_raw + (ring0 - smem_u32(hvs_raw));
+    const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+    const uint32_t sums0 = smem_u32(sums), excl0 = smem_u32(exclb), leaf0 = smem_u32(leafb);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+            mbar_init(sums0 + 8 * i, kHvsLeaves);
+            mbar_init(excl0 + 8 * i, 1);
+            mbar_init(leaf0 + 8 * i, kHvsLeaves);
+            s_flags[i] = 0u;
+            s_summed[i] = 0u;
+        }
+        s_err = 0u;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const long long total = (long long)a.n_planes * a.n_nodes;
+    const int nk = total > (long long)blockIdx.x
+                       ? (int)((total - 1 - (long long)blockIdx.x) / gridDim.x + 1)
+                       : 0;
+    const u64 tag = (u64)a.epoch << 34;
+
+    if (warp == kHvsTmaProducer) {
+        if (lane != 0) return;
+        if (!a.terms_ready) grid_dependency_wait();
+        int k = 0;
+        for (; k < nk; k++) {
+            const int st = k % S;
+            if (k >= S && !mbar_wait_sleep(empty0 + 8 * st, ((k / S) - 1) & 1)) {
+                s_err = 1u;
+                break;
+            }
+            const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
+            const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
+            mbar_arrive_expect_tx(full0 + 8 * st, kHvsNodeBytes);
+            tensor_g2s_3d(ring0 + (uint32_t)st * kHvsNodeBytes, &tm, 0, node * kHvsNodeRows, plane,
+                          full0 + 8 * st);
+        }
+        // the copies in flight land before the CTA (and its shared memory) ends
+        for (int q = k > S ? k - S : 0; q < k; q++) mbar_wait_sleep(full0 + 8 * (q % S), (q / S) & 1);
+        return;
+    }
+
+    if (warp > kHvsTmaProducer) {
+        bool err = false;
+        for (int k = warp - kHvsTmaProducer - 1; k < nk; k += kHvsTmaLookback) {
+            const int st = k % S;
+            const uint32_t par = (k / S) & 1;
+            if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(sums0 + 8 * st, par))) {
+                err = true;
+                if (lane == 0) s_err = 1u;
+            }
+            const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
+            const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
+            float excl = 0.0f;
+            if (!err && node > 0) {
+                // the node's sum is published already (by the consumers)
+                const float node_sum = s_node_sum[st];
+                u64 *stw = a.status + (size_t)plane * (size_t)a.n_nodes;
+                {
+                    const bool ok = hvs_lookback(stw, node, lane, tag, excl);
+                    if (lane == 0) {
+                        if (!ok) atomicOr(&s_flags[st], kHvsFlagGuess);
+                        st_relaxed_u64(stw + node,
+                                       tag | kHvsPrefix | __float_as_uint(__fadd_rn(excl, node_sum)));
+                    }
+                }
+            }
+            if (lane == 0) {
+                s_excl[st] = excl;
+                mbar_arrive(excl0 + 8 * st);
+            }
+            // the node's record, from its eight leaf records; then the buffer
+            // is free (every table warp arrived on leafb after its last read)
+            if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(leaf0 + 8 * st, par))) {
+                err = true;
+                if (lane == 0) s_err = 1u;
+            }
+            const uint32_t bn = hvs_guess(excl);
+            const long long nl = (long long)a.n_leaves - (long long)node * kHvsLeaves;
+            const bool in = lane < kHvsLeaves && lane < nl;
+            const HvsRec lr = s_leaf[st][lane & (kHvsLeaves - 1)];
+            const HvsFn g0 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn) : hvs_identity());
+            const HvsFn g1 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn + 1u) : hvs_identity());
+            if (lane == 0) {
+                HvsRec r;
+                r.k = make_uint4(g0.k0, g0.k1, g1.k0, g1.k1);
+                r.b = bn;
+                r.pad[0] = s_flags[st] | ((err || s_err) ? kHvsFlagTimeout : 0u);
+                r.pad[1] = r.pad[2] = 0;
+                a.nodes[(size_t)plane * (size_t)a.n_nodes + (size_t)node] = r;
+                s_flags[st] = 0u;
+                mbar_arrive(empty0 + 8 * st);
+            }
+        }
+        return;
+    }
+
+    // summers (warps kHvsLeaves ..) and table warps (0 ..): leaf = warp mod 8
+    const bool summer = warp >= kHvsTmaSummers;
+    const int lw = summer ? warp - kHvsTmaSummers : warp;
+    bool err = false;
+    const float *const planes = a.terms;
+    auto pass1 = [&](int k) {
+        const int st = k % S;
+        if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(full0 + 8 * st, (k / S) & 1))) {
+            err = true;
+            if (lane == 0) s_err = 1u;
+        }
+        const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
+        const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
+        float ls = 0.0f;
+        bool bad = false;
+        if (!err) {
+            const float4 *lf = reinterpret_cast<const float4 *>(ring + (size_t)st * kHvsNodeBytes +
+                                                                (size_t)lw * kHvsLeaf * 4);
+            f32x2 acc_a = 0ull, acc_b = 0ull;
+            uint32_t mx = 0u;
+#pragma unroll
+            for (int i = 0; i < kHvsLeafVecs / 32; i++) {
+                const float4 v = lf[lane + 32 * i];
+                const uint32_t ux = __float_as_uint(v.x), uy = __float_as_uint(v.y);
+                const uint32_t uz = __float_as_uint(v.z), uw = __float_as_uint(v.w);
+                acc_a = f2_add(acc_a, f2_pack(ux, uy));
+                acc_b = f2_add(acc_b, f2_pack(uz, uw));
+                mx = __vimax3_u32(mx, ux, uy);
+                mx = __vimax3_u32(mx, uz, uw);
+            }
+            uint32_t a0, a1, b0, b1;
+            f2_unpack(acc_a, a0, a1);
+            f2_unpack(acc_b, b0, b1);
+            ls = __fadd_rn(__fadd_rn(__uint_as_float(a0), __uint_as_float(a1)),
+                           __fadd_rn(__uint_as_float(b0), __uint_as_float(b1)));
+            if (mx >= kHvsTermLimit) {
+#pragma unroll 1
+                for (int i = 0; i < kHvsLeafVecs / 32; i++) {
+                    const float4 v = lf[lane + 32 * i];
+                    bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) |
+                           hvs_bad_term(v.w);
+                }
+            }
+            // the partial row, if it is one of this leaf's rows
+            const long long row0 = (long long)node * kHvsNodeRows + (long long)lw * 32;
+            if (t.tail && t.rows_full >= row0 && t.rows_full < row0 + 32 && lane < t.tail) {
+                const float v = __ldg(planes + (size_t)plane * (size_t)a.pitch +
+                                      (size_t)t.rows_full * 32 + lane);
+                ls = __fadd_rn(ls, v);
+                bad |= hvs_bad_term(v);
+            }
+        }
+        ls = warp_sum_f(ls);
+        bad = __any_sync(0xffffffffu, bad);
+        unsigned last = 0u;
+        if (lane == 0) {
+            s_leaf_sum[st][lw] = ls;
+            if (bad) atomicOr(&s_flags[st], kHvsFlagRange);
+            __threadfence_block();
+            last = atomicAdd(&s_summed[st], 1u) == kHvsLeaves - 1 ? 1u : 0u;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            // the last warp: node sum, published as this node's aggregate
+            // (the inclusive prefix for a plane's first node)
+            __threadfence_block();
+            const float node_sum = warp_sum_f(lane < kHvsLeaves ? s_leaf_sum[st][lane] : 0.0f);
+            if (lane == 0) {
+                s_node_sum[st] = node_sum;
+                s_summed[st] = 0u;
+                if (!err) {
+                    u64 *stw = a.status + (size_t)plane * (size_t)a.n_nodes + node;
+                    st_relaxed_u64(stw, tag | (node == 0 ? kHvsPrefix : kHvsAgg) |
+                                            __float_as_uint(node_sum));
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sums0 + 8 * st);
+    };
+
+    auto pass2 = [&](int k) {
+        const int st = k % S;
+        if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(full0 + 8 * st, (k / S) & 1) &&
+                                                 mbar_wait_sleep(excl0 + 8 * st, (k / S) & 1))) {
+            err = true;
+            if (lane == 0) s_err = 1u;
+        }
+        const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
+        const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
+        const long long leaf = (long long)node * kHvsLeaves + lw;
+        HvsFn f0 = {kHvsBad, kHvsBad}, f1 = {kHvsBad, kHvsBad};
+        uint32_t bl = 1u;
+        if (!err) {
+            float lp = s_excl[st];
+            for (int j = 0; j < lw; j++) lp = __fadd_rn(lp, s_leaf_sum[st][j]);
+            bl = hvs_guess(lp);
+            const bool two = hvs_binade(__float_as_uint(__fmul_rn(lp, 1.0625f))) != bl;
+            const long long row = (long long)node * kHvsNodeRows + (long long)lw * 32 + lane;
+            float tv[kHvsLane];
+            if (row == t.rows_full && t.tail) {
+                // the partial row: its terms from the plane, zeros past its end
+                const float *src = planes + (size_t)plane * (size_t)a.pitch + (size_t)row * 32;
+#pragma unroll
+                for (int i = 0; i < kHvsLane; i++) tv[i] = i < t.tail ? __ldg(src + i) : 0.0f;
+            } else {
+                const float4 *rw = reinterpret_cast<const float4 *>(
+                    ring + (size_t)st * kHvsNodeBytes + (size_t)(lw * 32 + lane) * 128);
+                const int sw = lane & 7;
+#pragma unroll
+                for (int c = 0; c < kHvsLane / 4; c++) {
+                    const float4 v = rw[c ^ sw];
+                    tv[4 * c] = v.x;
+                    tv[4 * c + 1] = v.y;
+                    tv[4 * c + 2] = v.z;
+                    tv[4 * c + 3] = v.w;
+                }
+            }
+            if (two) {
+                f0 = hvs_reduce(hvs_run_fn(tv, bl));
+                f1 = hvs_reduce(hvs_run_fn(tv, bl + 1u));
+            } else {
+                f0 = hvs_reduce(hvs_run_fn(tv, bl));
+            }
+        }
+        if (lane == 0) {
+            HvsRec r;
+            r.k = make_uint4(f0.k0, f0.k1, f1.k0, f1.k1);
+            r.b = bl;
+            r.pad[0] = r.pad[1] = r.pad[2] = 0;
+            s_leaf[st][lw] = r;
+            if (leaf < a.n_leaves) a.leaves[(size_t)plane * (size_t)a.n_leaves + (size_t)leaf] = r;
+            if (err) s_err = 1u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(leaf0 + 8 * st);
+    };
+
+    if (summer) {
+        for (int k = 0; k < nk; k++) pass1(k);
+    } else {
+        for (int k = 0; k < nk; k++) pass2(k);
+    }
+}
+
 __device__ __forceinline__ HvsRec hvs_load_rec(const HvsRec *p) {
     HvsRec r;
     r.k = __ldcg(reinterpret_cast<const uint4 *>(p));
@@ -556,8 +884,8 @@ __global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
                 nf = r[j].pad[0];
             }
             o.flags |= __reduce_or_sync(0xffffffffu, nf) & kHvsFlagGuess;
-            if (__any_sync(0xffffffffu, nf & kHvsFlagRange)) {
-                o.flags |= kHvsFlagRange;
+            if (__any_sync(0xffffffffu, nf & (kHvsFlagRange | kHvsFlagTimeout))) {
+                o.flags |= __reduce_or_sync(0xffffffffu, nf) & (kHvsFlagRange | kHvsFlagTimeout);
                 range = true;
                 break;
             }
@@ -588,7 +916,7 @@ __global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
         nd++;
     }
     if (lane == 0) {
-        o.sum_bits = (o.flags & kHvsFlagRange) ? 0x7FC00000u : s;
+        o.sum_bits = (o.flags & (kHvsFlagRange | kHvsFlagTimeout)) ? 0x7FC00000u : s;
         out[plane] = o;
     }
 }

@@ -140,6 +140,25 @@ cudaError_t encode_planes(CUtensorMap *tm, const void *base, int elem_bytes, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// psnr_hvs terms as a 32 x rows x planes tensor of floats (rows of 128
+// bytes, planes pitch floats apart), read in 32 x 256 x 1 boxes with the
+// 128-byte swizzle.  Only full rows are in the tensor.
+cudaError_t encode_hvs(CUtensorMap *tm, const float *terms, long long rows, long long pitch,
+                       int planes) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    cudaError_t e = encode_fn(&enc);
+    if (e != cudaSuccess) return e;
+    const cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)pitch * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)vqx::kHvsNodeRows, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(terms), dims,
+                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 Stage1Shape stage1_shape(int path, int variant) {
     switch (variant) {
     case 0: return stage1_shape<8, vqx::TermSums<8>>(path);
@@ -182,6 +201,7 @@ struct DeviceCtx {
     cudaMemPool_t pool = nullptr;
     cudaStream_t copy_stream = nullptr;
     std::atomic<uint32_t> hvs_epoch{0};  // tags of the psnr_hvs look-back words
+    int hvs_tma_resident = 0;            // hvs_tables_tma CTAs per SM
 };
 
 constexpr int kMaxDevices = 64;
@@ -194,6 +214,19 @@ cudaError_t init_device(DeviceCtx &c, int dev) {
     e = cudaFuncSetAttribute(vqx::hvs_tables, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)vqx::kHvsTablesSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(vqx::hvs_tables_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)vqx::kHvsTmaSmem);
+    if (e != cudaSuccess) return e;
+    // The walk (one warp, no shared memory) runs beside the next batch's
+    // tables kernel: keep the SMs it sits on configured for the tables'
+    // shared memory, so that their CTAs are not held back until it ends.
+    e = cudaFuncSetAttribute(vqx::hvs_walk, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.hvs_tma_resident, vqx::hvs_tables_tma,
+                                                      vqx::kHvsTmaThreads, vqx::kHvsTmaSmem);
+    if (e != cudaSuccess) return e;
+    if (c.hvs_tma_resident < 1) c.hvs_tma_resident = 1;
     cudaMemPoolProps props;
     memset(&props, 0, sizeof props);
     props.allocType = cudaMemAllocationTypePinned;
@@ -775,7 +808,7 @@ namespace {
 void conclude_hvs(const vqx::HvsOut &w, int bpc, long long n_terms, vqx_hvs_plane *o) {
     o->flags = w.flags & (VQX_FLAG_RANGE | VQX_FLAG_TIMEOUT);
     o->replayed_leaves = w.replayed_leaves;
-    if (o->flags & VQX_FLAG_RANGE) {
+    if (o->flags & (VQX_FLAG_RANGE | VQX_FLAG_TIMEOUT)) {
         o->sum = o->score = std::nanf("");
         return;
     }
@@ -1434,8 +1467,27 @@ extern "C" int vqx_psnr_hvs_sum_submit(const float *terms, int64_t n_terms, int6
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (pd->timed) e = cudaEventRecord(pd->ev[0], st);
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, vqx::hvs_tables, a);
+    // Planes of 16-byte aligned terms with a pitch of whole vectors and at
+    // least one full row of 32 terms stream through the persistent TMA
+    // pipeline; anything else takes one CTA per node.
+    const long long rows_full = n_terms / 32;
+    const bool tma = a.vec && rows_full >= 1;
+    CUtensorMap tm;
+    vqx::HvsTmaArgs ta;
+    ta.rows_full = rows_full;
+    ta.tail = (int)(n_terms % 32);
+    if (tma) {
+        e = encode_hvs(&tm, terms, rows_full, plane_pitch, n_planes);
+        const long long total = (long long)n_planes * a.n_nodes;
+        const long long grid = (long long)ctx->hvs_tma_resident * ctx->sms;
+        cfg.gridDim = dim3((unsigned)(total < grid ? total : grid));
+        cfg.blockDim = dim3(vqx::kHvsTmaThreads);
+        cfg.dynamicSmemBytes = vqx::kHvsTmaSmem;
+    }
+    if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[0], st);
+    if (e == cudaSuccess)
+        e = tma ? cudaLaunchKernelEx(&cfg, vqx::hvs_tables_tma, tm, a, ta)
+                : cudaLaunchKernelEx(&cfg, vqx::hvs_tables, a);
     if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[1], st);
     if (e == cudaSuccess) {
         vqx::hvs_walk<<<(unsigned)n_planes, 32, 0, st>>>(a, (vqx::HvsOut *)pd->rec.dev);
