@@ -88,6 +88,47 @@ def test_layouts_wide_and_scalar_loads(lib, orc, offset, pitch_extra):
     check(lib, orc, t, n_terms=t.shape[1], pitch=t.shape[1] + pitch_extra, offset_floats=offset)
 
 
+@pytest.mark.parametrize("n,extra", [(36, 0), (1052, 4), (8220, 0), (16400, 12), (65540, 4),
+                                     (540696, 8), (1577988, 0)])
+def test_pipeline_partial_rows(lib, orc, n, extra):
+    """16-byte aligned planes with a pitch of whole vectors stream through the
+    persistent pipeline in boxes of full 32-term rows; a plane whose length is
+    not a multiple of 32 ends in a partial row that no box holds (the lane
+    whose run it is reads it itself).  NaN padding after every plane would
+    poison any sum that read past the plane's end."""
+    rng = np.random.default_rng(n)
+    t = rng.uniform(0, 5, (3, n)).astype(np.float32)
+    t[rng.random(t.shape) < 0.6] = 0.0
+    check(lib, orc, t, n_terms=n, pitch=n + extra)
+
+
+def test_pipeline_many_planes_with_partial_rows(lib, orc):
+    """500 planes of 1028 terms (one node each, four terms past the last full
+    row) through the pipeline: nodes of many planes interleave in every CTA."""
+    rng = np.random.default_rng(11)
+    t = rng.uniform(0, 1000, (500, 1028)).astype(np.float32)
+    t[rng.random(t.shape) < 0.7] = 0.0
+    check(lib, orc, t, n_terms=1028, pitch=1032)
+
+
+@pytest.mark.parametrize("where", ["row", "partial_row"])
+def test_pipeline_term_outside_the_domain(lib, orc, where):
+    """A negative term in a full row or in the partial last row flags its
+    plane on the pipelined path too; the other planes are unaffected."""
+    n = 70004
+    rng = np.random.default_rng(5)
+    t = rng.uniform(0, 3, (3, n)).astype(np.float32)
+    t[1, 31337 if where == "row" else n - 2] = -1.0
+    keep, ptr = to_device(t)
+    rec, rc = lib.vqx_psnr_hvs_sum(ptr, n, n, 3, 8, check=False)
+    torch.cuda.synchronize()
+    assert rc == lib.VQX_ERANGE
+    assert list(rec["flags"]) == [0, lib.VQX_FLAG_RANGE, 0]
+    sums, scores = orc.hvs(t[[0, 2]], 8)
+    assert rec[0]["sum"].tobytes() == sums[0].tobytes()
+    assert rec[2]["sum"].tobytes() == sums[1].tobytes()
+
+
 def test_many_small_planes(lib, orc):
     """3000 planes of 37 terms: one node each, 3000 walks."""
     rng = np.random.default_rng(7)
