@@ -498,28 +498,34 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
 // - Summer warp w sums leaf w (rows 32 w .. 32 w + 31) of every node as soon
 //   as it lands (any order) and checks its terms; the last of the eight adds
 //   the leaf sums and publishes the node's sum at once (its status word).
-// - kHvsTmaLookback look-back warps take nodes in turn: the look-back of
-//   hvs_tables, giving the prefix estimate of the node.
-// - Table warp w then tabulates each lane's run of leaf w in order and
+// - kHvsTmaLookback look-back warps take nodes in turn, once a node is
+//   summed: the look-back of hvs_tables gives its prefix estimate, and its
+//   inclusive prefix is published.
+// - Table warp w of set j (two sets of eight, taking even and odd nodes, so
+//   that each warp's chain of dependent additions and shuffles has two
+//   nodes' time) then tabulates each lane's run of leaf w in order and
 //   writes the leaf's record.
-// - The node's look-back warp, once the eight leaf records are in, composes
-//   the node's record and releases the buffer (all eight table warps do the
-//   same work, so none falls behind the others and holds the ring).
+// - Once its eight warps are past a named barrier, warp 0 of the set
+//   releases the buffer (keeping the node's flags and estimate) and then
+//   composes the node's record from the leaf records.
 // The summers run up to kHvsTmaStages nodes ahead of the table warps, so the
 // look-back's latency hides behind the ring instead of stalling it.
 // Terms of a plane's last, partial row (fewer than 32) are not in any box:
 // the lane whose run they are reads them itself.
 // Stage k of a CTA uses buffer k mod kHvsTmaStages; each of its mbarriers
 // (full: bytes landed; sums: the eight leaf sums written; excl: the prefix
-// estimate written; empty: the eight warps done with the buffer) completes
+// estimate written; empty: the buffer read, the record's inputs kept) completes
 // one phase per use, parity (k / kHvsTmaStages) & 1.  Every wait is
 // bounded; a warp whose wait gives up waits for nothing more, and every node
 // record written after it carries kHvsFlagTimeout.
 constexpr int kHvsTmaStages = 6;
-constexpr int kHvsTmaLookback = 4;
-constexpr int kHvsTmaSummers = kHvsLeaves;       // warps kHvsLeaves .. 2 kHvsLeaves - 1
-constexpr int kHvsTmaProducer = 2 * kHvsLeaves;  // warp index
-constexpr int kHvsTmaThreads = (2 * kHvsLeaves + 1 + kHvsTmaLookback) * 32;
+constexpr int kHvsTmaLookback = 2;
+constexpr int kHvsTmaTableSets = 2;                           // table warps 0 .. 15
+constexpr int kHvsTmaSummer0 = kHvsTmaTableSets * kHvsLeaves;  // summers 16 .. 23
+constexpr int kHvsTmaSummers = kHvsLeaves;                     // one leaf each
+constexpr int kHvsTmaProducer = kHvsTmaSummer0 + kHvsTmaSummers;
+constexpr int kHvsTmaThreads = (kHvsTmaProducer + 1 + kHvsTmaLookback) * 32;
+static_assert(kHvsTmaStages % kHvsTmaTableSets == 0, "a table set's nodes keep their stages");
 static_assert(kHvsTmaLookback <= kHvsTmaStages, "a look-back warp's previous node bounds its wait");
 constexpr uint32_t kHvsNodeBytes = kHvsNode * 4;
 constexpr int kHvsNodeRows = kHvsNode / 32;
@@ -528,6 +534,34 @@ constexpr size_t kHvsTmaSmem = (size_t)kHvsTmaStages * kHvsNodeBytes + 1024;  //
 struct HvsTmaArgs {
     long long rows_full;  // full rows of 32 terms per plane
     int tail;             // terms in the partial row (0 .. 31)
+};
+
+// bar.sync on named barrier id (1 .. 15) for `threads` threads (whole warps).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// The nodes a CTA takes, g = blockIdx.x + k gridDim.x for k = k0, k0 + s, ...,
+// as (plane g mod n_planes, node g / n_planes), stepped without a division
+// per node (g < 2^31: the host bounds n_planes times the node count).
+struct HvsNodeIter {
+    int plane, node, dplane, dnode, n_planes;
+    __device__ __forceinline__ HvsNodeIter(int k0, int s, int n_planes_) : n_planes(n_planes_) {
+        const unsigned P = (unsigned)n_planes_;
+        const unsigned g = blockIdx.x + (unsigned)k0 * gridDim.x, step = (unsigned)s * gridDim.x;
+        plane = (int)(g % P);
+        node = (int)(g / P);
+        dplane = (int)(step % P);
+        dnode = (int)(step / P);
+    }
+    __device__ __forceinline__ void next() {
+        plane += dplane;
+        node += dnode;
+        if (plane >= n_planes) {
+            plane -= n_planes;
+            node++;
+        }
+    }
 };
 
 // A wait that sleeps: try_wait with a suspend-time hint lets the thread be
@@ -556,7 +590,7 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
     hvs_tables_tma(const __grid_constant__ CUtensorMap tm, HvsArgs a, HvsTmaArgs t) {
     constexpr int S = kHvsTmaStages;
     extern __shared__ unsigned char hvs_raw[];
-    __shared__ __align__(8) u64 full[S], empty[S], sums[S], exclb[S], leafb[S];
+    __shared__ __align__(8) u64 full[S], empty[S], sums[S], exclb[S];
     __shared__ float s_leaf_sum[S][kHvsLeaves];
     __shared__ float s_excl[S];
     __shared__ unsigned s_flags[S], s_summed[S];
@@ -568,14 +602,13 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
     const uint32_t ring0 = (smem_u32(hvs_raw) + 1023u) & ~1023u;
     unsigned char *ring = hvs_raw + (ring0 - smem_u32(hvs_raw));
     const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
-    const uint32_t sums0 = smem_u32(sums), excl0 = smem_u32(exclb), leaf0 = smem_u32(leafb);
+    const uint32_t sums0 = smem_u32(sums), excl0 = smem_u32(exclb);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
-            mbar_init(sums0 + 8 * i, kHvsLeaves);
+            mbar_init(sums0 + 8 * i, kHvsTmaSummers);
             mbar_init(excl0 + 8 * i, 1);
-            mbar_init(leaf0 + 8 * i, kHvsLeaves);
             s_flags[i] = 0u;
             s_summed[i] = 0u;
         }
@@ -594,17 +627,16 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
         if (lane != 0) return;
         if (!a.terms_ready) grid_dependency_wait();
         int k = 0;
-        for (; k < nk; k++) {
+        HvsNodeIter it(0, 1, a.n_planes);
+        for (; k < nk; k++, it.next()) {
             const int st = k % S;
             if (k >= S && !mbar_wait_sleep(empty0 + 8 * st, ((k / S) - 1) & 1)) {
                 s_err = 1u;
                 break;
             }
-            const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
-            const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
             mbar_arrive_expect_tx(full0 + 8 * st, kHvsNodeBytes);
-            tensor_g2s_3d(ring0 + (uint32_t)st * kHvsNodeBytes, &tm, 0, node * kHvsNodeRows, plane,
-                          full0 + 8 * st);
+            tensor_g2s_3d(ring0 + (uint32_t)st * kHvsNodeBytes, &tm, 0, it.node * kHvsNodeRows,
+                          it.plane, full0 + 8 * st);
         }
         // the copies in flight land before the CTA (and its shared memory) ends
         for (int q = k > S ? k - S : 0; q < k; q++) mbar_wait_sleep(full0 + 8 * (q % S), (q / S) & 1);
@@ -613,126 +645,107 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
 
     if (warp > kHvsTmaProducer) {
         bool err = false;
-        for (int k = warp - kHvsTmaProducer - 1; k < nk; k += kHvsTmaLookback) {
+        const int k0 = warp - kHvsTmaProducer - 1;
+        HvsNodeIter it(k0, kHvsTmaLookback, a.n_planes);
+        for (int k = k0; k < nk; k += kHvsTmaLookback, it.next()) {
             const int st = k % S;
             const uint32_t par = (k / S) & 1;
             if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(sums0 + 8 * st, par))) {
                 err = true;
                 if (lane == 0) s_err = 1u;
             }
-            const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
-            const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
+            const int plane = it.plane, node = it.node;
             float excl = 0.0f;
             if (!err && node > 0) {
-                // the node's sum is published already (by the consumers)
-                const float node_sum = s_node_sum[st];
+                // the node's own sum was published by the summers already
                 u64 *stw = a.status + (size_t)plane * (size_t)a.n_nodes;
-                {
-                    const bool ok = hvs_lookback(stw, node, lane, tag, excl);
-                    if (lane == 0) {
-                        if (!ok) atomicOr(&s_flags[st], kHvsFlagGuess);
-                        st_relaxed_u64(stw + node,
-                                       tag | kHvsPrefix | __float_as_uint(__fadd_rn(excl, node_sum)));
-                    }
+                const bool ok = hvs_lookback(stw, node, lane, tag, excl);
+                if (lane == 0) {
+                    if (!ok) atomicOr(&s_flags[st], kHvsFlagGuess);
+                    st_relaxed_u64(stw + node,
+                                   tag | kHvsPrefix | __float_as_uint(__fadd_rn(excl, s_node_sum[st])));
                 }
             }
             if (lane == 0) {
                 s_excl[st] = excl;
                 mbar_arrive(excl0 + 8 * st);
             }
-            // the node's record, from its eight leaf records; then the buffer
-            // is free (every table warp arrived on leafb after its last read)
-            if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(leaf0 + 8 * st, par))) {
-                err = true;
-                if (lane == 0) s_err = 1u;
-            }
-            const uint32_t bn = hvs_guess(excl);
-            const long long nl = (long long)a.n_leaves - (long long)node * kHvsLeaves;
-            const bool in = lane < kHvsLeaves && lane < nl;
-            const HvsRec lr = s_leaf[st][lane & (kHvsLeaves - 1)];
-            const HvsFn g0 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn) : hvs_identity());
-            const HvsFn g1 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn + 1u) : hvs_identity());
-            if (lane == 0) {
-                HvsRec r;
-                r.k = make_uint4(g0.k0, g0.k1, g1.k0, g1.k1);
-                r.b = bn;
-                r.pad[0] = s_flags[st] | ((err || s_err) ? kHvsFlagTimeout : 0u);
-                r.pad[1] = r.pad[2] = 0;
-                a.nodes[(size_t)plane * (size_t)a.n_nodes + (size_t)node] = r;
-                s_flags[st] = 0u;
-                mbar_arrive(empty0 + 8 * st);
-            }
         }
         return;
     }
 
-    // summers (warps kHvsLeaves ..) and table warps (0 ..): leaf = warp mod 8
-    const bool summer = warp >= kHvsTmaSummers;
-    const int lw = summer ? warp - kHvsTmaSummers : warp;
+    // table warps (0 ..): leaf lw = warp mod 8 of set warp / 8; summers
+    // (kHvsTmaSummer0 ..): leaf lw
+    const bool summer = warp >= kHvsTmaSummer0;
+    const int lw = summer ? warp - kHvsTmaSummer0 : warp % kHvsLeaves;
     bool err = false;
     const float *const planes = a.terms;
-    auto pass1 = [&](int k) {
+    auto pass1 = [&](int k, int plane, int node) {
         const int st = k % S;
         if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(full0 + 8 * st, (k / S) & 1))) {
             err = true;
             if (lane == 0) s_err = 1u;
         }
-        const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
-        const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
-        float ls = 0.0f;
         bool bad = false;
-        if (!err) {
-            const float4 *lf = reinterpret_cast<const float4 *>(ring + (size_t)st * kHvsNodeBytes +
-                                                                (size_t)lw * kHvsLeaf * 4);
-            f32x2 acc_a = 0ull, acc_b = 0ull;
-            uint32_t mx = 0u;
+        {
+            const int leafw = lw;
+            float ls = 0.0f;
+            if (!err) {
+                const float4 *lf = reinterpret_cast<const float4 *>(
+                    ring + (size_t)st * kHvsNodeBytes + (size_t)leafw * kHvsLeaf * 4);
+                f32x2 acc_a = 0ull, acc_b = 0ull;
+                uint32_t mx = 0u;
 #pragma unroll
-            for (int i = 0; i < kHvsLeafVecs / 32; i++) {
-                const float4 v = lf[lane + 32 * i];
-                const uint32_t ux = __float_as_uint(v.x), uy = __float_as_uint(v.y);
-                const uint32_t uz = __float_as_uint(v.z), uw = __float_as_uint(v.w);
-                acc_a = f2_add(acc_a, f2_pack(ux, uy));
-                acc_b = f2_add(acc_b, f2_pack(uz, uw));
-                mx = __vimax3_u32(mx, ux, uy);
-                mx = __vimax3_u32(mx, uz, uw);
-            }
-            uint32_t a0, a1, b0, b1;
-            f2_unpack(acc_a, a0, a1);
-            f2_unpack(acc_b, b0, b1);
-            ls = __fadd_rn(__fadd_rn(__uint_as_float(a0), __uint_as_float(a1)),
-                           __fadd_rn(__uint_as_float(b0), __uint_as_float(b1)));
-            if (mx >= kHvsTermLimit) {
-#pragma unroll 1
                 for (int i = 0; i < kHvsLeafVecs / 32; i++) {
                     const float4 v = lf[lane + 32 * i];
-                    bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) |
-                           hvs_bad_term(v.w);
+                    const uint32_t ux = __float_as_uint(v.x), uy = __float_as_uint(v.y);
+                    const uint32_t uz = __float_as_uint(v.z), uw = __float_as_uint(v.w);
+                    acc_a = f2_add(acc_a, f2_pack(ux, uy));
+                    acc_b = f2_add(acc_b, f2_pack(uz, uw));
+                    mx = __vimax3_u32(mx, ux, uy);
+                    mx = __vimax3_u32(mx, uz, uw);
+                }
+                uint32_t a0, a1, b0, b1;
+                f2_unpack(acc_a, a0, a1);
+                f2_unpack(acc_b, b0, b1);
+                ls = __fadd_rn(__fadd_rn(__uint_as_float(a0), __uint_as_float(a1)),
+                               __fadd_rn(__uint_as_float(b0), __uint_as_float(b1)));
+                if (mx >= kHvsTermLimit) {
+#pragma unroll 1
+                    for (int i = 0; i < kHvsLeafVecs / 32; i++) {
+                        const float4 v = lf[lane + 32 * i];
+                        bad |= hvs_bad_term(v.x) | hvs_bad_term(v.y) | hvs_bad_term(v.z) |
+                               hvs_bad_term(v.w);
+                    }
+                }
+                // the partial row, if it is one of this leaf's rows
+                const long long row0 = (long long)node * kHvsNodeRows + (long long)leafw * 32;
+                if (t.tail && t.rows_full >= row0 && t.rows_full < row0 + 32 && lane < t.tail) {
+                    const float v = __ldg(planes + (size_t)plane * (size_t)a.pitch +
+                                          (size_t)t.rows_full * 32 + lane);
+                    ls = __fadd_rn(ls, v);
+                    bad |= hvs_bad_term(v);
                 }
             }
-            // the partial row, if it is one of this leaf's rows
-            const long long row0 = (long long)node * kHvsNodeRows + (long long)lw * 32;
-            if (t.tail && t.rows_full >= row0 && t.rows_full < row0 + 32 && lane < t.tail) {
-                const float v = __ldg(planes + (size_t)plane * (size_t)a.pitch +
-                                      (size_t)t.rows_full * 32 + lane);
-                ls = __fadd_rn(ls, v);
-                bad |= hvs_bad_term(v);
-            }
+            ls = warp_sum_f(ls);
+            if (lane == 0) s_leaf_sum[st][leafw] = ls;
         }
-        ls = warp_sum_f(ls);
         bad = __any_sync(0xffffffffu, bad);
         unsigned last = 0u;
         if (lane == 0) {
-            s_leaf_sum[st][lw] = ls;
             if (bad) atomicOr(&s_flags[st], kHvsFlagRange);
             __threadfence_block();
-            last = atomicAdd(&s_summed[st], 1u) == kHvsLeaves - 1 ? 1u : 0u;
+            last = atomicAdd(&s_summed[st], 1u) == kHvsTmaSummers - 1 ? 1u : 0u;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             // the last warp: node sum, published as this node's aggregate
             // (the inclusive prefix for a plane's first node)
             __threadfence_block();
-            const float node_sum = warp_sum_f(lane < kHvsLeaves ? s_leaf_sum[st][lane] : 0.0f);
+            float node_sum = s_leaf_sum[st][lane & (kHvsLeaves - 1)];
+#pragma unroll
+            for (int off = kHvsLeaves / 2; off > 0; off >>= 1)
+                node_sum = __fadd_rn(node_sum, __shfl_xor_sync(0xffffffffu, node_sum, off));
             if (lane == 0) {
                 s_node_sum[st] = node_sum;
                 s_summed[st] = 0u;
@@ -747,15 +760,13 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
         if (lane == 0) mbar_arrive(sums0 + 8 * st);
     };
 
-    auto pass2 = [&](int k) {
+    auto pass2 = [&](int k, int plane, int node) {
         const int st = k % S;
         if (!err && !__all_sync(0xffffffffu, mbar_wait_sleep(full0 + 8 * st, (k / S) & 1) &&
                                                  mbar_wait_sleep(excl0 + 8 * st, (k / S) & 1))) {
             err = true;
             if (lane == 0) s_err = 1u;
         }
-        const long long g = (long long)blockIdx.x + (long long)k * gridDim.x;
-        const int plane = (int)(g % a.n_planes), node = (int)(g / a.n_planes);
         const long long leaf = (long long)node * kHvsLeaves + lw;
         HvsFn f0 = {kHvsBad, kHvsBad}, f1 = {kHvsBad, kHvsBad};
         uint32_t bl = 1u;
@@ -800,14 +811,44 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
             if (leaf < a.n_leaves) a.leaves[(size_t)plane * (size_t)a.n_leaves + (size_t)leaf] = r;
             if (err) s_err = 1u;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(leaf0 + 8 * st);
+        // the set's eight warps meet (their reads of the buffer are done);
+        // its warp 0 frees the buffer, keeping what the node's record needs
+        // (the flags, which the next use of the stage sets afresh, and the
+        // prefix estimate), then composes the record from the leaf records
+        // (which only this set rewrites, after its warp 0 is back)
+        named_barrier(1 + warp / kHvsLeaves, 32 * kHvsLeaves);
+        if (lw == 0) {
+            const float ex = s_excl[st];
+            const HvsRec lr = s_leaf[st][lane & (kHvsLeaves - 1)];
+            uint32_t fl = 0u;
+            if (lane == 0) {
+                fl = s_flags[st] | ((err || s_err) ? kHvsFlagTimeout : 0u);
+                s_flags[st] = 0u;
+                mbar_arrive(empty0 + 8 * st);
+            }
+            const uint32_t bn = hvs_guess(ex);
+            const long long nl = (long long)a.n_leaves - (long long)node * kHvsLeaves;
+            const bool in = lane < kHvsLeaves && lane < nl;
+            const HvsFn g0 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn) : hvs_identity());
+            const HvsFn g1 = hvs_reduce<kHvsLeaves>(in ? hvs_select(lr, bn + 1u) : hvs_identity());
+            if (lane == 0) {
+                HvsRec r;
+                r.k = make_uint4(g0.k0, g0.k1, g1.k0, g1.k1);
+                r.b = bn;
+                r.pad[0] = fl;
+                r.pad[1] = r.pad[2] = 0;
+                a.nodes[(size_t)plane * (size_t)a.n_nodes + (size_t)node] = r;
+            }
+        }
     };
 
     if (summer) {
-        for (int k = 0; k < nk; k++) pass1(k);
+        HvsNodeIter it(0, 1, a.n_planes);
+        for (int k = 0; k < nk; k++, it.next()) pass1(k, it.plane, it.node);
     } else {
-        for (int k = 0; k < nk; k++) pass2(k);
+        const int set = warp / kHvsLeaves;
+        HvsNodeIter it(set, kHvsTmaTableSets, a.n_planes);
+        for (int k = set; k < nk; k += kHvsTmaTableSets, it.next()) pass2(k, it.plane, it.node);
     }
 }
 
