@@ -136,38 +136,68 @@ __device__ __forceinline__ void ord_block_pixels(const OrdPlanes &g, int f, int 
 
 // Grid (blocks per frame / kSumWarps, frames), one warp per block: the exact
 // sums of the three term sequences over each block, sums[(f * nb + b) * 3 +
-// q], the OR of each sequence's terms, ors[same index] (a block whose terms
-// are all multiples of the ulp it works at adds without rounding), and the
-// sums of the block's reference and distorted samples, ssums[(f * nb + b) *
-// 2 + 0, 1] (below 4096 * 2^16 = 2^28).
+// q], the OR of each sequence's terms (at least of their low 16 bits),
+// ors[same index] (a block whose terms are all multiples of the ulp it works
+// at adds without rounding), and the sums of the block's reference and
+// distorted samples, ssums[(f * nb + b) * 2 + 0, 1] (below 4096 * 2^16 =
+// 2^28).
 // Dense frames, two pixels of a 32-bit word at a time: the samples' floats
 // from their bits, the three products as packed fp32 pairs (each lane one
-// round-to-nearest-even product, fma with +0 so that nothing fuses), their
-// exact integer conversions added in 64 bits and ORed three inputs at a
-// time, the samples summed by a two-way dot product.
+// round-to-nearest-even product, fma with +0 so that nothing fuses); the noise
+// and distorted squares converted to integers (F2I) and added in 64 bits, the
+// reference squares split by exact fp32 additions into a multiple of 2^16 and
+// a remainder of magnitude at most 2^15 whose bit patterns are added as
+// 32-bit integers (SplitSum2's form), so that the conversions, which run on
+// the SM's narrow XU pipe and bound this pass at three a pixel, are two.  The
+// remainder's bit pattern ends in the square's low 16 bits (the multiple of
+// 2^16 adds nothing there), so ORing the patterns gives the OR of the
+// reference squares' low 16 bits: all that the replay tests of it (ulps up to
+// 2^4, as every sum stays below 2^57).  The samples are summed by a two-way
+// dot product.
 struct OrdWordSums {
     u64 t[kOrdSeqs] = {0, 0, 0};
     uint32_t o[kOrdSeqs] = {0, 0, 0};
+    uint32_t hi = 0, lo = 0, n = 0;  // reference squares as split bit patterns
     uint32_t sr = 0, sd = 0;
 
     __device__ __forceinline__ void word(uint32_t a, uint32_t b) {
         constexpr uint32_t kBias = 0x4B000000u;
         const f32x2 two23 = ((f32x2)kBias << 32) | kBias;
+        const f32x2 c_hi = ((f32x2)SplitSum2::kHiBits << 32) | SplitSum2::kHiBits;
+        const f32x2 c_lo = ((f32x2)SplitSum2::kLoBits << 32) | SplitSum2::kLoBits;
         const f32x2 xr = f2_pack((a & 0xffffu) | kBias, __byte_perm(a, kBias, 0x7632));
         const f32x2 xd = f2_pack((b & 0xffffu) | kBias, __byte_perm(b, kBias, 0x7632));
-        uint32_t v[kOrdSeqs][2];
+        uint32_t v[2][2];
         f2_unpack(f2_square(f2_sub(xr, xd)), v[0][0], v[0][1]);
-        f2_unpack(f2_square(f2_sub(xr, two23)), v[1][0], v[1][1]);
-        f2_unpack(f2_square(f2_sub(xd, two23)), v[2][0], v[2][1]);
+        f2_unpack(f2_square(f2_sub(xd, two23)), v[1][0], v[1][1]);
 #pragma unroll
-        for (int q = 0; q < kOrdSeqs; q++) {
-            const uint32_t x0 = __float2uint_rn(__uint_as_float(v[q][0]));
-            const uint32_t x1 = __float2uint_rn(__uint_as_float(v[q][1]));
+        for (int i = 0; i < 2; i++) {
+            const int q = i == 0 ? 0 : 2;
+            const uint32_t x0 = __float2uint_rn(__uint_as_float(v[i][0]));
+            const uint32_t x1 = __float2uint_rn(__uint_as_float(v[i][1]));
             t[q] += (u64)x0 + x1;
             o[q] |= x0 | x1;
         }
+        const f32x2 rsq = f2_square(f2_sub(xr, two23));
+        const f32x2 hb = f2_add(rsq, c_hi);                            // kHiBits + h / 2^16
+        const f32x2 lb = f2_add(f2_sub(rsq, f2_sub(hb, c_hi)), c_lo);  // kLoBits + l
+        uint32_t h0, h1, l0, l1;
+        f2_unpack(hb, h0, h1);
+        f2_unpack(lb, l0, l1);
+        hi += h0 + h1;
+        lo += l0 + l1;
+        o[1] |= l0 | l1;
+        n += 2;
         sr = __dp2a_lo(a, 0x01010101u, sr);
         sd = __dp2a_lo(b, 0x01010101u, sd);
+    }
+    // the exact sum of sequence q (at most 2^15 split terms, far inside
+    // SplitSum2's bound)
+    __device__ __forceinline__ u64 total(int q) const {
+        if (q != 1) return t[q];
+        const u64 units = (u64)(uint32_t)(hi - n * SplitSum2::kHiBits);
+        const long long rest = (long long)(int32_t)(lo - n * SplitSum2::kLoBits);
+        return t[1] + units * 65536 + (u64)rest;
     }
 };
 
@@ -212,17 +242,20 @@ __global__ void __launch_bounds__(32 * kSumWarps)
             w.sd += d;
         });
     }
+    u64 tot[kOrdSeqs];
+#pragma unroll
+    for (int q = 0; q < kOrdSeqs; q++) tot[q] = w.total(q);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1)
 #pragma unroll
-        for (int q = 0; q < kOrdSeqs; q++) w.t[q] += __shfl_xor_sync(0xffffffffu, w.t[q], sh);
+        for (int q = 0; q < kOrdSeqs; q++) tot[q] += __shfl_xor_sync(0xffffffffu, tot[q], sh);
     uint32_t o[kOrdSeqs];
 #pragma unroll
     for (int q = 0; q < kOrdSeqs; q++) o[q] = __reduce_or_sync(0xffffffffu, w.o[q]);
     const uint32_t sr = __reduce_add_sync(0xffffffffu, w.sr), sd = __reduce_add_sync(0xffffffffu, w.sd);
     const size_t slot = ((size_t)f * g.nb + b) * kOrdSeqs;
     if (lane < kOrdSeqs) {
-        sums[slot + lane] = lane == 0 ? w.t[0] : lane == 1 ? w.t[1] : w.t[2];
+        sums[slot + lane] = lane == 0 ? tot[0] : lane == 1 ? tot[1] : tot[2];
         ors[slot + lane] = lane == 0 ? o[0] : lane == 1 ? o[1] : o[2];
     } else if (lane < kOrdSeqs + 2) {
         ssums[((size_t)f * g.nb + b) * 2 + (lane - kOrdSeqs)] = lane == kOrdSeqs ? sr : sd;
