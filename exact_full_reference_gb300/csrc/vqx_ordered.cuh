@@ -208,7 +208,7 @@ constexpr int kSumWarps = 4;  // blocks (one per warp) per CTA of ordered_block_
 // only its own batch's workspace (which the batch ahead does not hold) and,
 // unless planes_ready, waits for the kernel ahead before reading the planes.
 // It also zeroes the work-list count that ordered_classify appends to.
-__global__ void __launch_bounds__(32 * kSumWarps)
+__global__ void __launch_bounds__(32 * kSumWarps, 10)
     ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
                        uint32_t *__restrict__ ssums, int *__restrict__ n_work, int planes_ready) {
     if (!planes_ready) grid_dependency_wait();
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(32 * kSumWarps)
         const uint32_t len = ord_len(g, b);
         const size_t off = (size_t)f * g.frame_pitch + 2 * (size_t)b * kOrdBlock;
         const unsigned char *rb = g.ref + off, *db = g.dist + off;
-#pragma unroll 4
+#pragma unroll 8
         for (uint32_t v = lane; v < len / 8; v += 32) {
             const uint4 x = ord_ld16(rb + 16 * (size_t)v), y = ord_ld16(db + 16 * (size_t)v);
             w.word(x.x, y.x);
