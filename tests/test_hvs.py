@@ -64,6 +64,27 @@ def test_headline_batch_every_plane(lib, orc):
     assert rec["replayed_leaves"].max() < leaves // 100, rec["replayed_leaves"]
 
 
+def test_headline_batch_pipelined_as_the_benchmark_runs_it(lib, orc):
+    """The 3840x2160 batch of 32 planes as the benchmark times it: batch i + 1
+    submitted with VQX_SUBMIT_PLANES_READY before batch i is finished, so the
+    next batch's tables run beside this batch's walk; every batch equals the
+    oracle bit for bit."""
+    w = wl.HVS_WORKLOADS[wl.HVS_HEADLINE]
+    t = w.generate()
+    dev = torch.from_numpy(t).cuda()
+    torch.cuda.synchronize()
+    sums, scores = orc.hvs(t, w.bpc)
+    prev = None
+    for _ in range(6):
+        cur = lib.vqx_psnr_hvs_sum_submit(dev, bpc=w.bpc, flags=lib.VQX_SUBMIT_PLANES_READY)
+        if prev is not None:
+            rec = prev.finish()
+            assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
+        prev = cur
+    rec = prev.finish()
+    assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
+
+
 @pytest.mark.parametrize("bpc", [8, 10, 12, 16])
 def test_score_at_every_depth(lib, orc, bpc):
     w = wl.HVS_WORKLOADS["hvs_576x324_8bit_x4"]

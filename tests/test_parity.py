@@ -47,6 +47,26 @@ def test_workload_parity(lib, orc, name):
         assert parity.exact_count(un) == len(un)
 
 
+def test_headline_batch_pipelined_as_the_benchmark_runs_it(lib):
+    """The 3840x2160 16-bit batch in the benchmark's launch configuration:
+    batch i + 1 submitted with VQX_SUBMIT_PLANES_READY before batch i is
+    finished, so consecutive batches' kernels overlap; every batch's records
+    equal the blocking call's, which test_workload_parity holds to the
+    oracle."""
+    w = wl.WORKLOADS[wl.HEADLINE]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    geo = (w.width, w.height, stride, w.bpc, w.n_frames)
+    want = lib.vqx_plane_stats(pr, pd, *geo).tobytes()
+    prev = None
+    for _ in range(6):
+        cur = lib.vqx_plane_stats_submit(pr, pd, *geo, flags=lib.VQX_SUBMIT_PLANES_READY)
+        if prev is not None:
+            assert prev.finish().tobytes() == want
+        prev = cur
+    assert prev.finish().tobytes() == want
+
+
 def test_headline_checkerboard_frame(lib, orc):
     """The checkerboard frame of the 3840x2160 16-bit batch, alone."""
     w = wl.WORKLOADS["3840x2160_16bit_x32"]
