@@ -149,7 +149,9 @@ cudaError_t encode_hvs(CUtensorMap *tm, const float *terms, long long rows, long
     cudaError_t e = encode_fn(&enc);
     if (e != cudaSuccess) return e;
     const cuuint64_t dims[3] = {32, (cuuint64_t)rows, (cuuint64_t)planes};
-    const cuuint64_t strides[2] = {128, (cuuint64_t)pitch * 4};
+    // one plane: its pitch is never stepped over, so any valid stride does
+    // (a pitch of 2^38 floats or more would not encode)
+    const cuuint64_t strides[2] = {128, planes > 1 ? (cuuint64_t)pitch * 4 : (cuuint64_t)rows * 128};
     const cuuint32_t box[3] = {32, (cuuint32_t)vqx::kHvsNodeRows, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
     const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(terms), dims,

@@ -150,6 +150,19 @@ def test_pipeline_term_outside_the_domain(lib, orc, where):
     assert rec[2]["sum"].tobytes() == sums[1].tobytes()
 
 
+def test_one_plane_with_a_huge_pitch(lib, orc):
+    """With one plane the pitch is never stepped over: a pitch of 2^40 floats
+    (far more memory than exists) must not matter on the pipelined path."""
+    rng = np.random.default_rng(17)
+    t = rng.uniform(0, 4, (1, 40004)).astype(np.float32)
+    t[rng.random(t.shape) < 0.5] = 0.0
+    keep, ptr = to_device(t)
+    rec = lib.vqx_psnr_hvs_sum(ptr, t.shape[1], 1 << 40, 1, 8)
+    torch.cuda.synchronize()
+    sums, scores = orc.hvs(t, 8)
+    assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
+
+
 def test_many_small_planes(lib, orc):
     """3000 planes of 37 terms: one node each, 3000 walks."""
     rng = np.random.default_rng(7)
