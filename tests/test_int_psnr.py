@@ -107,3 +107,27 @@ def test_submit_finish_and_kind_check(lib, orc):
     p.kind = "int_psnr"
     out, rc = p.finish(check=False)
     assert rc == lib.VQX_EINVAL
+
+
+def test_headline_batch_pipelined_as_the_benchmark_runs_it(lib, orc):
+    """The 3840x2160 16-bit batch as bench.py --op int_psnr times it: batch
+    i + 1 submitted with VQX_SUBMIT_PLANES_READY before batch i is finished;
+    every batch equals the blocking call, whose SSE and doubles equal the
+    oracle's on the first and last frame."""
+    w = wl.WORKLOADS["3840x2160_16bit_x32"]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, _ = parity.place(ref, dist)
+    geo = (w.width, w.height, stride, w.bpc, w.n_frames)
+    want = lib.vqx_plane_int_psnr(pr, pd, *geo)
+    oracle_rec = orc.int_psnr_frames(ref[[0, -1]], dist[[0, -1]], w.bpc)
+    for i, f in enumerate((0, w.n_frames - 1)):
+        assert int(want[f]["sse"]) == int(oracle_rec[i]["sse"])
+        assert want[f]["psnr"] == oracle_rec[i]["psnr"] and want[f]["mse"] == oracle_rec[i]["mse"]
+    prev = None
+    for _ in range(6):
+        cur = lib.vqx_plane_int_psnr_submit(pr, pd, *geo, flags=lib.VQX_SUBMIT_PLANES_READY)
+        if prev is not None:
+            assert prev.finish().tobytes() == want.tobytes()
+        prev = cur
+    assert prev.finish().tobytes() == want.tobytes()
+

@@ -92,3 +92,28 @@ def test_ordered_submit_finish_pipelined(lib, orc):
     k2, p2, q2, s2, _ = parity.place(r2, d2)
     p = lib.vqx_plane_stats_ordered_submit(p2, q2, small.width, small.height, s2, 10, 2)
     assert p.finish().tobytes() == lib.vqx_plane_stats(p2, q2, small.width, small.height, s2, 10, 2).tobytes()
+
+
+def test_headline_batch_pipelined_as_the_benchmark_runs_it(lib, orc):
+    """The 3840x2160 16-bit batch as bench.py --op ordered times it: batch
+    i + 1 submitted with VQX_SUBMIT_PLANES_READY before batch i is finished
+    (its block sums run beside the previous batch's classification, tables
+    and walk); every batch equals the oracle's doubles, checked on the first
+    and the last (checkerboard) frame."""
+    w = wl.WORKLOADS["3840x2160_16bit_x32"]
+    ref, dist = w.generate()
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    geo = (w.width, w.height, stride, w.bpc, w.n_frames)
+    want = lib.vqx_plane_stats_ordered(pr, pd, *geo)
+    sub_r, sub_d = w.generate([0, w.n_frames - 1])
+    k2, p2, q2, s2, (r2, d2) = parity.place(sub_r, sub_d)
+    sc, un = orc.batch(r2, d2, w.width, w.height, s2, w.bpc, 2)
+    check_identical(want[[0, w.n_frames - 1]], sc, un)
+    prev = None
+    for _ in range(6):
+        cur = lib.vqx_plane_stats_ordered_submit(pr, pd, *geo, flags=lib.VQX_SUBMIT_PLANES_READY)
+        if prev is not None:
+            assert prev.finish().tobytes() == want.tobytes()
+        prev = cur
+    assert prev.finish().tobytes() == want.tobytes()
+
