@@ -89,7 +89,8 @@ typedef struct CUstream_st *vqx_stream_t;
 #define VQX_FLAG_TIMEOUT 2u /* a device-side wait for this frame timed out */
 
 /* Results for one frame pair.  The integer fields are the exact sums on the
- * device ("debug" accumulators); the doubles are concluded from them. */
+ * device (the accumulators a debug mode would show); the doubles are concluded
+ * from them. */
 typedef struct {
     uint64_t noise_units;     /* sum of float(D * D), D = r - d raw; unit 1/S^2 */
     uint64_t ref_sum;         /* sum of r; unit 1/S */

@@ -24,7 +24,7 @@
  *    plane, each divided by the number of pixels at the end.
  *
  * Readings where the pages are silent (each also listed in the design notes):
- *  - "row by row" is one double accumulator walked in raster order;
+ *  - the row-by-row accumulation is one double accumulator walked in raster order;
  *  - MSE = noise / (w * h); PSNR = 10 log10(255^2 / MSE);
  *  - the PSNR cap is 6 * bpc + 12 dB (60, 72, 84, 108), applied as a min; the
  *    uncapped value is +inf when MSE = 0;
