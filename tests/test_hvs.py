@@ -163,6 +163,19 @@ def test_one_plane_with_a_huge_pitch(lib, orc):
     assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
 
 
+def test_one_very_long_plane(lib, orc):
+    """2^27 terms in one plane (16384 nodes, 4 Mi rows of 32): the row and
+    node coordinates of the pipelined path at a large scale."""
+    rng = np.random.default_rng(23)
+    n = (1 << 27) + 12
+    t = rng.uniform(0, 2, n).astype(np.float32)
+    t[rng.random(n) < 0.7] = 0.0
+    dev = torch.from_numpy(t).cuda()
+    rec = lib.vqx_psnr_hvs_sum(dev, bpc=8)
+    sums, scores = orc.hvs(t, 8)
+    assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
+
+
 def test_many_small_planes(lib, orc):
     """3000 planes of 37 terms: one node each, 3000 walks."""
     rng = np.random.default_rng(7)

@@ -117,3 +117,18 @@ def test_headline_batch_pipelined_as_the_benchmark_runs_it(lib, orc):
         prev = cur
     assert prev.finish().tobytes() == want.tobytes()
 
+
+def test_ordered_at_the_largest_frame(lib, orc):
+    """One 8192x4096 16-bit frame pair (2^25 pixels, the largest frame the
+    library takes) of full-range noise: the square sums reach about 2^56
+    units, so the replay works at ulps up to 2^4, the most any frame needs
+    (the block ORs it tests keep at least the terms' low 16 bits)."""
+    rng = np.random.Generator(np.random.PCG64(2025))
+    ref = rng.integers(0, 1 << 16, (1, 4096, 8192), dtype=np.uint16)
+    dist = rng.integers(0, 1 << 16, (1, 4096, 8192), dtype=np.uint16)
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    rec = lib.vqx_plane_stats_ordered(pr, pd, 8192, 4096, stride, 16, 1)
+    sc, un = orc.batch(rb, db, 8192, 4096, stride, 16, 1)
+    assert int(un[0]["ref_sumsq"]) > 1 << 55
+    check_identical(rec, sc, un)
+
