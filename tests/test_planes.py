@@ -128,3 +128,43 @@ def test_planes_submit_finish(lib, orc):
     p.kind, p.shape = "stats", 4
     out, rc = p.finish(check=False)
     assert rc == lib.VQX_EINVAL
+
+
+def test_headline_planes_pipelined_as_the_benchmark_runs_it(lib, orc):
+    """Y, Cb and Cr of the 3840x2160 16-bit batch (the chroma planes at half
+    size, the same content recipe, their own seeds) as bench.py --op
+    planes420 times them: batch i + 1 submitted with VQX_SUBMIT_PLANES_READY
+    before batch i is finished.  Every batch equals the blocking call, whose
+    records equal vqx_plane_stats plane by plane and the oracle on the first
+    and last frame of each plane."""
+    import dataclasses
+
+    from exact_full_reference_gb300 import workloads as wl
+
+    w = wl.WORKLOADS[wl.HEADLINE]
+    chroma = [dataclasses.replace(w, name=w.name + "_c%d" % k, width=w.width // 2,
+                                  height=w.height // 2, seed=w.seed + 1000 * k) for k in (1, 2)]
+    keep, descs, frames = [], [], []
+    for p_w in [w] + chroma:
+        ref, dist = p_w.generate()
+        k, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+        keep.append(k)
+        descs.append((pr, pd, p_w.width, p_w.height, stride, 0))
+        frames.append((ref, dist, rb, db, stride, p_w))
+    n = w.n_frames
+    want = lib.vqx_planes_stats(descs, 16, n)
+    for q, (ref, dist, rb, db, stride, p_w) in enumerate(frames):
+        plain = lib.vqx_plane_stats(descs[q][0], descs[q][1], p_w.width, p_w.height, stride, 16, n)
+        assert want[:, q].tobytes() == plain.tobytes(), q
+        sc, un = orc.frames(ref[[0, n - 1]], dist[[0, n - 1]], 16)
+        for i, f in enumerate((0, n - 1)):
+            for k_u in parity.UNIT_FIELDS:
+                assert int(want[f, q][k_u]) == int(un[i][k_u]), (q, f, k_u)
+    prev = None
+    for _ in range(6):
+        cur = lib.vqx_planes_stats_submit(descs, 16, n, flags=lib.VQX_SUBMIT_PLANES_READY)
+        if prev is not None:
+            assert prev.finish().tobytes() == want.tobytes()
+        prev = cur
+    assert prev.finish().tobytes() == want.tobytes()
+
