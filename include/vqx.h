@@ -379,8 +379,8 @@ int vqx_plane_stats_noalloc(const void *ref, const void *dist, int width, int he
  *   p * plane_pitch floats after `terms`.  4-byte aligned.  A 16-byte aligned
  *   base with plane_pitch a multiple of 4 (and at least 32 terms) takes the
  *   fast path, a persistent pipeline of tensor-map copies; any other layout
- *   is read with plain loads, about 15 % slower.  Read only, not retained
- *   after the call.
+ *   takes one CTA per node with plain loads, which is slower.  Read only, not
+ *   retained after the call.
  * Every term must be a non-negative float below 2^95 (-0 counts as 0).  A
  *   plane holding anything else (a negative value, NaN, infinity, 2^95 or
  *   more) gets VQX_FLAG_RANGE and NaN sum and score; the call fills every
