@@ -24,6 +24,7 @@ collective in the data path); rank 0 prints.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -53,7 +54,8 @@ def metric_for(op, wlo):
     if op == "stats":
         return METRIC
     what = {"int_psnr": "integer psnr", "ordered": "fused PSNR+moments, CPU-order replay",
-            "planes420": "fused PSNR+moments, 4:2:0 Y+Cb+Cr"}[op]
+            "planes420": "fused PSNR+moments, 4:2:0 Y+Cb+Cr",
+            "scores": "fused PSNR+moments and integer psnr, one read"}[op]
     return "frame pairs/s and HBM GB/s (%s), %dx%d %d-bit, 1 GB300" % (
         what, wlo.width, wlo.height, wlo.bpc)
 FALLBACK_HBM_GBS = 6800.0
@@ -67,13 +69,25 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=None, help="workload name (default: the 3840x2160 16-bit batch)")
     p.add_argument("--e2e-steps", type=int, default=60)
+    p.add_argument("--repeats", type=int, default=21,
+                   help="at least this many timed regions of K steps; value is their median")
+    p.add_argument("--min-timed-seconds", type=float, default=1.5,
+                   help="repeat the timed region until about this much wall time has passed, so "
+                        "that the clock sampler sees the GPU under load")
+    p.add_argument("--inst-repeats", type=int, default=5,
+                   help="instrumented regions for the per-launch kernel times")
+    p.add_argument("--config-seconds", type=float, default=0.4,
+                   help="the same, for each of the other measured configurations")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other measured configurations after the headline")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--op", choices=["stats", "int_psnr", "ordered", "planes420", "hvs"],
+    p.add_argument("--op", choices=["stats", "int_psnr", "scores", "ordered", "planes420", "hvs"],
                    default="stats",
                    help="stats: the fused float_psnr + moments pass (the headline); int_psnr: "
-                        "the integer psnr (vqx_plane_int_psnr); ordered: the CPU-order replay "
+                        "the integer psnr (vqx_plane_int_psnr); scores: both from one read "
+                        "(vqx_plane_scores); ordered: the CPU-order replay "
                         "past 2^53 units (vqx_plane_stats_ordered_submit / _finish); "
                         "planes420: the workload as the luma of 4:2:0 video, Y, Cb and Cr "
                         "through one vqx_planes_stats call a step; hvs: psnr_hvs plane sums "
@@ -302,7 +316,7 @@ def time_oracle(wlo, ref, dist, seconds, cores, rows=None, min_rounds=1, op="sta
         y0 = (k * 7919) % (h - band + 1) if band < h else 0
         if op != "int_psnr":
             orc.batch(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
-        else:
+        if op in ("int_psnr", "scores"):
             orc.int_psnr(ref[f, y0 : y0 + band], dist[f, y0 : y0 + band], w, band, stride, wlo.bpc, 1)
         for cr, cd in extra:
             ch, cw = cr.shape[1:]
@@ -377,222 +391,398 @@ def run_reference(args, wlo):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, wlo):
-    import ctypes
+def repeat_count(region_s, min_repeats, min_seconds, cap=5000):
+    """How many timed regions to run: at least ``min_repeats``, and enough
+    to fill ``min_seconds`` of wall time at ``region_s`` seconds a region
+    (so that the clock sampler sees the GPU under load), at most ``cap``."""
+    want = min_repeats
+    if region_s > 0:
+        want = max(want, int(math.ceil(min_seconds / region_s)))
+    return int(min(max(want, 1), max(cap, min_repeats)))
 
-    import numpy as np
-    import torch
 
-    __import__("__graft_entry__").build()
-    import exact_full_reference_gb300 as vqx
+def summarize_regions(region_ms, steps):
+    """Median, minimum and maximum of the timed regions (ms, K steps each),
+    and the median's time per step."""
+    s = sorted(region_ms)
+    return {"repeats": len(s), "median_ms": statistics.median(s), "min_ms": s[0], "max_ms": s[-1],
+            "p10_ms": s[int(0.1 * (len(s) - 1))], "p90_ms": s[int(0.9 * (len(s) - 1))],
+            "ms_per_step": statistics.median(s) / max(steps, 1)}
 
-    rank, world, local = dist_env()
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
 
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-        pg = dist
-    torch.cuda.set_device(local)
-    dev = torch.cuda.current_device()
-    stream = torch.cuda.Stream()
-    sh = stream.cuda_stream
+class BenchDevice:
+    """What every measurement on this rank shares: torch, the binding, the
+    device, the launching stream and the process group."""
 
-    ref, dist_np = wlo.generate()
-    n, h, w = ref.shape
-    stride = w * wlo.bytes_per_sample
-    rbytes = ref.reshape(-1).view(np.uint8)
-    dbytes = dist_np.reshape(-1).view(np.uint8)
-    d_ref = torch.from_numpy(rbytes).to(dev)
-    d_dist = torch.from_numpy(dbytes).to(dev)
-    torch.cuda.synchronize()
+    def __init__(self, world, local):
+        import torch
 
-    so = vqx.library()
-    out = np.zeros(n, vqx.INT_PSNR_DTYPE if args.op == "int_psnr" else vqx.FRAME_STATS_DTYPE)
-    chroma_np, chroma_dev = [], []
-    if args.op == "planes420":
-        out = np.zeros((n, 3), vqx.FRAME_STATS_DTYPE)
-        for c in chroma_workloads(wlo):
-            cr, cd = c.generate()
-            chroma_np.append((cr, cd))
-            chroma_dev.append((torch.from_numpy(cr.reshape(-1).view(np.uint8)).to(dev),
-                               torch.from_numpy(cd.reshape(-1).view(np.uint8)).to(dev), c))
-        descs = (vqx.PlaneDesc * 3)(
-            vqx.PlaneDesc(d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, 0),
-            *[vqx.PlaneDesc(tr.data_ptr(), td.data_ptr(), c.width, c.height,
-                            c.width * c.bytes_per_sample, 0) for tr, td, c in chroma_dev])
-    out_p = out.ctypes.data
-    # the planes are written once, before any step: batches may start reading
-    # them while the batch ahead finishes
-    submit_args = (d_ref.data_ptr(), d_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh,
-                   vqx.VQX_SUBMIT_PLANES_READY)
-    if args.op == "planes420":
-        def submit_fn(*a):
-            return so.vqx_planes_stats_submit(descs, 3, wlo.bpc, n, sh, vqx.VQX_SUBMIT_PLANES_READY, a[-1])
+        __import__("__graft_entry__").build()
+        import exact_full_reference_gb300 as vqx
 
-        finish_fn = so.vqx_planes_stats_finish
-    elif args.op == "ordered":
-        submit_fn = so.vqx_plane_stats_ordered_submit
-        finish_fn = so.vqx_plane_stats_ordered_finish
-    else:
-        submit_fn = getattr(so, "vqx_plane_%s_submit" % args.op)
-        finish_fn = getattr(so, "vqx_plane_%s_finish" % args.op)
+        self.torch, self.vqx, self.so = torch, vqx, vqx.library()
+        self.world, self.pg = world, None
+        if world > 1:
+            import torch.distributed as dist
 
-    def submit():
-        handle = ctypes.c_void_p()
-        rc = submit_fn(*submit_args, ctypes.byref(handle))
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+            self.pg = dist
+        torch.cuda.set_device(local)
+        self.dev = torch.cuda.current_device()
+        self.stream = torch.cuda.Stream()
+        self.sh = self.stream.cuda_stream
+        self.l2_bytes = getattr(torch.cuda.get_device_properties(self.dev), "L2_cache_size", 0) or (129 << 20)
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+
+OP_API = {"stats": "vqx_plane_stats", "int_psnr": "vqx_plane_int_psnr",
+          "scores": "vqx_plane_scores", "ordered": "vqx_plane_stats_ordered",
+          "planes420": "vqx_planes_stats"}
+
+
+class Batch:
+    """One workload's planes on the device and the op's submit / finish
+    calls on them (the call a user makes; arguments only)."""
+
+    def __init__(self, ctx, wlo, op):
+        import ctypes
+
+        import numpy as np
+
+        torch, vqx, so = ctx.torch, ctx.vqx, ctx.so
+        self.ctx, self.wlo, self.op = ctx, wlo, op
+        self.ref, self.dist = wlo.generate()
+        n, h, w = self.ref.shape
+        self.n = n
+        stride = w * wlo.bytes_per_sample
+        self.rbytes = self.ref.reshape(-1).view(np.uint8)
+        self.dbytes = self.dist.reshape(-1).view(np.uint8)
+        self.d_ref = torch.from_numpy(self.rbytes).to(ctx.dev)
+        self.d_dist = torch.from_numpy(self.dbytes).to(ctx.dev)
+        torch.cuda.synchronize()
+        self.chroma_np, chroma_dev = [], []
+        self.out = np.zeros(n, vqx.INT_PSNR_DTYPE if op == "int_psnr" else vqx.FRAME_STATS_DTYPE)
+        self.out2 = np.zeros(n, vqx.INT_PSNR_DTYPE)  # scores: the integer psnr records
+        if op == "planes420":
+            self.out = np.zeros((n, 3), vqx.FRAME_STATS_DTYPE)
+            for c in chroma_workloads(wlo):
+                cr, cd = c.generate()
+                self.chroma_np.append((cr, cd))
+                chroma_dev.append((torch.from_numpy(cr.reshape(-1).view(np.uint8)).to(ctx.dev),
+                                   torch.from_numpy(cd.reshape(-1).view(np.uint8)).to(ctx.dev), c))
+            self._chroma_dev = chroma_dev
+            self.descs = (vqx.PlaneDesc * 3)(
+                vqx.PlaneDesc(self.d_ref.data_ptr(), self.d_dist.data_ptr(), w, h, stride, 0),
+                *[vqx.PlaneDesc(tr.data_ptr(), td.data_ptr(), c.width, c.height,
+                                c.width * c.bytes_per_sample, 0) for tr, td, c in chroma_dev])
+        self.geometry = (w, h, stride, wlo.bpc, n)
+        # the planes are written once, before any step: batches may start
+        # reading them while the batch ahead finishes
+        args = (self.d_ref.data_ptr(), self.d_dist.data_ptr(), w, h, stride, wlo.bpc, n, ctx.sh,
+                vqx.VQX_SUBMIT_PLANES_READY)
+        out_p, out2_p = self.out.ctypes.data, self.out2.ctypes.data
+        if op == "planes420":
+            descs = self.descs
+
+            def submit_call(handle):
+                return so.vqx_planes_stats_submit(descs, 3, wlo.bpc, n, ctx.sh,
+                                                  vqx.VQX_SUBMIT_PLANES_READY, handle)
+
+            def finish_call(handle):
+                return so.vqx_planes_stats_finish(handle, out_p)
+        else:
+            sub = getattr(so, {"ordered": "vqx_plane_stats_ordered_submit"}.get(
+                op, "vqx_plane_%s_submit" % op))
+            fin = getattr(so, {"ordered": "vqx_plane_stats_ordered_finish"}.get(
+                op, "vqx_plane_%s_finish" % op))
+
+            def submit_call(handle):
+                return sub(*args, handle)
+
+            if op == "scores":
+                def finish_call(handle):
+                    return fin(handle, out_p, out2_p)
+            else:
+                def finish_call(handle):
+                    return fin(handle, out_p)
+        self._submit_call, self._finish_call = submit_call, finish_call
+        self.flush = (self.rbytes.nbytes + self.dbytes.nbytes) < 2 * ctx.l2_bytes
+        self.scratch = (torch.empty(2 * ctx.l2_bytes, dtype=torch.uint8, device=ctx.dev)
+                        if self.flush else None)
+        self._ctypes = ctypes
+
+    @property
+    def plane_bytes(self):
+        return int(self.rbytes.nbytes + self.dbytes.nbytes
+                   + sum(cr.nbytes + cd.nbytes for cr, cd in self.chroma_np))
+
+    def submit(self):
+        handle = self._ctypes.c_void_p()
+        rc = self._submit_call(self._ctypes.byref(handle))
         if rc != 0:
-            raise RuntimeError("submit: %s" % vqx.status_string(rc))
+            raise RuntimeError("submit: %s" % self.ctx.vqx.status_string(rc))
         return handle
 
-    def finish(handle):
-        rc = finish_fn(handle, out_p)
+    def finish(self, handle):
+        rc = self._finish_call(handle)
         if rc != 0:
-            raise RuntimeError("finish: %s" % vqx.status_string(rc))
+            raise RuntimeError("finish: %s" % self.ctx.vqx.status_string(rc))
 
-    def steps(k):
+    def steps(self, k):
         """k whole steps, pipelined: batch i + 1 is enqueued before batch i is
         waited on and concluded, so the device runs the next batch's kernels
         while the host concludes this one."""
         prev = None
         for _ in range(k):
-            cur = submit()
+            cur = self.submit()
             if prev is not None:
-                finish(prev)
+                self.finish(prev)
             prev = cur
         if prev is not None:
-            finish(prev)
+            self.finish(prev)
 
-    def barrier():
-        if pg is not None:
-            pg.barrier()
-
-    steps(max(args.warmup, 3))
-    torch.cuda.synchronize()
-
-    # A batch that fits in L2 would be read from L2 after the first step: such
-    # batches get the L2 overwritten before every step, and each step is then
-    # timed on its own (not pipelined), flush excluded.
-    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
-    flush = (rbytes.nbytes + dbytes.nbytes) < 2 * l2_bytes
-    scratch = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
-
-    def flushed_steps(k):
+    def flushed_steps(self, k):
         """k steps, each after an L2 flush; returns the summed step time (ms)."""
+        torch, stream = self.ctx.torch, self.ctx.stream
         total = 0.0
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         for _ in range(k):
             with torch.cuda.stream(stream):
-                scratch.zero_()
+                self.scratch.zero_()
             e0.record(stream)
-            finish(submit())
+            self.finish(self.submit())
             e1.record(stream)
             e1.synchronize()
             total += e0.elapsed_time(e1)
         return total
 
-    def timed_region(instrumented):
+    def region(self, steps, instrumented):
         """K steps between a barrier + synchronize on both sides, timed with
-        CUDA events on the launching stream.  With ``instrumented`` the library
-        also records CUDA events around its kernels inside every call (which
-        costs the overlap of the two kernels' launches, so the throughput is
-        taken from the uninstrumented region)."""
-        barrier()
+        CUDA events on the launching stream (L2-sized batches: each step after
+        a flush, flush excluded).  With ``instrumented`` the library also
+        records CUDA events around its kernels inside every call, which costs
+        the overlap of consecutive launches, so throughput comes from the
+        uninstrumented regions.  Returns (max-over-ranks ms, wall t0, t1)."""
+        ctx = self.ctx
+        torch = ctx.torch
+        ctx.barrier()
         torch.cuda.synchronize()
-        vqx.profile_enable(instrumented)
-        vqx.profile_read(reset=True)
+        ctx.vqx.profile_enable(instrumented)
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         t0 = time.time()
-        if flush:
-            region_ms = flushed_steps(args.steps)
+        if self.flush:
+            ms = self.flushed_steps(steps)
         else:
-            ev0.record(stream)
-            steps(args.steps)  # the last conclusion is inside the region too
-            ev1.record(stream)
+            ev0.record(ctx.stream)
+            self.steps(steps)  # the last conclusion is inside the region too
+            ev1.record(ctx.stream)
         torch.cuda.synchronize()
         t1 = time.time()
-        if not flush:
-            region_ms = ev0.elapsed_time(ev1)
-        barrier()
-        prof = vqx.profile_read(reset=True)
-        vqx.profile_enable(False)
-        return reduce_max(region_ms, pg, dev), prof, t0, t1
+        if not self.flush:
+            ms = ev0.elapsed_time(ev1)
+        ctx.barrier()
+        ctx.vqx.profile_enable(False)
+        return reduce_max(ms, ctx.pg, ctx.dev), t0, t1
 
-    clocks = ClockSampler(gpu_smi_id(torch, dev))
-    time.sleep(0.3)
-    elapsed_ms, counted, t_wall0, t_wall1 = timed_region(False)
-    inst_ms, prof, _, _ = timed_region(True)
-    time.sleep(0.2)
-    clocks.stop()
-    value = job_throughput(world, n, args.steps, elapsed_ms / 1e3)
+    def measure(self, steps, warmup, min_repeats, min_seconds, inst_repeats):
+        """Warm up, then the timed regions (repeated: at least min_repeats and
+        about min_seconds of wall time, the same count on every rank), then
+        inst_repeats instrumented regions for the per-launch kernel times."""
+        ctx = self.ctx
+        self.steps(max(warmup, 3))
+        ctx.torch.cuda.synchronize()
+        calib_ms, c0, c1 = self.region(steps, False)
+        reps = repeat_count(c1 - c0, min_repeats, min_seconds)
+        reps = int(reduce_max(reps, ctx.pg, ctx.dev))
+        ctx.vqx.profile_read(reset=True)
+        regions, t_first, t_last = [], None, None
+        for _ in range(reps):
+            ms, t0, t1 = self.region(steps, False)
+            regions.append(ms)
+            t_first = t0 if t_first is None else t_first
+            t_last = t1
+        counted = ctx.vqx.profile_read(reset=True)
+        for _ in range(max(inst_repeats, 1)):
+            self.region(steps, True)
+        prof = ctx.vqx.profile_read(reset=True)
+        return {"regions": summarize_regions(regions, steps), "counted": counted, "prof": prof,
+                "t0": t_first, "t1": t_last, "reps": reps}
 
-    # roofline of the fused kernel, from the events recorded inside the calls
-    peak, peak_kind = measured_peak()
+
+def kernel_label(op, wlo):
+    if op == "int_psnr" and wlo.bpc == 16:
+        return "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
+    if op == "scores" and wlo.bpc == 16:
+        return "fused_stream_tma<16, 16, 1536, 2, DenseSource, TermSums16Sse>"
+    if op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
+        return "ordered_block_sums"
+    if op == "planes420":
+        return "fused_stream_tma, three planes (Y, Cb, Cr) timed together"
+    return KERNEL_LABEL % (wlo.bpc, wlo.bpc)
+
+
+def kernel_roofline(prof, peak):
     launches = max(prof["stage1_launches"], 1)
     avg_ms = prof["stage1_ms"] / launches
     bytes_per_launch = prof["stage1_bytes"] / launches
-    achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
+    achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else 0.0
+    return avg_ms, bytes_per_launch, achieved, achieved / peak
+
+
+def link_ceiling(ctx, rbytes, dbytes, repeats=5):
+    """A plain copy of the batch's planes from pinned host memory to the
+    device (torch copy_ on the launching stream, both planes, back to back),
+    timed with CUDA events; the median of ``repeats``.  Returns GB/s."""
+    torch = ctx.torch
+    h = [torch.from_numpy(b).pin_memory() for b in (rbytes, dbytes)]
+    d = [torch.empty(b.nbytes, dtype=torch.uint8, device=ctx.dev) for b in (rbytes, dbytes)]
+    times = []
+    for i in range(repeats + 1):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(ctx.stream)
+        with torch.cuda.stream(ctx.stream):
+            for dd, hh in zip(d, h):
+                dd.copy_(hh, non_blocking=True)
+        e1.record(ctx.stream)
+        e1.synchronize()
+        if i:  # the first copy is a warm-up
+            times.append(e0.elapsed_time(e1))
+    return (rbytes.nbytes + dbytes.nbytes) / (statistics.median(times) / 1e3) / 1e9
+
+
+def run_ours(args, wlo):
+    import ctypes
+
+    import numpy as np
+
+    rank, world, local = dist_env()
+    ctx = BenchDevice(world, local)
+    torch, vqx, so = ctx.torch, ctx.vqx, ctx.so
+    b = Batch(ctx, wlo, args.op)
+    n, h, w = b.ref.shape
+    stride = w * wlo.bytes_per_sample
+
+    clocks = ClockSampler(gpu_smi_id(torch, ctx.dev))
+    time.sleep(0.3)
+    m = b.measure(args.steps, args.warmup, args.repeats, args.min_timed_seconds, args.inst_repeats)
+    time.sleep(0.2)
+    clocks.stop()
+    reg = m["regions"]
+    value = job_throughput(world, n, args.steps, reg["median_ms"] / 1e3)
+
+    # roofline of the fused kernel, from the events recorded inside the calls
+    peak, peak_kind = measured_peak()
+    avg_ms, bytes_per_launch, achieved, frac = kernel_roofline(m["prof"], peak)
     traffic = recorded_traffic(wlo.name) if args.op == "stats" else None
-    label = KERNEL_LABEL % (wlo.bpc, wlo.bpc)
-    if args.op == "int_psnr" and wlo.bpc == 16:
-        label = "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
-    if args.op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
-        label = "ordered_block_sums"
-    if args.op == "planes420":
-        label = "fused_stream_tma, three planes (Y, Cb, Cr) timed together"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                "timing": "CUDA events recorded by the library around each launch in a second "
-                          "timed region of the same %d steps" % args.steps,
-                "instrumented_region_ms_per_step": inst_ms / args.steps,
-                "kernel": label, "avg_launch_us": avg_ms * 1e3,
+                "frac": frac, "traffic": traffic, "peak_source": peak_kind,
+                "timing": "CUDA events recorded by the library around each launch in %d "
+                          "instrumented regions of the same %d steps"
+                          % (max(args.inst_repeats, 1), args.steps),
+                "kernel": kernel_label(args.op, wlo), "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
-                "stage2_avg_us": prof["stage2_ms"] / launches * 1e3}
+                "stage2_avg_us": m["prof"]["stage2_ms"] / max(m["prof"]["stage1_launches"], 1) * 1e3}
 
     # end to end: planes in pinned host memory, copies inside the timed region
     e2e = None
     if not args.no_e2e and args.op == "stats":
-        h_ref = torch.from_numpy(rbytes).pin_memory()
-        h_dist = torch.from_numpy(dbytes).pin_memory()
+        h_ref = torch.from_numpy(b.rbytes).pin_memory()
+        h_dist = torch.from_numpy(b.dbytes).pin_memory()
         e2e_out = np.zeros(n, vqx.FRAME_STATS_DTYPE)
-        e2e_args = (h_ref.data_ptr(), h_dist.data_ptr(), w, h, stride, wlo.bpc, n, sh,
+        e2e_args = (h_ref.data_ptr(), h_dist.data_ptr(), w, h, stride, wlo.bpc, n, ctx.sh,
                     e2e_out.ctypes.data)
         for _ in range(3):
             rc = so.vqx_plane_stats_host(*e2e_args)
             if rc != 0:
                 raise RuntimeError("vqx_plane_stats_host: %s" % vqx.status_string(rc))
-        assert e2e_out.tobytes() == out.tobytes(), "host-memory path disagrees with the device path"
+        assert e2e_out.tobytes() == b.out.tobytes(), "host-memory path disagrees with the device path"
         k = max(1, min(args.e2e_steps, args.steps))
-        barrier()
+        ctx.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(k):
             so.vqx_plane_stats_host(*e2e_args)
         torch.cuda.synchronize()
-        el = reduce_max(time.perf_counter() - t0, pg, dev)
-        e2e = {"value": job_throughput(world, n, k, el), "unit": UNIT, "steps": k,
-               "h2d_bytes_per_step": int(rbytes.nbytes + dbytes.nbytes),
+        el = reduce_max(time.perf_counter() - t0, ctx.pg, ctx.dev)
+        e2e_value = job_throughput(world, n, k, el)
+        link = link_ceiling(ctx, b.rbytes, b.dbytes)
+        e2e_gbs = e2e_value / world * wlo.pair_bytes / 1e9
+        e2e = {"value": e2e_value, "unit": UNIT, "steps": k,
+               "h2d_bytes_per_step": int(b.rbytes.nbytes + b.dbytes.nbytes),
                "d2h_bytes_per_step": int(n * ctypes.sizeof(ctypes.c_uint64) * 6),
-               "api": "vqx_plane_stats_host (pinned host planes)"}
+               "api": "vqx_plane_stats_host (pinned host planes)",
+               "h2d_gbs": e2e_gbs, "link_gbs": link, "link_frac": e2e_gbs / link,
+               "link": "a plain pinned-host-to-device copy_ of the same planes on the same "
+                       "stream, CUDA events, median of 5"}
+        del h_ref, h_dist
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cores = host_cores()
         sub = list(range(min(n, cores)))
-        ex = [(cr[sub], cd[sub]) for cr, cd in chroma_np]
-        rate, pairs, el = time_oracle(wlo, ref[sub], dist_np[sub], args.cpu_seconds, cores,
+        ex = [(cr[sub], cd[sub]) for cr, cd in b.chroma_np]
+        rate, pairs, el = time_oracle(wlo, b.ref[sub], b.dist[sub], args.cpu_seconds, cores,
                                       op=args.op, extra=ex)
-        rate1, pairs1, el1 = time_oracle(wlo, ref[:1], dist_np[:1], min(args.cpu_seconds, 4.0), 1,
-                                         op=args.op, extra=[(cr[:1], cd[:1]) for cr, cd in chroma_np])
+        rate1, pairs1, el1 = time_oracle(wlo, b.ref[:1], b.dist[:1], min(args.cpu_seconds, 4.0), 1,
+                                         op=args.op, extra=[(cr[:1], cd[:1]) for cr, cd in b.chroma_np])
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%.1f frame pairs of %s (whole frames, one per thread) in %.1f s"
                          % (pairs, wlo.name, el),
                "single_core": {"value": rate1, "sample": "%.1f frame pairs on one thread in %.1f s"
                                                          % (pairs1, el1)}}
 
+    # the other configurations of the measured set, timed the same way after
+    # the headline (each batch placed on the device in turn)
+    configs = None
+    if args.op == "stats" and not args.no_configs and args.workload in (None, wlo.name):
+        from exact_full_reference_gb300 import workloads as wl
+
+        planes_bytes = b.plane_bytes
+        del b
+        torch.cuda.empty_cache()
+        configs = {}
+        for name in wl.BENCH_CONFIGS:
+            if name == wlo.name:
+                continue
+            cw = wl.WORKLOADS[name]
+            cb = Batch(ctx, cw, "stats")
+            cm = cb.measure(args.steps, args.warmup, args.repeats, args.config_seconds,
+                            args.inst_repeats)
+            cr = cm["regions"]
+            c_ms, c_bytes, c_ach, c_frac = kernel_roofline(cm["prof"], peak)
+            step_gbs = cw.pair_bytes * cw.n_frames / (cr["ms_per_step"] / 1e3) / 1e9
+            configs[name] = {
+                "value": job_throughput(world, cw.n_frames, args.steps, cr["median_ms"] / 1e3),
+                "unit": UNIT, "ms_per_step": cr["ms_per_step"],
+                "us_per_call": cr["ms_per_step"] * 1e3,
+                "repeats": cr["repeats"], "min_ms": cr["min_ms"], "max_ms": cr["max_ms"],
+                "step_gbs": step_gbs, "step_frac": step_gbs / peak,
+                "kernel": KERNEL_LABEL % (cw.bpc, cw.bpc), "kernel_avg_launch_us": c_ms * 1e3,
+                "kernel_frac": c_frac,
+                "l2": ("batch smaller than twice the L2: L2 overwritten before every step, steps "
+                       "timed one by one, flush excluded" if cb.flush else
+                       "inputs %.2f GB per step, larger than the L2; no flush, steps pipelined"
+                       % (cb.plane_bytes / 1e9)),
+                "gpu_launches_per_region": int(cm["counted"]["kernel_launches"] // max(cm["reps"], 1)),
+            }
+            del cb
+            torch.cuda.empty_cache()
+    else:
+        planes_bytes = b.plane_bytes
+
     if rank == 0:
+        pipeline = ("batch i + 1 submitted before batch i is finished (%s_submit with "
+                    "VQX_SUBMIT_PLANES_READY / _finish)" % OP_API[args.op])
+        if args.op == "planes420":
+            pipeline += "; Y, Cb, Cr"
+        is_flush = (n * wlo.pair_bytes) < 2 * ctx.l2_bytes
         line = {
             "metric": metric_for(args.op, wlo),
             "value": value,
@@ -600,49 +790,47 @@ def run_ours(args, wlo):
             "n_gpus": world,
             "steps": args.steps,
             "warmup": max(args.warmup, 3),
-            "ms_per_step": elapsed_ms / args.steps,
+            "ms_per_step": reg["ms_per_step"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": ("u%d samples, %s" % (8 if wlo.bpc == 8 else 16,
-                      "f32 terms, u64 sums" if args.op == "stats" else "exact integer squares, u64 sums")),
+                      "f32 terms, u64 sums" if args.op in ("stats", "ordered", "planes420")
+                      else "f32 terms and exact integer squares, u64 sums" if args.op == "scores"
+                      else "exact integer squares, u64 sums")),
             "data": "synthetic",
             "hbm_gbs": value * wlo.pair_bytes * (1.5 if args.op == "planes420" else 1.0) / 1e9 / world,
+            "timing": {"repeats": reg["repeats"], "statistic": "median of the repeated regions",
+                       "region_ms": {k: reg[k] for k in ("median_ms", "min_ms", "p10_ms", "p90_ms",
+                                                        "max_ms")},
+                       "value_min": job_throughput(world, n, args.steps, reg["max_ms"] / 1e3),
+                       "value_max": job_throughput(world, n, args.steps, reg["min_ms"] / 1e3)},
             "config": {"workload": wlo.name, "frames_per_gpu": n, "width": w, "height": h,
-                       "bpc": wlo.bpc,
-                       "batch_bytes": int(rbytes.nbytes + dbytes.nbytes
-                                          + sum(cr.nbytes + cd.nbytes for cr, cd in chroma_np)),
+                       "bpc": wlo.bpc, "batch_bytes": planes_bytes,
                        "l2": "inputs %.2f GB per step, larger than the 129 MB L2; no flush"
-                             % ((rbytes.nbytes + dbytes.nbytes) / 1e9),
-                       "pipeline": ("batch i + 1 submitted before batch i is finished "
-                                    "(vqx_plane_stats_ordered_submit with VQX_SUBMIT_PLANES_READY "
-                                    "/ _finish)"
-                                    if args.op == "ordered" else
-                                    "batch i + 1 submitted before batch i is finished "
-                                    "(vqx_planes_stats_submit with VQX_SUBMIT_PLANES_READY / "
-                                    "_finish; Y, Cb, Cr)"
-                                    if args.op == "planes420" else
-                                    "batch i + 1 submitted before batch i is finished "
-                                    "(vqx_plane_%s_submit with VQX_SUBMIT_PLANES_READY / "
-                                    "_finish)" % args.op),
+                             % (planes_bytes / 1e9),
+                       "pipeline": pipeline,
                        "parallelism": "frames independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e,
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "clocks": clocks.summary(t_wall0, t_wall1),
-            "gpu_launches": int(counted["kernel_launches"]),
+            "clocks": clocks.summary(m["t0"], m["t1"]),
+            "gpu_launches": int(m["counted"]["kernel_launches"] // max(m["reps"], 1)),
+            "gpu_launches_all_repeats": int(m["counted"]["kernel_launches"]),
         }
-        if flush:
+        if is_flush:
             line["config"]["l2"] = ("batch smaller than twice the L2: L2 overwritten (%d MB) before "
                                     "every step, steps timed one by one, flush excluded"
-                                    % (2 * l2_bytes >> 20))
+                                    % (2 * ctx.l2_bytes >> 20))
             line["config"]["pipeline"] = "none (each step timed on its own after the flush)"
         if args.op == "planes420":
             line["config"]["planes"] = "Y %dx%d, Cb and Cr %dx%d per frame" % (
                 w, h, max(1, w // 2), max(1, h // 2))
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    if ctx.pg is not None:
+        ctx.pg.destroy_process_group()
     return 0
 
 

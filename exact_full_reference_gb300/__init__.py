@@ -121,13 +121,15 @@ def library():
             fn = getattr(lib, name)
             fn.argtypes = [vp, vp, i, i, sz, i, i, vp, vp]
             fn.restype = i
-        for kind in ("stats", "int_psnr", "stats_ordered"):
+        for kind in ("stats", "int_psnr", "stats_ordered", "scores"):
             sub = getattr(lib, "vqx_plane_%s_submit" % kind)
             sub.argtypes = [vp, vp, i, i, sz, i, i, vp, ctypes.c_uint, ctypes.POINTER(vp)]
             sub.restype = i
             fin = getattr(lib, "vqx_plane_%s_finish" % kind)
-            fin.argtypes = [vp, vp]
+            fin.argtypes = [vp, vp, vp] if kind == "scores" else [vp, vp]
             fin.restype = i
+        lib.vqx_plane_scores.argtypes = [vp, vp, i, i, sz, i, i, vp, vp, vp]
+        lib.vqx_plane_scores.restype = i
         lib.vqx_planes_stats.argtypes = [ctypes.POINTER(PlaneDesc), i, i, i, vp, vp]
         lib.vqx_planes_stats.restype = i
         lib.vqx_planes_stats_submit.argtypes = [ctypes.POINTER(PlaneDesc), i, i, i, vp, ctypes.c_uint,
@@ -258,6 +260,15 @@ class Pending:
     def finish(self, out=None, check=True):
         if self._handle is False:
             raise RuntimeError("this batch was already finished")
+        if self.kind == "scores":
+            stats = np.zeros(self.shape, FRAME_STATS_DTYPE)
+            ints = np.zeros(self.shape, INT_PSNR_DTYPE)
+            rc = library().vqx_plane_scores_finish(self._handle, stats.ctypes.data if stats.size else None,
+                                                   ints.ctypes.data if ints.size else None)
+            self._handle, self._keep = False, None
+            if check and rc != VQX_OK:
+                _raise("vqx_plane_scores_finish", rc)
+            return (stats, ints) if check else (stats, ints, rc)
         if out is None:
             dtype = {"int_psnr": INT_PSNR_DTYPE, "hvs": HVS_PLANE_DTYPE}.get(self.kind, FRAME_STATS_DTYPE)
             out = np.zeros(self.shape, dtype)
@@ -310,6 +321,31 @@ def vqx_plane_int_psnr(ref, dist, width=None, height=None, stride=None, bpc=16, 
     out, rc = _call("vqx_plane_int_psnr", ref, dist, width, height, stride, bpc, n_frames,
                     _stream_handle(stream), out, check, INT_PSNR_DTYPE)
     return out if check else (out, rc)
+
+
+def vqx_plane_scores_submit(ref, dist, width=None, height=None, stride=None, bpc=16,
+                            n_frames=None, stream=None, flags=0):
+    """The same for ``vqx_plane_scores`` (``finish()`` gives the pair of
+    record arrays)."""
+    return _submit("scores", ref, dist, width, height, stride, bpc, n_frames, stream, flags)
+
+
+def vqx_plane_scores(ref, dist, width=None, height=None, stride=None, bpc=16, n_frames=None,
+                     stream=None, check=True):
+    """float_psnr, float_moment and the integer psnr of device-resident planes
+    from one read: returns ``(stats, int_psnr)``, a ``FRAME_STATS_DTYPE`` and
+    an ``INT_PSNR_DTYPE`` array of ``n_frames`` records each (with
+    ``check=False``, ``(stats, int_psnr, status)``)."""
+    width, height, stride, n_frames = _geometry(ref, width, height, stride, n_frames, bpc)
+    stats = np.zeros(max(n_frames, 0), FRAME_STATS_DTYPE)
+    ints = np.zeros(max(n_frames, 0), INT_PSNR_DTYPE)
+    rc = library().vqx_plane_scores(_address(ref), _address(dist), width, height, stride, bpc,
+                                    n_frames, _stream_handle(stream),
+                                    stats.ctypes.data if stats.size else None,
+                                    ints.ctypes.data if ints.size else None)
+    if check and rc != VQX_OK:
+        _raise("vqx_plane_scores", rc)
+    return (stats, ints) if check else (stats, ints, rc)
 
 
 def vqx_plane_stats_host(ref, dist, width=None, height=None, stride=None, bpc=16,

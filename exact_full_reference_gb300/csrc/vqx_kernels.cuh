@@ -33,11 +33,23 @@ namespace vqx {
 
 typedef unsigned long long u64;
 
-// One CTA's sums: noise, ref sum, dist sum, ref sum of squares, dist sum of
-// squares, and the OR of every sample read (for the range check).
+// One record of sums (a warp's, a CTA's, a unit's or a frame's), 64 bytes:
+//   v[0] noise         sum of float(D * D)
+//   v[1], v[2]         sums of the reference and distorted samples
+//   v[3], v[4]         sums of float(r * r), float(d * d)
+//   v[5]               OR of every sample read (the range check), plus
+//                      kErrTimeout when a device wait gave up
+//   v[6]               the exact sum of D * D minus v[0], modulo 2^64 (the
+//                      integer psnr's SSE is v[0] + v[6]); 0 wherever the
+//                      float squares are exact or the accumulator does not
+//                      form it
+//   v[7]               0
+// The accumulators' totals() fill the same eight words; every word but v[5]
+// is a sum, v[5] an OR.
 struct Partial {
-    u64 v[6];
+    u64 v[8];
 };
+constexpr int kWords = 8;
 
 constexpr int kThreads = 256;     // CTA size of the strided-layout stage-1 kernel
 constexpr int kSumThreads = 128;  // stage-2 CTA size
@@ -217,14 +229,14 @@ struct TermSums<8> {
         srd += rd_;
         r_ = d_ = rr_ = dd_ = rd_ = 0;
     }
-    __device__ __forceinline__ void totals(u64 (&t)[6]) {
+    __device__ __forceinline__ void totals(u64 (&t)[kWords]) {
         flush();
         t[0] = srr + sdd - 2 * srd;
         t[1] = sr;
         t[2] = sd;
         t[3] = srr;
         t[4] = sdd;
-        t[5] = 0;
+        t[5] = t[6] = t[7] = 0;
     }
 };
 
@@ -270,7 +282,7 @@ struct TermSums {
         sd += d_;
         r_ = d_ = 0;
     }
-    __device__ __forceinline__ void totals(u64 (&t)[6]) {
+    __device__ __forceinline__ void totals(u64 (&t)[kWords]) {
         flush();
         t[0] = rr + dd - 2 * rd;
         t[1] = sr;
@@ -278,6 +290,7 @@ struct TermSums {
         t[3] = rr;
         t[4] = dd;
         t[5] = (orv & 0xffffu) | (orv >> 16);  // word() ORs two samples per word
+        t[6] = t[7] = 0;
     }
 };
 
@@ -315,6 +328,12 @@ __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
 __device__ __forceinline__ f32x2 f2_square(f32x2 a) {
     f32x2 d;
     asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(d) : "l"(a), "l"(0ull));
+    return d;
+}
+// fl(a * b + c) per lane: one rounding of the exact a * b + c.
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
 
@@ -372,25 +391,42 @@ struct SplitSum2 {
 //   integer at least every kFlushVecs vectors (8 terms each).  The noise and
 //   the distorted plane's square streams are converted (exactly: the values
 //   are integers below 2^32) with F2I, which runs on the XU pipe, and added in
-//   64-bit integers on the ALU pipe.  No stream is accumulated in floating
-//   point.  The work is spread over the FMA, ALU and XU pipes so that none of
+//   64-bit integers on the ALU pipe.  None of these streams is accumulated
+//   in floating point.  The work is spread over the FMA, ALU and XU pipes so that none of
 //   them limits the pass (two conversions a pixel keep the XU pipe, a quarter
 //   as wide, below its own limit at full HBM bandwidth).
 // - Sums of samples: dp2a adds the two 16-bit halves of a word.
-template <>
-struct TermSums<16> {
+// With kSse the same pass also forms the exact sum of D * D (the integer
+// psnr's SSE), from the rounding error of each noise square: with D exact in
+// fp32 and q = fl(D * D), the fused multiply-add fl(-D * D + q) is exact
+// (q - D * D is the rounding error of a product, itself a float: an integer
+// of magnitude at most 128, half an ulp of 2^32), so
+//   SSE = sum of q - sum of (q - D * D) = noise - sum of the errors.
+// The errors are added per lane in fp32, which is exact while the running sum
+// stays below 2^24 in magnitude: a run between flushes holds at most
+// 4 * kFlushVecs = 8192 terms a lane, so at most 2^20.  Three more packed
+// operations a pixel pair (the negated difference, the fma, the add), all on
+// the FMA pipe; no further conversion.
+template <bool kSse>
+struct Sums16 {
     static constexpr uint32_t kBias = 0x4B000000u;
     static constexpr uint32_t kFlushVecs = 2048;
     static_assert(8 * kFlushVecs <= SplitSum2::kMaxTerms, "SplitSum2 run bound");
+    static_assert(4 * kFlushVecs * 128 <= (1u << 24), "fp32 error sums stay exact");
     SplitSum2 rsq_;
     u64 noise = 0, rss = 0, dss = 0, sr = 0, sd = 0;
+    long long err = 0;  // sum of fl(D * D) - D * D (kSse)
+    f32x2 err_ = 0;     // the current run of it, two fp32 lanes
     uint32_t r_ = 0, d_ = 0;
 
     __device__ __forceinline__ void pair(f32x2 xr, f32x2 xd) {
         const f32x2 two23 = ((f32x2)kBias << 32) | kBias;
         uint32_t t0, t1;
-        f2_unpack(f2_square(f2_sub(xr, xd)), t0, t1);
+        const f32x2 diff = f2_sub(xr, xd);
+        const f32x2 sq = f2_square(diff);
+        f2_unpack(sq, t0, t1);
         noise += (u64)__float2uint_rn(__uint_as_float(t0)) + __float2uint_rn(__uint_as_float(t1));
+        if constexpr (kSse) err_ = f2_add(err_, f2_fma(f2_sub(xd, xr), diff, sq));
         const f32x2 fr = f2_sub(xr, two23);
         rsq_.add(f2_square(fr));
         uint32_t q0, q1;
@@ -420,8 +456,15 @@ struct TermSums<16> {
         sd += d_;
         r_ = d_ = 0;
         rss += rsq_.drain();
+        if constexpr (kSse) {
+            uint32_t e0, e1;
+            f2_unpack(err_, e0, e1);
+            err += (long long)small_float_to_int(__uint_as_float(e0)) +
+                   small_float_to_int(__uint_as_float(e1));
+            err_ = 0;
+        }
     }
-    __device__ __forceinline__ void totals(u64 (&t)[6]) {
+    __device__ __forceinline__ void totals(u64 (&t)[kWords]) {
         flush();
         t[0] = noise;
         t[1] = sr;
@@ -429,8 +472,16 @@ struct TermSums<16> {
         t[3] = rss;
         t[4] = dss;
         t[5] = 0;
+        t[6] = (u64)(-err);  // SSE - noise
+        t[7] = 0;
     }
 };
+
+template <>
+struct TermSums<16> : Sums16<false> {};
+
+// The 16-bit form that also carries the integer psnr's SSE (record word 6).
+struct TermSums16Sse : Sums16<true> {};
 
 // Integer psnr at 16 bits: the exact sum of (r - d)^2 (each below 2^32) in a
 // 64-bit integer.  Per 32-bit word one packed absolute difference gives the
@@ -458,46 +509,47 @@ struct SseSums16 {
         sse += (u64)e * e;
     }
     __device__ __forceinline__ void flush() {}
-    __device__ __forceinline__ void totals(u64 (&t)[6]) {
+    __device__ __forceinline__ void totals(u64 (&t)[kWords]) {
         t[0] = sse;
-        t[1] = t[2] = t[3] = t[4] = t[5] = 0;
+        t[1] = t[2] = t[3] = t[4] = t[5] = t[6] = t[7] = 0;
     }
 };
 
 // ---------------------------------------------------------------- reduction
-// Warp shuffles, then one value per warp through shared memory, then warp 0.
-// Integer sums: exact and independent of the order.
+// Warp shuffles, then one value per warp through shared memory, then warp 0:
+// words 0..4, 6 and 7 of a record are added, word 5 ORed.  Integer sums:
+// exact and independent of the order.
+__device__ __forceinline__ u64 combine(int k, u64 a, u64 b) { return k == 5 ? (a | b) : a + b; }
+
 template <int NT>
-__device__ __forceinline__ void block_reduce_store(u64 (&t)[6], u64 *dst) {
+__device__ __forceinline__ void block_reduce_store(u64 (&t)[kWords], u64 *dst) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-        for (int k = 0; k < 5; k++) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
-        t[5] |= __shfl_xor_sync(0xffffffffu, t[5], o);
+        for (int k = 0; k < kWords; k++) t[k] = combine(k, t[k], __shfl_xor_sync(0xffffffffu, t[k], o));
     }
     constexpr int kWarps = NT / 32;
-    __shared__ u64 s[kWarps][6];
+    __shared__ u64 s[kWarps][kWords];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 6; k++) s[warp][k] = t[k];
+        for (int k = 0; k < kWords; k++) s[warp][k] = t[k];
     }
     __syncthreads();
     if (warp == 0) {
-        u64 y[6];
+        u64 y[kWords];
 #pragma unroll
-        for (int k = 0; k < 6; k++) y[k] = lane < kWarps ? s[lane][k] : 0ull;
+        for (int k = 0; k < kWords; k++) y[k] = lane < kWarps ? s[lane][k] : 0ull;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-            for (int k = 0; k < 5; k++) y[k] += __shfl_xor_sync(0xffffffffu, y[k], o);
-            y[5] |= __shfl_xor_sync(0xffffffffu, y[5], o);
+            for (int k = 0; k < kWords; k++) y[k] = combine(k, y[k], __shfl_xor_sync(0xffffffffu, y[k], o));
         }
         u64 mine = 0;
 #pragma unroll
-        for (int k = 0; k < 6; k++)
+        for (int k = 0; k < kWords; k++)
             if (lane == k) mine = y[k];
-        if (lane < 6) dst[lane] = mine;
+        if (lane < kWords) dst[lane] = mine;
     }
 }
 
@@ -530,7 +582,7 @@ __global__ void __launch_bounds__(kThreads)
             acc.flush();
         }
     }
-    u64 t[6];
+    u64 t[kWords];
     acc.totals(t);
     block_reduce_store<kThreads>(t, partials[(size_t)f * segs + s].v);
 }
@@ -541,27 +593,28 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 }
 
-// A warp's totals, reduced and spread over its lanes: t[0..4] summed, t[5]
-// ORed.  The sums take a reduce-scatter over eight slots (t[0..4] and three
-// zeros): at each of the first three halvings a lane sends its partner the
-// half of its slots the partner keeps, so 18 shuffles do the work of 60.
-// Afterwards lane L holds the sum of slot (L >> 2) & 7 (in all four lanes of
-// its group); the OR of t[5] (two 32-bit warp reductions) is in every lane.
+// A warp's totals, reduced and spread over its lanes: the sums (words 0..4
+// and 6 of a record) added, word 5 ORed.  The sums take a reduce-scatter over
+// eight slots (words 0..4, word 6 and two zeros): at each of the first three
+// halvings a lane sends its partner the half of its slots the partner keeps,
+// so 18 shuffles do the work of 30 (six sums, five halvings each).  Afterwards lane L holds the sum of slot
+// (L >> 2) & 7 (in all four lanes of its group); the OR of word 5 (two 32-bit
+// warp reductions) is in every lane.  Word 7 is 0 in every accumulator.
 struct WarpTotals {
     u64 sum;    // slot (lane >> 2) & 7
-    u64 flags;  // OR of t[5]
+    u64 flags;  // OR of word 5
 };
 
-__device__ __forceinline__ WarpTotals warp_reduce_scatter(const u64 (&t)[6]) {
+__device__ __forceinline__ WarpTotals warp_reduce_scatter(const u64 (&t)[kWords]) {
     const int lane = threadIdx.x & 31;
     WarpTotals w;
     w.flags = ((u64)__reduce_or_sync(0xffffffffu, (uint32_t)(t[5] >> 32)) << 32) |
               __reduce_or_sync(0xffffffffu, (uint32_t)t[5]);
     const bool up16 = lane & 16, up8 = lane & 8, up4 = lane & 4;
-    u64 a[4];  // lanes below 16: slots 0..3; from 16: slots 4..7 = t[4], 0, 0, 0
+    u64 a[4];  // lanes below 16: slots 0..3; from 16: slots 4..7 = t[4], t[6], 0, 0
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const u64 lo = t[i], hi = i == 0 ? t[4] : 0ull;
+        const u64 lo = t[i], hi = i == 0 ? t[4] : i == 1 ? t[6] : 0ull;
         a[i] = (up16 ? hi : lo) + __shfl_xor_sync(0xffffffffu, up16 ? lo : hi, 16);
     }
     u64 b[2];
@@ -575,27 +628,36 @@ __device__ __forceinline__ WarpTotals warp_reduce_scatter(const u64 (&t)[6]) {
     return w;
 }
 
-// One warp's totals to one record (lanes 0, 4, .., 20 store a word each).
+// The record word a lane group of warp_reduce_scatter writes, and its value:
+// slots 0..4 are words 0..4, slot 5 is word 6, slot 6 carries the OR (word
+// 5), slot 7 the zero sum (word 7).
+__device__ __forceinline__ int slot_word(int slot) { return slot == 5 ? 6 : slot == 6 ? 5 : slot; }
+__device__ __forceinline__ u64 slot_value(int slot, const WarpTotals &w) {
+    return slot == 6 ? w.flags : w.sum;
+}
+
+// One warp's totals to one record (lanes 0, 4, .., 28 store a word each).
 // No other warp takes part, so no warp waits at the end of a unit.
-__device__ __forceinline__ void warp_reduce_store(const u64 (&t)[6], u64 *dst) {
+__device__ __forceinline__ void warp_reduce_store(const u64 (&t)[kWords], u64 *dst) {
     const WarpTotals w = warp_reduce_scatter(t);
     const int lane = threadIdx.x & 31, slot = (lane >> 2) & 7;
-    if ((lane & 3) == 0 && slot < 6) dst[slot] = slot < 5 ? w.sum : w.flags;
+    if ((lane & 3) == 0) dst[slot_word(slot)] = slot_value(slot, w);
 }
 
 // The consumer warps' totals reduced to one record: each warp's totals
-// through shared memory (warp_reduce_scatter), then lanes 0..5 of warp 0 add
+// through shared memory (warp_reduce_scatter), then lanes 0..7 of warp 0 add
 // (or OR) one word each over the warps.  Only consumer threads take part
 // (named barrier 1), so the producer lane keeps streaming meanwhile.
 template <int NCW>
-__device__ __forceinline__ void consumer_reduce_store(const u64 (&t)[6], u64 (*scratch)[6], u64 *dst) {
+__device__ __forceinline__ void consumer_reduce_store(const u64 (&t)[kWords], u64 (*scratch)[kWords],
+                                                      u64 *dst) {
     const WarpTotals w = warp_reduce_scatter(t);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, slot = (lane >> 2) & 7;
-    if ((lane & 3) == 0 && slot < 6) scratch[warp][slot] = slot < 5 ? w.sum : w.flags;
+    if ((lane & 3) == 0) scratch[warp][slot_word(slot)] = slot_value(slot, w);
     consumer_sync<NCW>();
-    if (warp == 0 && lane < 6) {
+    if (warp == 0 && lane < kWords) {
         u64 y = 0;
-        for (int k = 0; k < NCW; k++) y = lane < 5 ? y + scratch[k][lane] : (y | scratch[k][lane]);
+        for (int k = 0; k < NCW; k++) y = combine(lane, y, scratch[k][lane]);
         dst[lane] = y;
     }
     consumer_sync<NCW>();  // scratch is reused by the next unit
@@ -628,7 +690,7 @@ __global__ void __launch_bounds__(32 * kFrameWarps)
             for (; c < stop; c += 32) acc.vec(ld_stream16(r + 16 * (size_t)c), ld_stream16(d + 16 * (size_t)c));
             acc.flush();
         }
-        u64 t[6];
+        u64 t[kWords];
         acc.totals(t);
         warp_reduce_store(t, partials[f].v);
     }
@@ -821,7 +883,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     constexpr uint32_t kStagesPerFlush = Acc::kFlushVecs / kPerThread;
     extern __shared__ __align__(128) unsigned char ring[];  // [STAGES][2][kStageBytes]
     __shared__ __align__(8) u64 full[STAGES], empty[STAGES];
-    __shared__ u64 red[NCW][6];
+    __shared__ u64 red[NCW][kWords];
 
     allow_dependent_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -901,7 +963,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
                 since_flush = 0;
             }
         }
-        u64 t[6];
+        u64 t[kWords];
         acc.totals(t);
         t[5] |= err;
         // The same before the first record store (the kernel ahead may still
@@ -926,12 +988,11 @@ __global__ void __launch_bounds__(kSumThreads)
     allow_dependent_launch();  // the next batch's stage 1 may start on free SMs
     grid_dependency_wait();
     const int f = blockIdx.x;
-    u64 t[6] = {0, 0, 0, 0, 0, 0};
+    u64 t[kWords] = {0, 0, 0, 0, 0, 0, 0, 0};
     for (int s = threadIdx.x; s < per_frame; s += kSumThreads) {
         const Partial &p = partials[(size_t)f * per_frame + s];
 #pragma unroll
-        for (int k = 0; k < 5; k++) t[k] += p.v[k];
-        t[5] |= p.v[5];
+        for (int k = 0; k < kWords; k++) t[k] = combine(k, t[k], p.v[k]);
     }
     block_reduce_store<kSumThreads>(t, out[f].v);
 }

@@ -56,14 +56,18 @@ enum Path { kDense = 0, kTiles = 1, kRowsScalar = 2, kRows = 3, kFrames = 4, kPa
 constexpr uint32_t kFramesMaxVecs = 1024;  // 16 KB of each plane
 constexpr size_t kRowsMinBytes = 512;
 
-// What a call computes: the fused statistics, or the integer psnr.  Up to 12
-// bits the integer psnr's SSE is the fused pass's noise sum (its squares are
-// exact), so only 16 bits has a kernel variant of its own.
-enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2, kOrdered = 3, kHvs = 4 };
-constexpr int kVariants = 5;  // fused 8, 10, 12, 16 bits; integer psnr 16 bits
+// What a call computes: the fused statistics, the integer psnr, or both from
+// one read (kScores).  Up to 12 bits the integer psnr's SSE is the fused
+// pass's noise sum (its squares are exact), so only 16 bits has kernel
+// variants of its own: the SSE alone, and the fused statistics carrying the
+// SSE as well.
+enum Kind { kStats = 0, kIntPsnr = 1, kPlanes = 2, kOrdered = 3, kHvs = 4, kScores = 5 };
+// fused 8, 10, 12, 16 bits; integer psnr 16 bits; fused with the SSE, 16 bits
+constexpr int kVariants = 6;
 
 int variant_index(int bpc, int kind) {  // kPlanes runs the fused statistics
     if (kind == kIntPsnr && bpc == 16) return 4;
+    if (kind == kScores && bpc == 16) return 5;
     return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3;
 }
 
@@ -167,7 +171,8 @@ Stage1Shape stage1_shape(int path, int variant) {
     case 1: return stage1_shape<10, vqx::TermSums<10>>(path);
     case 2: return stage1_shape<12, vqx::TermSums<12>>(path);
     case 3: return stage1_shape<16, vqx::TermSums<16>>(path);
-    default: return stage1_shape<16, vqx::SseSums16>(path);
+    case 4: return stage1_shape<16, vqx::SseSums16>(path);
+    default: return stage1_shape<16, vqx::TermSums16Sse>(path);
     }
 }
 
@@ -665,8 +670,10 @@ cudaError_t launch_stage1(const Plan &p, const void *ref, const void *dist, int 
                                                        planes_ready);
     case 3: return launch_stage1_bpc<16, vqx::TermSums<16>>(p, r, d, frame0, frames, partials, st, overlap,
                                                        planes_ready);
-    default: return launch_stage1_bpc<16, vqx::SseSums16>(p, r, d, frame0, frames, partials, st, overlap,
+    case 4: return launch_stage1_bpc<16, vqx::SseSums16>(p, r, d, frame0, frames, partials, st, overlap,
                                                        planes_ready);
+    default: return launch_stage1_bpc<16, vqx::TermSums16Sse>(p, r, d, frame0, frames, partials, st,
+                                                              overlap, planes_ready);
     }
 }
 
@@ -735,16 +742,18 @@ int merge_status_flags(int rc, uint32_t flags) {
 
 int merge_status(int rc, const vqx_frame_stats &f) { return merge_status_flags(rc, f.flags); }
 
-// Integer psnr of one frame from its record: slot 0 is the exact SSE (the
-// integer-psnr kernel's sum at 16 bits, the fused pass's noise sum below,
-// where the float squares are the integer squares).  MSE = SSE / N, one
-// division; PSNR = 10 log10(peak^2 / MSE), peak = 2^bpc - 1, capped as
-// float_psnr is.
+// Integer psnr of one frame from its record: the exact SSE is word 0 plus
+// word 6 (the integer-psnr kernel's sum and 0 at 16 bits; the fused pass's
+// noise sum and 0 up to 12 bits, where the float squares are the integer
+// squares; the float noise sum and the exact difference to the SSE from the
+// fused pass that carries it).  MSE = SSE / N, one division; PSNR =
+// 10 log10(peak^2 / MSE), peak = 2^bpc - 1, capped as float_psnr is.
 void conclude_int_psnr(const Partial &s, int bpc, int width, int height, vqx_int_psnr_stats *o) {
-    o->sse = s.v[0];
+    const u64 sse = s.v[0] + s.v[6];
+    o->sse = sse;
     o->flags = record_flags(s, bpc);
     o->reserved = 0;
-    o->mse = (double)s.v[0] / ((double)width * (double)height);
+    o->mse = (double)sse / ((double)width * (double)height);
     const double peak = (double)((1u << bpc) - 1);
     o->psnr_uncapped = 10.0 * log10(peak * peak / o->mse);
     const double cap = vqx_psnr_cap(bpc);
@@ -878,14 +887,15 @@ int submit_impl(const void *ref, const void *dist, int width, int height, size_t
 }
 
 // Waits for a batch, concludes it into out (vqx_frame_stats or
-// vqx_int_psnr_stats records, as kind says) and releases the handle.
-int finish_impl(vqx_pending *p, int kind, void *out) {
+// vqx_int_psnr_stats records, as kind says; kScores: both, into out and
+// out2) and releases the handle.
+int finish_impl(vqx_pending *p, int kind, void *out, void *out2 = nullptr) {
     if (!p) return VQX_OK;
     int rc = VQX_OK;
     const cudaError_t e = cudaEventSynchronize(p->done);
     if (e != cudaSuccess) {
         rc = cuda_status(e);
-    } else if (!out || p->kind != kind) {
+    } else if (!out || p->kind != kind || (kind == kScores && !out2)) {
         rc = VQX_EINVAL;
     } else {
         t_prof.totals.calls++;
@@ -917,6 +927,7 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
                 s_f.v[3] = o[4];  // exact squares
                 s_f.v[4] = o[5];
                 s_f.v[5] = 0;  // 16 bits: no sample out of range; no device wait to time out
+                s_f.v[6] = s_f.v[7] = 0;
                 vqx_frame_stats &r = ((vqx_frame_stats *)out)[f];
                 conclude(s_f, p->bpc, p->width, p->height, &r, o);
                 rc = merge_status(rc, r);
@@ -930,6 +941,11 @@ int finish_impl(vqx_pending *p, int kind, void *out) {
             }
         } else if (kind == kStats) {
             rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
+        } else if (kind == kScores) {
+            rc = conclude_all(sums, p->n_frames, p->bpc, p->width, p->height, (vqx_frame_stats *)out);
+            vqx_int_psnr_stats *o = (vqx_int_psnr_stats *)out2;
+            for (int f = 0; f < p->n_frames; f++)
+                conclude_int_psnr(sums[f], p->bpc, p->width, p->height, &o[f]);
         } else if (kind == kPlanes) {
             vqx_frame_stats *o = (vqx_frame_stats *)out;
             for (int q = 0; q < p->n_planes; q++)
@@ -981,6 +997,30 @@ int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int 
 
 int vqx_plane_int_psnr_finish(vqx_pending *pending, vqx_int_psnr_stats *out) {
     return finish_impl(pending, kIntPsnr, out);
+}
+
+int vqx_plane_scores_submit(const void *ref, const void *dist, int width, int height,
+                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                            unsigned flags, vqx_pending **pending) {
+    return submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kScores, flags,
+                       pending);
+}
+
+int vqx_plane_scores_finish(vqx_pending *pending, vqx_frame_stats *out,
+                            vqx_int_psnr_stats *int_out) {
+    return finish_impl(pending, kScores, out, int_out);
+}
+
+int vqx_plane_scores(const void *ref, const void *dist, int width, int height, size_t stride,
+                     int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out,
+                     vqx_int_psnr_stats *int_out) {
+    int rc = validate(ref, dist, width, height, stride, bpc, n_frames, out);
+    if (rc != VQX_OK || n_frames == 0) return rc;
+    if (!int_out) return VQX_EINVAL;
+    vqx_pending *p = nullptr;
+    rc = submit_impl(ref, dist, width, height, stride, bpc, n_frames, stream, kScores, 0u, &p);
+    if (rc != VQX_OK) return rc;
+    return finish_impl(p, kScores, out, int_out);
 }
 
 int vqx_plane_int_psnr(const void *ref, const void *dist, int width, int height, size_t stride,
@@ -1374,7 +1414,7 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
     // clearing between calls.
     e = launch_stage1(plan, ref, dist, 0, n_frames, partials, st);
     if (e == cudaSuccess) e = launch_stage2(plan, n_frames, partials, sums, st);
-    // The sums (48 bytes a frame) land in the front of the caller's array,
+    // The sums (64 bytes a frame) land in the front of the caller's array,
     // which has 112 bytes a frame; they are concluded in place below.
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(out, sums, (size_t)n_frames * sizeof(Partial), cudaMemcpyDeviceToHost, st);
@@ -1383,6 +1423,9 @@ extern "C" int vqx_plane_stats_noalloc(const void *ref, const void *dist, int wi
     if (e != cudaSuccess) return cuda_status(e);
     // Last frame first: record f starts at byte 112 f, at or after the sums of
     // every frame below f, so no sums are overwritten before they are read.
+    // That holds only while a record is at least as large as a frame's sums.
+    static_assert(sizeof(vqx_frame_stats) >= sizeof(Partial),
+                  "in-place conclusion needs records at least as large as the sums");
     rc = VQX_OK;
     for (int f = n_frames - 1; f >= 0; f--) {
         Partial s_f;

@@ -204,6 +204,10 @@ WORKLOADS = {
 }
 
 HEADLINE = "3840x2160_16bit_x32"
+# The measured configurations, in order: the Netflix-sized 8-bit pair, 1080p
+# 10-bit, 4K 12-bit, 1080p 16-bit and the 4K 16-bit headline batch.
+BENCH_CONFIGS = ("576x324_8bit_x1", "1920x1080_10bit_x48", "3840x2160_12bit_x32",
+                 "1920x1080_16bit_x64", "3840x2160_16bit_x32")
 
 
 # ---------------------------------------------------------------- psnr_hvs terms

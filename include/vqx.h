@@ -43,6 +43,8 @@
  *                              also past 2^53 units
  *   vqx_plane_stats_noalloc    no allocation at call time (fixed scratch)
  *   vqx_plane_int_psnr (+ _submit / _finish)   the integer psnr
+ *   vqx_plane_scores (+ _submit / _finish)     the fused statistics and the
+ *                              integer psnr from one read of the planes
  *   vqx_psnr_hvs_sum (+ _submit / _finish)     psnr_hvs plane sums of given
  *                              terms, the CPU's sequential float sum
  *   vqx_psnr_cap, vqx_status_string, vqx_last_cuda_error,
@@ -245,6 +247,37 @@ int vqx_plane_int_psnr_submit(const void *ref, const void *dist, int width, int 
 int vqx_plane_int_psnr_finish(vqx_pending *pending, vqx_int_psnr_stats *out);
 
 /*
+ * vqx_plane_scores: float_psnr, float_moment and the integer psnr of every
+ * frame from one read of the planes.  "ADR-1440: float_psnr_hip adds its
+ * squared differences as integers ..." (Alternatives) sets psnr_hip's one
+ * uint64 per frame beside float_psnr's integer sums; both are sums over the
+ * same sample pairs, so one pass forms both.
+ *
+ * out receives exactly what vqx_plane_stats returns, int_out exactly what
+ * vqx_plane_int_psnr returns (both host arrays of n_frames records,
+ * caller-owned; int_out may not be NULL when n_frames > 0).  Up to 12 bits
+ * the SSE is the noise sum itself (the float squares are the integer
+ * squares there); at 16 bits the fused kernel also adds up, exactly, the
+ * rounding error of every float noise square (one fused multiply-add a
+ * pixel), and SSE = noise sum - the sum of those errors.  Arguments, layout,
+ * ownership and status codes (one status for both arrays) as for
+ * vqx_plane_stats; synchronous on return.
+ */
+int vqx_plane_scores(const void *ref, const void *dist, int width, int height, size_t stride,
+                     int bpc, int n_frames, vqx_stream_t stream, vqx_frame_stats *out,
+                     vqx_int_psnr_stats *int_out);
+
+/* The same in two halves, as vqx_plane_stats_submit / _finish (flags, the
+ * planes' lifetime and the handle's rules alike; a handle of another pair is
+ * refused with VQX_EINVAL and released, and so is a NULL out or int_out). */
+int vqx_plane_scores_submit(const void *ref, const void *dist, int width, int height,
+                            size_t stride, int bpc, int n_frames, vqx_stream_t stream,
+                            unsigned flags, vqx_pending **pending);
+
+int vqx_plane_scores_finish(vqx_pending *pending, vqx_frame_stats *out,
+                            vqx_int_psnr_stats *int_out);
+
+/*
  * vqx_plane_stats_host: the same results for planes in host memory.  The
  * frames are copied to the device in chunks on an internal copy stream while
  * earlier chunks are reduced on `stream` (copy and compute overlap); pinned
@@ -324,8 +357,8 @@ void vqx_profile_read(vqx_profile *out, int reset);
 
 /*
  * Records held by the static scratch of vqx_plane_stats_noalloc: 65536
- * records of 48 bytes (3 MiB of device memory on every GPU that loads the
- * library, held until the process exits).
+ * records of 64 bytes (4 MiB of device memory on every GPU the library's
+ * device code is loaded on, held until the process exits).
  */
 #define VQX_NOALLOC_MAX_RECORDS 65536
 
@@ -337,10 +370,18 @@ void vqx_profile_read(vqx_profile *out, int reset);
  * pipeline whose frame deadline cannot absorb a device or pinned allocation
  * (these can take driver locks or wait for the device), or a host
  * application that hands all of the GPU's memory to its own allocator and
- * lets no library take memory behind its back.  This entry point allocates
- * nothing, in any call, the first one included: its scratch is a
- * fixed-size array in the library's device memory, and the per-frame sums
- * are copied straight into `out`.
+ * lets no library take memory behind its back.  Its calls allocate nothing:
+ * its scratch is a fixed-size array in the library's device memory, and the
+ * per-frame sums are copied straight into `out`.
+ *
+ * That array is reserved when the library's device code is loaded on a
+ * device: with CUDA's default lazy module loading, during the first call on
+ * that device that needs it (of this entry point, or of any other vqx entry
+ * point), or when the CUDA context is created if the process runs with
+ * CUDA_MODULE_LOADING=EAGER.  A caller whose own allocator takes all of the
+ * GPU's memory should therefore make one call of this entry point (any
+ * valid batch) before its allocator takes the memory; later calls then have
+ * nothing to reserve.
  *
  * Arguments, results and status codes are those of vqx_plane_stats.  The
  * batch may hold at most VQX_NOALLOC_MAX_RECORDS / 2 frames; a larger
@@ -348,9 +389,13 @@ void vqx_profile_read(vqx_profile *out, int reset);
  * may be split into fewer segments than vqx_plane_stats uses, so a batch of
  * many frames can run somewhat slower; the results are identical.
  *
- * The first call on each device (with that device current) looks up the
- * scratch array's device address; make that first call before any stream
- * capture.  Every call uses the same scratch array, which keeps the last
+ * The first call on each device (with that device current) also looks up the
+ * scratch array's device address and sets the kernels' attributes.  Every
+ * call ends by copying the sums into `out` (pageable host memory) and
+ * waiting for `stream`: it is synchronous, and it cannot be captured into a
+ * CUDA graph.  Make the first call before any other thread begins a stream
+ * capture in global mode, which the set-up's calls would disturb.  Every
+ * call uses the same scratch array, which keeps the last
  * call's contents; nothing in it needs to start at zero, because every
  * record is written before it is read.  Two calls whose work overlaps on the
  * GPU (calls on different streams, or from different threads, at the same

@@ -23,7 +23,7 @@
  *    double total of the scaled samples and one of their float squares per
  *    plane, each divided by the number of pixels at the end.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *  - the row-by-row accumulation is one double accumulator walked in raster order;
  *  - MSE = noise / (w * h); PSNR = 10 log10(255^2 / MSE);
  *  - the PSNR cap is 6 * bpc + 12 dB (60, 72, 84, 108), applied as a min; the
@@ -179,7 +179,7 @@ int vqx_oracle_units_frame(const void *ref, const void *dist, int w, int h, size
  * Integer psnr, the integer sibling of float_psnr.  "ADR-1440: float_psnr_hip
  * adds its squared differences as integers ..." (Alternatives) names its HIP
  * twin, psnr_hip, as keeping one uint64 per frame; the pages give no formula
- * beyond that.  Readings taken (also listed in the design notes):
+ * beyond that.  Readings taken:
  *  - SSE = the sum over pixels of (r - d)^2, raw samples at their own depth,
  *    in uint64 (exact: at most 2^25 (2^16 - 1)^2 < 2^57);
  *  - MSE = SSE / (w * h), one double division of the converted SSE;
@@ -258,7 +258,7 @@ int vqx_oracle_batch(const void *ref, const void *dist, int w, int h, size_t str
  * operation, rounded to nearest even, subnormals kept.
  *
  * The terms themselves (transform, CSF and masking) are not on the pages;
- * here they are the input.  Readings taken (also listed in the design notes):
+ * here they are the input.  Readings taken:
  *  - the two divisions happen in the order the page names them: first by the
  *    term count converted to float, then by the squared maximum;
  *  - the squared maximum is the float product of (2^bpc - 1) with itself.

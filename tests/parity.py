@@ -43,9 +43,24 @@ def place(ref, dist, stride=None, offset_ref=0, offset_dist=0):
     return (tr, td), pr, pd, stride, (rb, db)
 
 
-def compare(rec, sc, un, bpc, pixels):
-    """Assert the GPU records ``rec`` match the oracle's ``sc``/``un``."""
+def range_flags(ref, dist, bpc):
+    """Per frame, 1 where a sample of either plane (n, h, w) is 2^bpc or more
+    (the library's VQX_FLAG_RANGE), else 0."""
+    top = (1 << bpc) - 1
+    n = ref.shape[0]
+    over = (ref.reshape(n, -1) > top).any(axis=1) | (dist.reshape(n, -1) > top).any(axis=1)
+    return [int(x) for x in over]
+
+
+def compare(rec, sc, un, bpc, pixels, planes=None):
+    """Assert the GPU records ``rec`` match the oracle's ``sc``/``un``.
+
+    ``planes``: the (ref, dist) sample arrays (n, h, w) the records come
+    from; the range flag of each frame must then be set exactly where a
+    sample is 2^bpc or more.  Without them every frame's flags must be 0 (the
+    callers pass in-range samples)."""
     assert len(rec) == len(sc) == len(un)
+    want_flags = range_flags(planes[0], planes[1], bpc) if planes is not None else [0] * len(rec)
     for f in range(len(rec)):
         g, s, u = rec[f], sc[f], un[f]
         for k in UNIT_FIELDS:
@@ -70,8 +85,7 @@ def compare(rec, sc, un, bpc, pixels):
                 bound = oracle.moment_bound(pixels, oracle.binade(units))
                 assert abs(g[plane + "_meansq"] - s[plane + "_meansq"]) <= bound
         # and the flags: only out-of-range samples set one
-        top = (1 << bpc) - 1
-        assert int(g["flags"]) in (0, 1)
+        assert int(g["flags"]) == want_flags[f], (f, int(g["flags"]), want_flags[f])
     return True
 
 

@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
               "vqx_plane_stats_ordered_submit", "vqx_plane_stats_ordered_finish",
               "vqx_plane_int_psnr_submit", "vqx_plane_int_psnr_finish", "vqx_status_string",
               "vqx_last_cuda_error", "vqx_psnr_cap", "vqx_profile_enable", "vqx_profile_read",
-              "vqx_psnr_hvs_sum", "vqx_psnr_hvs_sum_submit", "vqx_psnr_hvs_sum_finish"):
+              "vqx_psnr_hvs_sum", "vqx_psnr_hvs_sum_submit", "vqx_psnr_hvs_sum_finish",
+              "vqx_plane_scores", "vqx_plane_scores_submit", "vqx_plane_scores_finish"):
         assert n in names
 
 
@@ -144,6 +145,41 @@ def test_planes_argument_errors_need_no_gpu(lib):
     assert so.vqx_planes_stats_submit(arr, 2, 16, 2, None, 4, ctypes.byref(handle)) == -1
     assert so.vqx_planes_stats_submit(arr, 2, 16, 0, None, 0, ctypes.byref(handle)) == 0
     assert handle.value is None and so.vqx_planes_stats_finish(None, None) == 0
+
+
+@pytest.mark.parametrize("args,status", [(dict(bpc=9), -2), (dict(width=0), -1), (dict(ref=0), -1),
+                                         (dict(stride=2 * 64 + 1), -1), (dict(n_frames=-2), -1),
+                                         (dict(width=8192, height=4097, stride=8192 * 2), -1)])
+def test_scores_argument_errors_need_no_gpu(lib, args, status):
+    a = dict(ref=FAKE, dist=FAKE, width=64, height=4, stride=128, bpc=16, n_frames=2)
+    a.update(args)
+    so = lib.library()
+    out = (ctypes.c_char * (112 * 2))()
+    ints = (ctypes.c_char * (40 * 2))()
+    rc = so.vqx_plane_scores(a["ref"] or None, a["dist"] or None, a["width"], a["height"], a["stride"],
+                             a["bpc"], a["n_frames"], None, out, ints)
+    assert rc == status
+    handle = ctypes.c_void_p(1234)
+    rc = so.vqx_plane_scores_submit(a["ref"] or None, a["dist"] or None, a["width"], a["height"],
+                                    a["stride"], a["bpc"], a["n_frames"], None, 0, ctypes.byref(handle))
+    assert rc == status and handle.value is None
+
+
+def test_scores_outputs_and_empty_batches_without_gpu(lib):
+    so = lib.library()
+    out = (ctypes.c_char * 112)()
+    ints = (ctypes.c_char * 40)()
+    # either output missing: refused before anything runs
+    assert so.vqx_plane_scores(FAKE, FAKE, 4, 4, 8, 16, 1, None, None, ints) == -1
+    assert so.vqx_plane_scores(FAKE, FAKE, 4, 4, 8, 16, 1, None, out, None) == -1
+    # empty batches touch nothing and need no outputs
+    assert so.vqx_plane_scores(None, None, 0, 0, 0, 16, 0, None, None, None) == 0
+    handle = ctypes.c_void_p(1234)
+    assert so.vqx_plane_scores_submit(None, None, 0, 0, 0, 10, 0, None, 0, ctypes.byref(handle)) == 0
+    assert handle.value is None and so.vqx_plane_scores_finish(None, None, None) == 0
+    assert so.vqx_plane_scores_submit(FAKE, FAKE, 4, 4, 8, 16, 1, None, 2, ctypes.byref(handle)) == -1
+    stats, ip = lib.vqx_plane_scores(np.zeros((0, 4, 4), np.uint16), np.zeros((0, 4, 4), np.uint16))
+    assert stats.size == 0 and ip.size == 0
 
 
 def test_empty_batch_is_ok_without_gpu(lib):

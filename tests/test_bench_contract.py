@@ -56,3 +56,14 @@ def test_library_arm_line():
         assert k in d["clocks"], k
     # two launches a step (the fused pass and the per-frame sums)
     assert d["gpu_launches"] == 2 * d["steps"]
+    # the median of repeated regions, with its spread
+    t = d["timing"]
+    assert t["repeats"] >= 21
+    assert t["region_ms"]["min_ms"] <= t["region_ms"]["median_ms"] <= t["region_ms"]["max_ms"]
+    assert abs(d["ms_per_step"] - t["region_ms"]["median_ms"] / d["steps"]) < 1e-9
+    # the other measured configurations, timed in the same run
+    from exact_full_reference_gb300 import workloads as wl
+
+    assert sorted(d["configs"]) == sorted(c for c in wl.BENCH_CONFIGS if c != wl.HEADLINE)
+    for name, c in d["configs"].items():
+        assert c["value"] > 0 and c["repeats"] >= 21 and 0 < c["kernel_frac"] < 1.5, name

@@ -53,3 +53,17 @@ def test_single_process_needs_no_group():
 
     assert bench.reduce_max(3.5) == 3.5
     assert bench.job_throughput(1, 32, 10, 2.0) == 160.0
+
+
+def test_repeats_fill_the_sampled_time():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # at least the minimum count; more when regions are short
+    assert bench.repeat_count(0.5, 21, 1.5) == 21
+    assert bench.repeat_count(0.003, 21, 1.5) == 500
+    assert bench.repeat_count(1e-6, 21, 1.5, cap=5000) == 5000
+    assert bench.repeat_count(0.0, 21, 1.5) == 21
+    s = bench.summarize_regions([3.0, 1.0, 2.0, 10.0, 4.0], 10)
+    assert s["repeats"] == 5 and s["median_ms"] == 3.0 and s["min_ms"] == 1.0 and s["max_ms"] == 10.0
+    assert s["ms_per_step"] == 0.3

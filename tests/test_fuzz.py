@@ -53,7 +53,7 @@ def test_fuzz_every_entry_point(lib, orc, seed):
     keep, pr, pd, stride, (rb, db) = parity.place(ref, dist, stride, off_r, off_d)
     sc, un = orc.batch(rb, db, w, h, stride, bpc, n)
     rec = lib.vqx_plane_stats(pr, pd, w, h, stride, bpc, n)
-    parity.compare(rec, sc, un, bpc, w * h)
+    parity.compare(rec, sc, un, bpc, w * h, planes=(ref, dist))
     # integer psnr
     ip = lib.vqx_plane_int_psnr(pr, pd, w, h, stride, bpc, n)
     want = orc.int_psnr(rb, db, w, h, stride, bpc, n)

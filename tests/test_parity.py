@@ -28,7 +28,7 @@ def run_case(lib, orc, ref, dist, bpc, stride=None, offset_ref=0, offset_dist=0)
     rec = lib.vqx_plane_stats(pr, pd, w, h, stride, bpc, n)
     torch.cuda.synchronize()
     sc, un = orc.batch(rb, db, w, h, stride, bpc, n)
-    parity.compare(rec, sc, un, bpc, w * h)
+    parity.compare(rec, sc, un, bpc, w * h, planes=(ref, dist))
     return rec, sc, un
 
 

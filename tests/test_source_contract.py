@@ -89,12 +89,16 @@ def check_run_bounds(src):
     # 10 and 12 bits: 8 samples a vector into the 32-bit sample sums
     if f1012 * 8 * 0xFFFF > U32:
         problems.append("10/12-bit sample-sum runs overflow: %d vectors" % f1012)
-    f16 = constant(src, "struct TermSums<16> {", "kFlushVecs")
+    f16 = constant(src, "struct Sums16 {", "kFlushVecs")
     max_terms = constant(src, "struct SplitSum2 {", "kMaxTerms")
     if f16 * 8 * 0xFFFF > U32:
         problems.append("16-bit sample-sum runs overflow: %d vectors" % f16)
     if 8 * f16 > max_terms:
         problems.append("16-bit square runs exceed SplitSum2's bound")
+    # the SSE form's fp32 lanes add one rounding error (at most 128 in
+    # magnitude) per word of a vector: exact while below 2^24
+    if 4 * f16 * 128 > (1 << 24):
+        problems.append("16-bit rounding-error runs leave fp32's exact integers")
     # SplitSum2: sum(h) / 2^16 below 2^32 and |sum(l)| below 2^31
     if max_terms * (1 << 16) > U32 or max_terms * (1 << 15) >= (1 << 31):
         problems.append("SplitSum2 bound too large: %d terms" % max_terms)
@@ -174,7 +178,7 @@ def test_planted_oracle_flag_regressions_are_caught(plant):
 @pytest.mark.parametrize("struct_head,new", [
     ("struct TermSums<8> {", 8192),
     ("struct TermSums {", 16384),
-    ("struct TermSums<16> {", 8192),
+    ("struct Sums16 {", 8192),
 ], ids=["8-bit", "10-12-bit", "16-bit"])
 def test_planted_run_length_overflows_are_caught(struct_head, new):
     with open(KERNELS) as f:
@@ -184,6 +188,16 @@ def test_planted_run_length_overflows_are_caught(struct_head, new):
     k = src.index(";", j)
     planted = src[:j] + "kFlushVecs = %d" % new + src[k:]
     assert check_run_bounds(planted)
+
+
+def test_planted_error_run_overflow_is_caught():
+    with open(KERNELS) as f:
+        src = f.read()
+    i = src.index("struct Sums16 {")
+    j = src.index("kFlushVecs = ", i)
+    k = src.index(";", j)
+    planted = src[:j] + "kFlushVecs = 65536" + src[k:]
+    assert "16-bit rounding-error runs leave fp32's exact integers" in check_run_bounds(planted)
 
 
 def test_planted_split_bound_overflow_is_caught():

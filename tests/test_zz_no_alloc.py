@@ -4,9 +4,12 @@ It exists for callers that must not allocate once they run (a real-time
 pipeline whose frame budget cannot absorb an allocation that may take driver
 locks or wait for the GPU, or an application whose own allocator owns all of
 the GPU's memory).  It runs the same kernels as vqx_plane_stats with a fixed
-static scratch array, so its records must equal vqx_plane_stats' records
-exactly, call after call, even though the scratch keeps the previous call's
-contents.
+static scratch array, so its records must equal the oracle's, and
+vqx_plane_stats' records exactly, call after call, even though the scratch
+keeps the previous call's contents.  Batches large enough to leave the
+scratch short make every unit write one record instead of one per warp; two
+of the cases below take that branch, one of them at the largest batch the
+scratch holds.
 
 This file is collected last on purpose, so that a run stopping at the first
 failure has already run every other test.
@@ -14,6 +17,7 @@ failure has already run every other test.
 import numpy as np
 import pytest
 
+import parity
 from exact_full_reference_gb300 import workloads as wl
 
 
@@ -27,11 +31,31 @@ def test_noalloc_rejects_batches_beyond_its_scratch(lib):
     assert rc == lib.VQX_EINVAL
 
 
-@pytest.mark.gpu
-def test_noalloc_matches_the_allocating_entry_point(lib):
+def _need_gpu():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    return torch
+
+
+def _check(lib, orc, ref, dist, bpc, stride=None):
+    """One noalloc call on (n, h, w) planes: records equal to the oracle's and
+    to vqx_plane_stats'."""
+    torch = _need_gpu()
+    n, h, w = ref.shape
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist, stride)
+    got = lib.vqx_plane_stats_noalloc(pr, pd, w, h, stride, bpc, n)
+    torch.cuda.synchronize()
+    sc, un = orc.batch(rb, db, w, h, stride, bpc, n)
+    parity.compare(got, sc, un, bpc, w * h, planes=(ref, dist))
+    expect = lib.vqx_plane_stats(pr, pd, w, h, stride, bpc, n)
+    assert got.tobytes() == expect.tobytes()
+    return got
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle_and_the_allocating_entry_point(lib, orc):
+    _need_gpu()
     # Two calls in a row with different batches: the larger one first, so
     # that stale records from it would show up in the second call.
     cases = [
@@ -40,12 +64,26 @@ def test_noalloc_matches_the_allocating_entry_point(lib):
     ]
     for w, frames in cases:
         ref, dist = w.generate(frames)
-        n = ref.shape[0]
-        dr = torch.from_numpy(ref.reshape(-1).view(np.uint8)).cuda()
-        dd = torch.from_numpy(dist.reshape(-1).view(np.uint8)).cuda()
-        stride = w.width * w.bytes_per_sample
-        expect = lib.vqx_plane_stats(dr, dd, w.width, w.height, stride, w.bpc, n)
-        got = lib.vqx_plane_stats_noalloc(dr, dd, w.width, w.height, stride, w.bpc, n)
-        torch.cuda.synchronize()
-        # the tolerance of every parity test of the integer path: exact
-        assert got.tobytes() == expect.tobytes(), w.name
+        _check(lib, orc, ref, dist, w.bpc)
+
+
+@pytest.mark.gpu
+def test_noalloc_short_scratch_one_record_per_unit(lib, orc):
+    """The largest batch the scratch holds, VQX_NOALLOC_MAX_RECORDS / 2 =
+    32768 frames, of 64x2 16-bit frames on a padded pitch (the tile path, not
+    the warp-per-frame one): one record per frame is left for stage 1, so
+    every unit writes a single record.  Then 5000 dense 176x144 8-bit frames
+    (the bulk-copy path, 12 records a frame left) take the same branch.  A
+    small batch afterwards must not see either call's records."""
+    _need_gpu()
+    n = lib.VQX_NOALLOC_MAX_RECORDS // 2
+    rng = np.random.Generator(np.random.PCG64(4242))
+    ref = rng.integers(0, 65536, (n, 2, 64)).astype(np.uint16)
+    dist = rng.integers(0, 65536, (n, 2, 64)).astype(np.uint16)
+    _check(lib, orc, ref, dist, 16, stride=64 * 2 + 16)
+    ref = rng.integers(0, 256, (5000, 144, 176)).astype(np.uint8)
+    dist = np.clip(ref.astype(np.int64) + rng.integers(-9, 10, ref.shape), 0, 255).astype(np.uint8)
+    _check(lib, orc, ref, dist, 8)
+    w = wl.WORKLOADS["576x324_8bit_x1"]
+    ref, dist = w.generate()
+    _check(lib, orc, ref, dist, 8)
