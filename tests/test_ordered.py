@@ -132,3 +132,24 @@ def test_ordered_at_the_largest_frame(lib, orc):
     assert int(un[0]["ref_sumsq"]) > 1 << 55
     check_identical(rec, sc, un)
 
+
+
+@pytest.mark.parametrize("w,h,n", [(2048, 1026, 3), (2560, 1440, 2), (4096, 520, 5)])
+def test_ordered_whole_block_frames_and_partial_units(lib, orc, w, h, n):
+    """Dense frames of whole 4096-pixel blocks just above 2^21 pixels and
+    beyond: 2048 x 1026 (513 blocks a frame), 2560 x 1440 (900) and
+    4096 x 520 (520); bright samples, every other frame a plane against its
+    inverse.  Every double equals the oracle's, and the records equal those
+    of the same frames on a padded pitch (sample loads row by row)."""
+    rng = np.random.Generator(np.random.PCG64(w + h + n))
+    ref = rng.integers(50000, 1 << 16, (n, h, w), dtype=np.uint16)
+    dist = rng.integers(50000, 1 << 16, (n, h, w), dtype=np.uint16)
+    dist[::2] = 65535 - ref[::2]
+    keep, pr, pd, stride, (rb, db) = parity.place(ref, dist)
+    rec = lib.vqx_plane_stats_ordered(pr, pd, w, h, stride, 16, n)
+    sc, un = orc.batch(rb, db, w, h, stride, 16, n)
+    check_identical(rec, sc, un)
+    if w * h > 3_000_000:  # bright enough and large enough to pass 2^53 units
+        assert parity.exact_count(un) < n
+    keep2, pr2, pd2, stride2, _ = parity.place(ref, dist, stride=2 * w + 32)
+    assert lib.vqx_plane_stats_ordered(pr2, pd2, w, h, stride2, 16, n).tobytes() == rec.tobytes()
