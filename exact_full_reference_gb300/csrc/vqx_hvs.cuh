@@ -517,19 +517,38 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
 // estimate written; empty: the buffer read, the record's inputs kept) completes
 // one phase per use, parity (k / kHvsTmaStages) & 1.  Every wait is
 // bounded; a warp whose wait gives up waits for nothing more, and every node
-// record written after it carries kHvsFlagTimeout.
-constexpr int kHvsTmaStages = 6;
+// record written after it carries kHvsFlagTimeout.  Seven stages of 32 KB
+// and the control block fill the 227 KB a CTA may have, so the ring must
+// start at the window's first byte: a CTA that finds its shared memory
+// elsewhere (not 1024-byte aligned) marks its nodes' records with
+// kHvsFlagTimeout and does nothing else.
+constexpr int kHvsTmaStages = 7;
 constexpr int kHvsTmaLookback = 2;
 constexpr int kHvsTmaTableSets = 2;                           // table warps 0 .. 15
 constexpr int kHvsTmaSummer0 = kHvsTmaTableSets * kHvsLeaves;  // summers 16 .. 23
 constexpr int kHvsTmaSummers = kHvsLeaves;                     // one leaf each
 constexpr int kHvsTmaProducer = kHvsTmaSummer0 + kHvsTmaSummers;
 constexpr int kHvsTmaThreads = (kHvsTmaProducer + 1 + kHvsTmaLookback) * 32;
-static_assert(kHvsTmaStages % kHvsTmaTableSets == 0, "a table set's nodes keep their stages");
 static_assert(kHvsTmaLookback <= kHvsTmaStages, "a look-back warp's previous node bounds its wait");
 constexpr uint32_t kHvsNodeBytes = kHvsNode * 4;
 constexpr int kHvsNodeRows = kHvsNode / 32;
-constexpr size_t kHvsTmaSmem = (size_t)kHvsTmaStages * kHvsNodeBytes + 1024;  // + alignment
+
+// The kernel's shared memory, all of it dynamic: the ring (1024-byte aligned
+// for the 128-byte swizzle, at the start of the CTA's window), then this
+// control block.  Per stage: its mbarriers and what its node's roles pass
+// on; the leaf records per table set, in two slots used by the set's nodes
+// in turn.
+struct HvsTmaShared {
+    u64 full[kHvsTmaStages], empty[kHvsTmaStages], sums[kHvsTmaStages], exclb[kHvsTmaStages];
+    float leaf_sum[kHvsTmaStages][kHvsLeaves];
+    float excl[kHvsTmaStages];
+    unsigned flags[kHvsTmaStages], summed[kHvsTmaStages];
+    float node_sum[kHvsTmaStages];
+    unsigned err;
+    HvsRec leaf[kHvsTmaTableSets][2][kHvsLeaves];
+};
+constexpr size_t kHvsTmaRing = (size_t)kHvsTmaStages * kHvsNodeBytes;
+constexpr size_t kHvsTmaSmem = kHvsTmaRing + sizeof(HvsTmaShared);
 
 struct HvsTmaArgs {
     long long rows_full;  // full rows of 32 terms per plane
@@ -589,20 +608,40 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
 __global__ void __launch_bounds__(kHvsTmaThreads, 1)
     hvs_tables_tma(const __grid_constant__ CUtensorMap tm, HvsArgs a, HvsTmaArgs t) {
     constexpr int S = kHvsTmaStages;
-    extern __shared__ unsigned char hvs_raw[];
-    __shared__ __align__(8) u64 full[S], empty[S], sums[S], exclb[S];
-    __shared__ float s_leaf_sum[S][kHvsLeaves];
-    __shared__ float s_excl[S];
-    __shared__ unsigned s_flags[S], s_summed[S];
-    __shared__ float s_node_sum[S];
-    __shared__ unsigned s_err;
-    __shared__ HvsRec s_leaf[S][kHvsLeaves];
+    extern __shared__ __align__(1024) unsigned char hvs_raw[];
+    unsigned char *ring = hvs_raw;
+    HvsTmaShared *ctl = reinterpret_cast<HvsTmaShared *>(hvs_raw + kHvsTmaRing);
+    float(*const s_leaf_sum)[kHvsLeaves] = ctl->leaf_sum;
+    float *const s_excl = ctl->excl;
+    unsigned *const s_flags = ctl->flags;
+    unsigned *const s_summed = ctl->summed;
+    float *const s_node_sum = ctl->node_sum;
+    unsigned &s_err = ctl->err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ring0 = (smem_u32(hvs_raw) + 1023u) & ~1023u;
-    unsigned char *ring = hvs_raw + (ring0 - smem_u32(hvs_raw));
-    const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
-    const uint32_t sums0 = smem_u32(sums), excl0 = smem_u32(exclb);
+    const uint32_t ring0 = smem_u32(hvs_raw);
+    const uint32_t full0 = smem_u32(ctl->full), empty0 = smem_u32(ctl->empty);
+    const uint32_t sums0 = smem_u32(ctl->sums), excl0 = smem_u32(ctl->exclb);
+
+    const long long total = (long long)a.n_planes * a.n_nodes;
+    const int nk = total > (long long)blockIdx.x
+                       ? (int)((total - 1 - (long long)blockIdx.x) / gridDim.x + 1)
+                       : 0;
+    const u64 tag = (u64)a.epoch << 34;
+    if (ring0 & 1023u) {
+        // no room to align the ring: this CTA's nodes are reported, not summed
+        HvsNodeIter it(0, 1, a.n_planes);
+        for (int k = 0; k < nk; k++, it.next())
+            if (threadIdx.x == 0) {
+                HvsRec r;
+                r.k = make_uint4(kHvsBad, kHvsBad, kHvsBad, kHvsBad);
+                r.b = 1u;
+                r.pad[0] = kHvsFlagTimeout;
+                r.pad[1] = r.pad[2] = 0;
+                a.nodes[(size_t)it.plane * (size_t)a.n_nodes + (size_t)it.node] = r;
+            }
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; i++) {
             mbar_init(full0 + 8 * i, 1);
@@ -616,12 +655,6 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
         mbar_fence_init();
     }
     __syncthreads();
-
-    const long long total = (long long)a.n_planes * a.n_nodes;
-    const int nk = total > (long long)blockIdx.x
-                       ? (int)((total - 1 - (long long)blockIdx.x) / gridDim.x + 1)
-                       : 0;
-    const u64 tag = (u64)a.epoch << 34;
 
     if (warp == kHvsTmaProducer) {
         if (lane != 0) return;
@@ -802,12 +835,13 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
                 f0 = hvs_reduce(hvs_run_fn(tv, bl));
             }
         }
+        HvsRec *const set_leaf = ctl->leaf[warp / kHvsLeaves][(k >> 1) & 1];
         if (lane == 0) {
             HvsRec r;
             r.k = make_uint4(f0.k0, f0.k1, f1.k0, f1.k1);
             r.b = bl;
             r.pad[0] = r.pad[1] = r.pad[2] = 0;
-            s_leaf[st][lw] = r;
+            set_leaf[lw] = r;
             if (leaf < a.n_leaves) a.leaves[(size_t)plane * (size_t)a.n_leaves + (size_t)leaf] = r;
             if (err) s_err = 1u;
         }
@@ -815,11 +849,12 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
         // its warp 0 frees the buffer, keeping what the node's record needs
         // (the flags, which the next use of the stage sets afresh, and the
         // prefix estimate), then composes the record from the leaf records
-        // (which only this set rewrites, after its warp 0 is back)
+        // (their slot is rewritten only by this set's node after next, which
+        // its warps reach past the next named barrier, after warp 0 is back)
         named_barrier(1 + warp / kHvsLeaves, 32 * kHvsLeaves);
         if (lw == 0) {
             const float ex = s_excl[st];
-            const HvsRec lr = s_leaf[st][lane & (kHvsLeaves - 1)];
+            const HvsRec lr = set_leaf[lane & (kHvsLeaves - 1)];
             uint32_t fl = 0u;
             if (lane == 0) {
                 fl = s_flags[st] | ((err || s_err) ? kHvsFlagTimeout : 0u);

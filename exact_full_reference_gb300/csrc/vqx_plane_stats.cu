@@ -208,7 +208,7 @@ struct DeviceCtx {
     cudaMemPool_t pool = nullptr;
     cudaStream_t copy_stream = nullptr;
     std::atomic<uint32_t> hvs_epoch{0};  // tags of the psnr_hvs look-back words
-    int hvs_tma_resident = 0;            // hvs_tables_tma CTAs per SM
+    int hvs_tma_resident = 0;            // hvs_tables_tma CTAs per SM (0: not used here)
 };
 
 constexpr int kMaxDevices = 64;
@@ -221,19 +221,28 @@ cudaError_t init_device(DeviceCtx &c, int dev) {
     e = cudaFuncSetAttribute(vqx::hvs_tables, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)vqx::kHvsTablesSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(vqx::hvs_tables_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)vqx::kHvsTmaSmem);
+    // The pipelined psnr_hvs kernel takes all the shared memory a CTA may
+    // have; on a device that offers less it is not used (hvs_tables is).
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
+    const bool hvs_tma = (size_t)optin >= vqx::kHvsTmaSmem;
+    if (hvs_tma) {
+        e = cudaFuncSetAttribute(vqx::hvs_tables_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)vqx::kHvsTmaSmem);
+        if (e != cudaSuccess) return e;
+    }
     // The walk (one warp, no shared memory) runs beside the next batch's
     // tables kernel: keep the SMs it sits on configured for the tables'
     // shared memory, so that their CTAs are not held back until it ends.
     e = cudaFuncSetAttribute(vqx::hvs_walk, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.hvs_tma_resident, vqx::hvs_tables_tma,
-                                                      vqx::kHvsTmaThreads, vqx::kHvsTmaSmem);
-    if (e != cudaSuccess) return e;
-    if (c.hvs_tma_resident < 1) c.hvs_tma_resident = 1;
+    if (hvs_tma) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.hvs_tma_resident, vqx::hvs_tables_tma,
+                                                          vqx::kHvsTmaThreads, vqx::kHvsTmaSmem);
+        if (e != cudaSuccess) return e;
+    }
 
     cudaMemPoolProps props;
     memset(&props, 0, sizeof props);
@@ -1517,7 +1526,7 @@ extern "C" int vqx_psnr_hvs_sum_submit(const float *terms, int64_t n_terms, int6
     // least one full row of 32 terms stream through the persistent TMA
     // pipeline; anything else takes one CTA per node.
     const long long rows_full = n_terms / 32;
-    const bool tma = a.vec && rows_full >= 1;
+    const bool tma = a.vec && rows_full >= 1 && ctx->hvs_tma_resident > 0;
     CUtensorMap tm;
     vqx::HvsTmaArgs ta;
     ta.rows_full = rows_full;
