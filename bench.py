@@ -443,7 +443,99 @@ OP_API = {"stats": "vqx_plane_stats", "int_psnr": "vqx_plane_int_psnr",
           "planes420": "vqx_planes_stats"}
 
 
-class Batch:
+class Stepper:
+    """Pipelined steps of submit / finish pairs and their timed regions.
+    Subclasses provide submit(), finish(handle), ``flush`` (an L2-sized
+    batch: each step timed on its own after overwriting the L2) and
+    ``scratch`` (the buffer that overwrites it)."""
+
+    flush = False
+    scratch = None
+
+    def steps(self, k):
+        """k whole steps, pipelined: batch i + 1 is enqueued before batch i is
+        waited on and concluded, so the device runs the next batch's kernels
+        while the host concludes this one."""
+        prev = None
+        for _ in range(k):
+            cur = self.submit()
+            if prev is not None:
+                self.finish(prev)
+            prev = cur
+        if prev is not None:
+            self.finish(prev)
+
+    def flushed_steps(self, k):
+        """k steps, each after an L2 flush; returns the summed step time (ms)."""
+        torch, stream = self.ctx.torch, self.ctx.stream
+        total = 0.0
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for _ in range(k):
+            with torch.cuda.stream(stream):
+                self.scratch.zero_()
+            e0.record(stream)
+            self.finish(self.submit())
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+        return total
+
+    def region(self, steps, instrumented):
+        """K steps between a barrier + synchronize on both sides, timed with
+        CUDA events on the launching stream (L2-sized batches: each step after
+        a flush, flush excluded).  With ``instrumented`` the library also
+        records CUDA events around its kernels inside every call, which costs
+        the overlap of consecutive launches, so throughput comes from the
+        uninstrumented regions.  Returns (max-over-ranks ms, wall t0, t1)."""
+        ctx = self.ctx
+        torch = ctx.torch
+        ctx.barrier()
+        torch.cuda.synchronize()
+        ctx.vqx.profile_enable(instrumented)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        if self.flush:
+            ms = self.flushed_steps(steps)
+        else:
+            ev0.record(ctx.stream)
+            self.steps(steps)  # the last conclusion is inside the region too
+            ev1.record(ctx.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        if not self.flush:
+            ms = ev0.elapsed_time(ev1)
+        ctx.barrier()
+        ctx.vqx.profile_enable(False)
+        return reduce_max(ms, ctx.pg, ctx.dev), t0, t1
+
+    def measure(self, steps, warmup, min_repeats, min_seconds, inst_repeats):
+        """Warm up, then the timed regions (repeated: at least min_repeats and
+        about min_seconds of wall time, the same count on every rank), then
+        inst_repeats instrumented regions for the per-launch kernel times."""
+        ctx = self.ctx
+        self.steps(max(warmup, 3))
+        ctx.torch.cuda.synchronize()
+        calib_ms, c0, c1 = self.region(steps, False)
+        reps = repeat_count(c1 - c0, min_repeats, min_seconds)
+        reps = int(reduce_max(reps, ctx.pg, ctx.dev))
+        ctx.vqx.profile_read(reset=True)
+        regions, t_first, t_last = [], None, None
+        for _ in range(reps):
+            ms, t0, t1 = self.region(steps, False)
+            regions.append(ms)
+            t_first = t0 if t_first is None else t_first
+            t_last = t1
+        counted = ctx.vqx.profile_read(reset=True)
+        for _ in range(max(inst_repeats, 1)):
+            self.region(steps, True)
+        prof = ctx.vqx.profile_read(reset=True)
+        return {"regions": summarize_regions(regions, steps), "counted": counted, "prof": prof,
+                "t0": t_first, "t1": t_last, "reps": reps}
+
+
+class Batch(Stepper):
     """One workload's planes on the device and the op's submit / finish
     calls on them (the call a user makes; arguments only)."""
 
@@ -530,88 +622,6 @@ class Batch:
         rc = self._finish_call(handle)
         if rc != 0:
             raise RuntimeError("finish: %s" % self.ctx.vqx.status_string(rc))
-
-    def steps(self, k):
-        """k whole steps, pipelined: batch i + 1 is enqueued before batch i is
-        waited on and concluded, so the device runs the next batch's kernels
-        while the host concludes this one."""
-        prev = None
-        for _ in range(k):
-            cur = self.submit()
-            if prev is not None:
-                self.finish(prev)
-            prev = cur
-        if prev is not None:
-            self.finish(prev)
-
-    def flushed_steps(self, k):
-        """k steps, each after an L2 flush; returns the summed step time (ms)."""
-        torch, stream = self.ctx.torch, self.ctx.stream
-        total = 0.0
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        for _ in range(k):
-            with torch.cuda.stream(stream):
-                self.scratch.zero_()
-            e0.record(stream)
-            self.finish(self.submit())
-            e1.record(stream)
-            e1.synchronize()
-            total += e0.elapsed_time(e1)
-        return total
-
-    def region(self, steps, instrumented):
-        """K steps between a barrier + synchronize on both sides, timed with
-        CUDA events on the launching stream (L2-sized batches: each step after
-        a flush, flush excluded).  With ``instrumented`` the library also
-        records CUDA events around its kernels inside every call, which costs
-        the overlap of consecutive launches, so throughput comes from the
-        uninstrumented regions.  Returns (max-over-ranks ms, wall t0, t1)."""
-        ctx = self.ctx
-        torch = ctx.torch
-        ctx.barrier()
-        torch.cuda.synchronize()
-        ctx.vqx.profile_enable(instrumented)
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        t0 = time.time()
-        if self.flush:
-            ms = self.flushed_steps(steps)
-        else:
-            ev0.record(ctx.stream)
-            self.steps(steps)  # the last conclusion is inside the region too
-            ev1.record(ctx.stream)
-        torch.cuda.synchronize()
-        t1 = time.time()
-        if not self.flush:
-            ms = ev0.elapsed_time(ev1)
-        ctx.barrier()
-        ctx.vqx.profile_enable(False)
-        return reduce_max(ms, ctx.pg, ctx.dev), t0, t1
-
-    def measure(self, steps, warmup, min_repeats, min_seconds, inst_repeats):
-        """Warm up, then the timed regions (repeated: at least min_repeats and
-        about min_seconds of wall time, the same count on every rank), then
-        inst_repeats instrumented regions for the per-launch kernel times."""
-        ctx = self.ctx
-        self.steps(max(warmup, 3))
-        ctx.torch.cuda.synchronize()
-        calib_ms, c0, c1 = self.region(steps, False)
-        reps = repeat_count(c1 - c0, min_repeats, min_seconds)
-        reps = int(reduce_max(reps, ctx.pg, ctx.dev))
-        ctx.vqx.profile_read(reset=True)
-        regions, t_first, t_last = [], None, None
-        for _ in range(reps):
-            ms, t0, t1 = self.region(steps, False)
-            regions.append(ms)
-            t_first = t0 if t_first is None else t_first
-            t_last = t1
-        counted = ctx.vqx.profile_read(reset=True)
-        for _ in range(max(inst_repeats, 1)):
-            self.region(steps, True)
-        prof = ctx.vqx.profile_read(reset=True)
-        return {"regions": summarize_regions(regions, steps), "counted": counted, "prof": prof,
-                "t0": t_first, "t1": t_last, "reps": reps}
 
 
 def kernel_label(op, wlo):
@@ -906,133 +916,94 @@ def run_hvs_reference(args, hw):
     return 0
 
 
-def run_hvs(args, hw):
-    """One step = one batch of term planes resident in HBM through
-    vqx_psnr_hvs_sum_submit + _finish (tables, walk, read-back, score),
-    pipelined one deep like the plane statistics."""
-    import ctypes
+class HvsBatch(Stepper):
+    """A batch of psnr_hvs term planes on the device and its submit / finish
+    calls (vqx_psnr_hvs_sum_submit / _finish)."""
 
-    import numpy as np
-    import torch
+    def __init__(self, ctx, hw):
+        import ctypes
 
-    __import__("__graft_entry__").build()
-    import exact_full_reference_gb300 as vqx
+        import numpy as np
 
-    rank, world, local = dist_env()
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
+        torch, vqx = ctx.torch, ctx.vqx
+        self.ctx, self.hw = ctx, hw
+        self.terms = hw.generate()
+        self.n_planes, self.n_terms = self.terms.shape
+        self.d_terms = torch.from_numpy(self.terms).to(ctx.dev)
+        torch.cuda.synchronize()
+        self.out = np.zeros(self.n_planes, vqx.HVS_PLANE_DTYPE)
+        self._ctypes = ctypes
+        if self.terms.nbytes < 2 * ctx.l2_bytes:
+            raise SystemExit("psnr_hvs bench batches must be larger than twice the L2")
 
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-        pg = dist
-    torch.cuda.set_device(local)
-    dev = torch.cuda.current_device()
-    stream = torch.cuda.Stream()
-    sh = stream.cuda_stream
-    terms = hw.generate()
-    n_planes, n_terms = terms.shape
-    d_terms = torch.from_numpy(terms).to(dev)
-    torch.cuda.synchronize()
-    so = vqx.library()
-    out = np.zeros(n_planes, vqx.HVS_PLANE_DTYPE)
-    out_p = out.ctypes.data
-
-    def submit(ptr=None):
-        handle = ctypes.c_void_p()
-        rc = so.vqx_psnr_hvs_sum_submit(ptr or d_terms.data_ptr(), n_terms, n_terms, n_planes,
-                                        hw.bpc, sh, vqx.VQX_SUBMIT_PLANES_READY if ptr is None else 0,
-                                        ctypes.byref(handle))
+    def submit(self, ptr=None):
+        vqx = self.ctx.vqx
+        handle = self._ctypes.c_void_p()
+        rc = self.ctx.so.vqx_psnr_hvs_sum_submit(
+            ptr or self.d_terms.data_ptr(), self.n_terms, self.n_terms, self.n_planes, self.hw.bpc,
+            self.ctx.sh, vqx.VQX_SUBMIT_PLANES_READY if ptr is None else 0, self._ctypes.byref(handle))
         if rc != 0:
             raise RuntimeError("submit: %s" % vqx.status_string(rc))
         return handle
 
-    def finish(handle):
-        rc = so.vqx_psnr_hvs_sum_finish(handle, out_p)
+    def finish(self, handle):
+        rc = self.ctx.so.vqx_psnr_hvs_sum_finish(handle, self.out.ctypes.data)
         if rc != 0:
-            raise RuntimeError("finish: %s" % vqx.status_string(rc))
+            raise RuntimeError("finish: %s" % self.ctx.vqx.status_string(rc))
 
-    def steps(k):
-        prev = None
-        for _ in range(k):
-            cur = submit()
-            if prev is not None:
-                finish(prev)
-            prev = cur
-        if prev is not None:
-            finish(prev)
 
-    def barrier():
-        if pg is not None:
-            pg.barrier()
+def run_hvs(args, hw):
+    """One step = one batch of term planes resident in HBM through
+    vqx_psnr_hvs_sum_submit + _finish (tables, walk, read-back, score),
+    pipelined one deep like the plane statistics, timed the same way."""
+    rank, world, local = dist_env()
+    ctx = BenchDevice(world, local)
+    torch = ctx.torch
+    b = HvsBatch(ctx, hw)
+    n_planes, n_terms = b.n_planes, b.n_terms
 
-    steps(max(args.warmup, 3))
-    torch.cuda.synchronize()
-    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (129 << 20)
-    if terms.nbytes < 2 * l2_bytes:
-        raise SystemExit("psnr_hvs bench batches must be larger than twice the L2")
-
-    def timed_region(instrumented):
-        barrier()
-        torch.cuda.synchronize()
-        vqx.profile_enable(instrumented)
-        vqx.profile_read(reset=True)
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        t0 = time.time()
-        ev0.record(stream)
-        steps(args.steps)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        t1 = time.time()
-        barrier()
-        prof = vqx.profile_read(reset=True)
-        vqx.profile_enable(False)
-        return reduce_max(ev0.elapsed_time(ev1), pg, dev), prof, t0, t1
-
-    clocks = ClockSampler(gpu_smi_id(torch, dev))
+    clocks = ClockSampler(gpu_smi_id(torch, ctx.dev))
     time.sleep(0.3)
-    elapsed_ms, counted, t_wall0, t_wall1 = timed_region(False)
-    inst_ms, prof, _, _ = timed_region(True)
+    m = b.measure(args.steps, args.warmup, args.repeats, args.min_timed_seconds, args.inst_repeats)
     time.sleep(0.2)
     clocks.stop()
-    value = job_throughput(world, n_planes, args.steps, elapsed_ms / 1e3)
+    reg = m["regions"]
+    value = job_throughput(world, n_planes, args.steps, reg["median_ms"] / 1e3)
     peak, peak_kind = measured_peak()
-    launches = max(prof["stage1_launches"], 1)
-    avg_ms = prof["stage1_ms"] / launches
-    bytes_per_launch = prof["stage1_bytes"] / launches
-    achieved = bytes_per_launch / (avg_ms / 1e3) / 1e9
+    avg_ms, bytes_per_launch, achieved, frac = kernel_roofline(m["prof"], peak)
+    launches = max(m["prof"]["stage1_launches"], 1)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                "timing": "CUDA events recorded by the library around each launch in a second "
-                          "timed region of the same %d steps" % args.steps,
-                "instrumented_region_ms_per_step": inst_ms / args.steps,
-                "kernel": "hvs_tables", "avg_launch_us": avg_ms * 1e3,
+                "frac": frac, "traffic": None, "peak_source": peak_kind,
+                "timing": "CUDA events recorded by the library around each launch in %d "
+                          "instrumented regions of the same %d steps"
+                          % (max(args.inst_repeats, 1), args.steps),
+                "kernel": "hvs_tables_tma", "avg_launch_us": avg_ms * 1e3,
                 "bytes_per_launch": bytes_per_launch,
-                "walk_avg_us": prof["stage2_ms"] / launches * 1e3}
+                "walk_avg_us": m["prof"]["stage2_ms"] / launches * 1e3}
 
     e2e = None
     if not args.no_e2e:
-        h_terms = torch.from_numpy(terms).pin_memory()
-        d_e2e = torch.empty_like(d_terms)
+        h_terms = torch.from_numpy(b.terms).pin_memory()
+        d_e2e = torch.empty_like(b.d_terms)
         k = max(1, min(args.e2e_steps, args.steps))
-        barrier()
+        ctx.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(k):
-            with torch.cuda.stream(stream):
+            with torch.cuda.stream(ctx.stream):
                 d_e2e.copy_(h_terms, non_blocking=True)
-            finish(submit(d_e2e.data_ptr()))
+            b.finish(b.submit(d_e2e.data_ptr()))
         torch.cuda.synchronize()
-        el = reduce_max(time.perf_counter() - t0, pg, dev)
+        el = reduce_max(time.perf_counter() - t0, ctx.pg, ctx.dev)
         e2e = {"value": job_throughput(world, n_planes, k, el), "unit": HVS_UNIT, "steps": k,
-               "h2d_bytes_per_step": int(terms.nbytes),
+               "h2d_bytes_per_step": int(b.terms.nbytes),
                "d2h_bytes_per_step": int(n_planes * 16),
                "api": "copy of pinned host terms on the call's stream, then vqx_psnr_hvs_sum_submit / _finish"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cores = host_cores()
-        sub = terms[: min(n_planes, cores)]
+        sub = b.terms[: min(n_planes, cores)]
         rate, planes, el = time_oracle_hvs(hw, sub, args.cpu_seconds, cores)
         cpu = {"value": rate, "unit": HVS_UNIT, "cores": cores, "kind": "oracle",
                "sample": "%.1f whole planes of %s (one per thread) in %.1f s" % (planes, hw.name, el)}
@@ -1041,24 +1012,28 @@ def run_hvs(args, hw):
         line = {
             "metric": hvs_metric(hw), "value": value, "unit": HVS_UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": reg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "hbm_gbs": value * 4 * n_terms / 1e9 / world,
+            "timing": {"repeats": reg["repeats"], "statistic": "median of the repeated regions",
+                       "region_ms": {k: reg[k] for k in ("median_ms", "min_ms", "p10_ms", "p90_ms",
+                                                        "max_ms")}},
             "config": {"workload": hw.name, "planes_per_gpu": n_planes, "terms_per_plane": n_terms,
-                       "bpc": hw.bpc, "batch_bytes": int(terms.nbytes),
+                       "bpc": hw.bpc, "batch_bytes": int(b.terms.nbytes),
                        "l2": "terms %.2f GB per step, larger than the 129 MB L2; no flush"
-                             % (terms.nbytes / 1e9),
+                             % (b.terms.nbytes / 1e9),
                        "pipeline": "batch i + 1 submitted before batch i is finished "
                                    "(vqx_psnr_hvs_sum_submit with VQX_SUBMIT_PLANES_READY / _finish)",
                        "parallelism": "planes independent per GPU" if world > 1 else "1 GPU"},
             "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu,
-            "clocks": clocks.summary(t_wall0, t_wall1),
-            "gpu_launches": int(counted["kernel_launches"]),
-            "replayed_leaves_max": int(out["replayed_leaves"].max()),
+            "clocks": clocks.summary(m["t0"], m["t1"]),
+            "gpu_launches": int(m["counted"]["kernel_launches"] // max(m["reps"], 1)),
+            "gpu_launches_all_repeats": int(m["counted"]["kernel_launches"]),
+            "replayed_leaves_max": int(b.out["replayed_leaves"].max()),
         }
         print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    if ctx.pg is not None:
+        ctx.pg.destroy_process_group()
     return 0
 
 

@@ -404,15 +404,17 @@ struct SplitSum2 {
 //   SSE = sum of q - sum of (q - D * D) = noise - sum of the errors.
 // The errors are added per lane in fp32, which is exact while the running sum
 // stays below 2^24 in magnitude: a run between flushes holds at most
-// 4 * kFlushVecs = 8192 terms a lane, so at most 2^20.  Three more packed
-// operations a pixel pair (the negated difference, the fma, the add), all on
-// the FMA pipe; no further conversion.
+// 4 * kFlushVecs = 8192 terms a lane, so at most 2^20.  Per pixel pair: the
+// difference negated by flipping both sign bits (ALU pipe: the FMA pipe is
+// the busier one here), one packed fma and one packed add; no further
+// conversion.
 template <bool kSse>
 struct Sums16 {
     static constexpr uint32_t kBias = 0x4B000000u;
     static constexpr uint32_t kFlushVecs = 2048;
     static_assert(8 * kFlushVecs <= SplitSum2::kMaxTerms, "SplitSum2 run bound");
     static_assert(4 * kFlushVecs * 128 <= (1u << 24), "fp32 error sums stay exact");
+    static constexpr f32x2 kSigns = 0x8000000080000000ull;  // -x of both lanes: x ^ kSigns
     SplitSum2 rsq_;
     u64 noise = 0, rss = 0, dss = 0, sr = 0, sd = 0;
     long long err = 0;  // sum of fl(D * D) - D * D (kSse)
@@ -426,7 +428,7 @@ struct Sums16 {
         const f32x2 sq = f2_square(diff);
         f2_unpack(sq, t0, t1);
         noise += (u64)__float2uint_rn(__uint_as_float(t0)) + __float2uint_rn(__uint_as_float(t1));
-        if constexpr (kSse) err_ = f2_add(err_, f2_fma(f2_sub(xd, xr), diff, sq));
+        if constexpr (kSse) err_ = f2_add(err_, f2_fma(diff ^ kSigns, diff, sq));
         const f32x2 fr = f2_sub(xr, two23);
         rsq_.add(f2_square(fr));
         uint32_t q0, q1;

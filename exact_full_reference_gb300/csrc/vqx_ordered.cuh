@@ -46,7 +46,6 @@ constexpr int kOrdExact = -1;     // block class: every prefix below 2^53
 constexpr int kOrdReplay = 99;    // block class: replay term by term
 constexpr int kOrdLane = kOrdBlock / 32;  // terms per lane in ordered_tables
 constexpr u64 kTwo53 = 1ull << 53;
-constexpr uint32_t kOrdErrBit = 1u << 31;  // in a block's reference sample sum: a wait gave up
 constexpr u64 kOrdMargin = 1ull << 28;
 
 struct OrdTable {
@@ -203,13 +202,10 @@ struct OrdWordSums {
 };
 
 // A warp's sums of one block to the block's records: the three exact
-// sums, their ORs and the two sample sums (see ordered_block_sums).  err: a
-// device wait of this warp gave up, so the sums are incomplete; bit 31 of
-// the reference sample sum (which is below 2^28) carries that to
-// ordered_classify.
+// sums, their ORs and the two sample sums (see ordered_block_sums).
 __device__ __forceinline__ void ord_store_block(const OrdWordSums &w, int f, int b, int nb, int lane,
                                                 u64 *__restrict__ sums, uint32_t *__restrict__ ors,
-                                                uint32_t *__restrict__ ssums, bool err) {
+                                                uint32_t *__restrict__ ssums) {
     u64 tot[kOrdSeqs];
 #pragma unroll
     for (int q = 0; q < kOrdSeqs; q++) tot[q] = w.total(q);
@@ -226,8 +222,7 @@ __device__ __forceinline__ void ord_store_block(const OrdWordSums &w, int f, int
         sums[slot + lane] = lane == 0 ? tot[0] : lane == 1 ? tot[1] : tot[2];
         ors[slot + lane] = lane == 0 ? o[0] : lane == 1 ? o[1] : o[2];
     } else if (lane < kOrdSeqs + 2) {
-        ssums[((size_t)f * nb + b) * 2 + (lane - kOrdSeqs)] =
-            lane == kOrdSeqs ? (sr | (err ? kOrdErrBit : 0u)) : sd;
+        ssums[((size_t)f * nb + b) * 2 + (lane - kOrdSeqs)] = lane == kOrdSeqs ? sr : sd;
     }
 }
 
@@ -272,7 +267,7 @@ __global__ void __launch_bounds__(32 * kSumWarps, 10)
             w.sd += d;
         });
     }
-    ord_store_block(w, f, b, g.nb, lane, sums, ors, ssums, false);
+    ord_store_block(w, f, b, g.nb, lane, sums, ors, ssums);
 }
 
 __device__ __forceinline__ int binade_of(u64 x) { return 63 - __clzll((long long)x); }
@@ -283,13 +278,11 @@ struct OrdWork {
 };
 
 constexpr int kOrdBatch = 8;  // chunks of 32 blocks loaded at once by the one-warp kernels
-constexpr int kOrdOut = 9;    // words per frame of the ordered kernels' output
+constexpr int kOrdOut = 8;    // words per frame of the ordered kernels' output
 
 // Grid (frames, 3), kClassThreads threads: prefix sums over the blocks of
 // one sequence and the class of every block, cls[(f * 3 + q) * nb + b]; the
-// q = 0 CTA also adds the blocks' sample sums into out[f * kOrdOut + 6, 7]
-// and writes the frame's flags, kErrTimeout if a block's sums are
-// incomplete (kOrdErrBit), into out[f * kOrdOut + 8].
+// q = 0 CTA also adds the blocks' sample sums into out[f * kOrdOut + 6, 7].
 // Thread t takes a run of consecutive blocks; the runs' sums are scanned
 // across the CTA (warp scans, then the warps' totals), and each thread walks
 // its run from its exclusive prefix.  A single-binade block whose terms are
@@ -307,13 +300,10 @@ __global__ void __launch_bounds__(kClassThreads)
     const int b0 = min(t * per, nb), b1 = min(b0 + per, nb);
     const size_t row = (size_t)f * nb;
     u64 mine = 0, sr = 0, sd = 0;
-    uint32_t err = 0;
     for (int b = b0; b < b1; b++) {
         mine += sums[(row + b) * kOrdSeqs + q];
         if (q == 0) {
-            const uint32_t r = ssums[(row + b) * 2];
-            err |= r & kOrdErrBit;
-            sr += r & ~kOrdErrBit;
+            sr += ssums[(row + b) * 2];
             sd += ssums[(row + b) * 2 + 1];
         }
     }
@@ -328,7 +318,6 @@ __global__ void __launch_bounds__(kClassThreads)
     __shared__ int wcount[kWarps];
     __shared__ int wbase[kWarps];
     __shared__ u64 s2[kWarps][2];
-    __shared__ uint32_t serr[kWarps];
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     u64 before = 0;
@@ -365,11 +354,9 @@ __global__ void __launch_bounds__(kClassThreads)
             sr += __shfl_xor_sync(0xffffffffu, sr, sh);
             sd += __shfl_xor_sync(0xffffffffu, sd, sh);
         }
-        err = __reduce_or_sync(0xffffffffu, err);
         if (lane == 0) {
             s2[warp][0] = sr;
             s2[warp][1] = sd;
-            serr[warp] = err;
         }
     }
     __syncthreads();
@@ -383,15 +370,12 @@ __global__ void __launch_bounds__(kClassThreads)
         for (int w = 0; w < kWarps; w++) wbase[w] += first;
         if (q == 0) {
             u64 a = 0, d = 0;
-            uint32_t e = 0;
             for (int w = 0; w < kWarps; w++) {
                 a += s2[w][0];
                 d += s2[w][1];
-                e |= serr[w];
             }
             out[(size_t)f * kOrdOut + 6] = a;
             out[(size_t)f * kOrdOut + 7] = d;
-            out[(size_t)f * kOrdOut + 8] = e ? kErrTimeout : 0ull;
         }
     }
     __syncthreads();

@@ -936,7 +936,7 @@ int finish_impl(vqx_pending *p, int kind, void *out, void *out2 = nullptr) {
                 s_f.v[2] = o[7];
                 s_f.v[3] = o[4];  // exact squares
                 s_f.v[4] = o[5];
-                s_f.v[5] = o[8];  // 16 bits: no sample out of range; a wait that gave up
+                s_f.v[5] = 0;  // 16 bits: no sample out of range; no device wait to time out
                 s_f.v[6] = s_f.v[7] = 0;
                 vqx_frame_stats &r = ((vqx_frame_stats *)out)[f];
                 conclude(s_f, p->bpc, p->width, p->height, &r, o);
