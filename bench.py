@@ -234,7 +234,8 @@ TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "fused_stream_traffic.json")
 KERNEL_LABEL = "fused_stream_tma<%d, 16, 1536, 2, DenseSource, TermSums<%d>>"
 # the capture the traffic record is taken from (the plain command runs first)
 TRAFFIC_CAPTURE = ("ncu --set full --clock-control none -k regex:fused_stream -s 3 -c 1 "
-                   "-o prof_fused_stream python bench.py --steps 5 --warmup 3 --no-cpu --no-e2e")
+                   "-o prof_fused_stream python bench.py --steps 3 --warmup 3 --no-cpu --no-e2e "
+                   "--no-configs --repeats 1 --min-timed-seconds 0 --inst-repeats 1")
 
 
 def recorded_traffic(workload_name):
