@@ -372,3 +372,26 @@ def test_every_kind_from_four_threads(lib, orc):
     for t in th:
         t.join()
     assert not bad, bad
+
+
+@pytest.mark.parametrize("w,h,bpc,n", [(512, 512, 16, 400), (512, 512, 8, 400), (1920, 1080, 16, 64),
+                                       (1920, 1080, 12, 70), (2000, 1000, 10, 5)])
+def test_dense_batches_against_padded_pitches(lib, orc, w, h, bpc, n):
+    """Batches of many mid-size dense frames (512x512 x400: more frames than
+    CTAs, units of whole frames) and of few large ones: every frame's records
+    equal the oracle's and those of the same frames on a padded pitch (row
+    pieces instead of whole-frame copies); so do the integer psnr and the
+    one-read scores."""
+    rng = np.random.Generator(np.random.PCG64(w + 7 * n + bpc))
+    dt = np.uint8 if bpc == 8 else np.uint16
+    bps = 1 if bpc == 8 else 2
+    ref = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    dist = rng.integers(0, 1 << bpc, (n, h, w)).astype(dt)
+    rec, sc, un = run_case(lib, orc, ref, dist, bpc)
+    keep, pr, pd, stride, _ = parity.place(ref, dist, stride=w * bps + 32)
+    assert lib.vqx_plane_stats(pr, pd, w, h, stride, bpc, n).tobytes() == rec.tobytes()
+    keep2, pr2, pd2, stride2, _ = parity.place(ref, dist)
+    ip = lib.vqx_plane_int_psnr(pr2, pd2, w, h, stride2, bpc, n)
+    assert ip.tobytes() == lib.vqx_plane_int_psnr(pr, pd, w, h, stride, bpc, n).tobytes()
+    st, ip2 = lib.vqx_plane_scores(pr2, pd2, w, h, stride2, bpc, n)
+    assert st.tobytes() == rec.tobytes() and ip2.tobytes() == ip.tobytes()
