@@ -231,16 +231,7 @@ def kernel_source_digest():
 
 
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "fused_stream_traffic.json")
-
-
-def stats_label(bpc):
-    """The fused-statistics kernel of a bit depth, with its pipeline shape
-    (bit depth, consumer warps, vectors per stage, stages, CTAs per SM)."""
-    if bpc == 16:
-        return "fused_stream_tma<16, 16, 1536, 4, 1, DenseSource, TermSums<16>>"
-    return "fused_stream_tma<%d, 16, 1536, 2, 2, DenseSource, TermSums<%d>>" % (bpc, bpc)
-
-
+KERNEL_LABEL = "fused_stream_tma<%d, 16, 1536, 2, DenseSource, TermSums<%d>>"
 # the capture the traffic record is taken from (the plain command runs first)
 TRAFFIC_CAPTURE = ("ncu --set full --clock-control none -k regex:fused_stream -s 3 -c 1 "
                    "-o prof_fused_stream python bench.py --steps 3 --warmup 3 --no-cpu --no-e2e "
@@ -288,7 +279,7 @@ def write_traffic_record(report, wlo):
     rd, wr = val("dram__bytes_read.sum"), val("dram__bytes_write.sum")
     bps = 1 if wlo.bpc == 8 else 2
     rec = {
-        "kernel": stats_label(wlo.bpc),
+        "kernel": KERNEL_LABEL % (wlo.bpc, wlo.bpc),
         "source_sha256": kernel_source_digest(),
         "per_launch_bytes": {wlo.name: rd + wr},
         "dram_bytes_read": rd,
@@ -636,14 +627,14 @@ class Batch(Stepper):
 
 def kernel_label(op, wlo):
     if op == "int_psnr" and wlo.bpc == 16:
-        return "fused_stream_tma<16, 20, 1920, 3, 1, DenseSource, SseSums16>"
+        return "fused_stream_tma<16, 16, 1536, 2, DenseSource, SseSums16>"
     if op == "scores" and wlo.bpc == 16:
-        return "fused_stream_tma<16, 24, 2304, 3, 0, DenseSource, TermSums16Sse>"
+        return "fused_stream_tma<16, 16, 1536, 2, DenseSource, TermSums16Sse>"
     if op == "ordered" and wlo.bpc == 16 and wlo.width * wlo.height > 2 ** 21:
         return "ordered_block_sums"
     if op == "planes420":
         return "fused_stream_tma, three planes (Y, Cb, Cr) timed together"
-    return stats_label(wlo.bpc)
+    return KERNEL_LABEL % (wlo.bpc, wlo.bpc)
 
 
 def kernel_roofline(prof, peak):
@@ -784,7 +775,7 @@ def run_ours(args, wlo):
                 "us_per_call": cr["ms_per_step"] * 1e3,
                 "repeats": cr["repeats"], "min_ms": cr["min_ms"], "max_ms": cr["max_ms"],
                 "step_gbs": step_gbs, "step_frac": step_gbs / peak,
-                "kernel": stats_label(cw.bpc), "kernel_avg_launch_us": c_ms * 1e3,
+                "kernel": KERNEL_LABEL % (cw.bpc, cw.bpc), "kernel_avg_launch_us": c_ms * 1e3,
                 "kernel_frac": c_frac,
                 "l2": ("batch smaller than twice the L2: L2 overwritten before every step, steps "
                        "timed one by one, flush excluded" if cb.flush else

@@ -54,6 +54,17 @@ constexpr int kWords = 8;
 constexpr int kThreads = 256;     // CTA size of the strided-layout stage-1 kernel
 constexpr int kSumThreads = 128;  // stage-2 CTA size
 
+// Shape of the stage-1 TMA pipeline (fused_stream_tma): consumer
+// warps, 16-byte vectors per plane per stage, stages in the ring.  Chosen by
+// measurement on GB300 over 8-, 10-, 12- and 16-bit batches of 3840x2160 and
+// 1920x1080 frames (two large stages beat three or more smaller ones: fewer
+// hand-offs per byte); two CTAs (96 KB of ring each) are resident per SM.
+constexpr int kTmaWarps = 16;
+constexpr int kTmaStageVecs = 1536;
+constexpr int kTmaStages = 2;
+constexpr int kTmaThreads = (kTmaWarps + 1) * 32;
+constexpr size_t kTmaSmem = (size_t)kTmaStages * 2 * kTmaStageVecs * 16;
+
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     uint4 v;
@@ -506,42 +517,6 @@ struct SseSums16 {
     }
 };
 
-// ---------------------------------------------------------------- pipeline shape
-// Shape of the stage-1 TMA pipeline (fused_stream_tma) per accumulator:
-// consumer warps, 16-byte vectors per plane per stage, stages in the ring,
-// and the CTAs per SM the register allocation must allow (0: the compiler
-// chooses).  Chosen by measurement on GB300 over batches of 3840x2160 and
-// 1920x1080 frames.  Up to 12 bits two CTAs share an SM, each with two large
-// stages (96 KB of ring): two large stages beat three or more smaller ones,
-// with fewer hand-offs per byte.  At 16 bits, where a vector takes the most
-// instructions, one CTA per SM does better: of two CTAs on an SM the one
-// started first finishes about a quarter sooner, leaving the SM half used
-// for the rest of the launch.
-template <class Acc>
-struct TmaShape {
-    static constexpr int kWarps = 16, kStageVecs = 1536, kStages = 2, kMinCtas = 2;
-};
-template <>
-struct TmaShape<TermSums<16>> {
-    static constexpr int kWarps = 16, kStageVecs = 1536, kStages = 4, kMinCtas = 1;
-};
-template <>
-struct TmaShape<SseSums16> {
-    static constexpr int kWarps = 20, kStageVecs = 1920, kStages = 3, kMinCtas = 1;
-};
-template <>
-struct TmaShape<TermSums16Sse> {
-    static constexpr int kWarps = 24, kStageVecs = 2304, kStages = 3, kMinCtas = 0;
-};
-template <class Acc>
-constexpr int tma_threads() {
-    return (TmaShape<Acc>::kWarps + 1) * 32;
-}
-template <class Acc>
-constexpr size_t tma_smem() {
-    return (size_t)TmaShape<Acc>::kStages * 2 * TmaShape<Acc>::kStageVecs * 16;
-}
-
 // ---------------------------------------------------------------- reduction
 // Warp shuffles, then one value per warp through shared memory, then warp 0:
 // words 0..4, 6 and 7 of a record are added, word 5 ORed.  Integer sums:
@@ -899,8 +874,8 @@ struct TileSource {
 // each unit (record r of the source becomes records r * NCW .. r * NCW +
 // NCW - 1) and ends a unit without waiting for the others; otherwise the
 // consumers reduce to one record per unit through shared memory.
-template <int BPC, int NCW, int SV, int STAGES, int MINCTAS, class Src, class Acc>
-__global__ void __launch_bounds__((NCW + 1) * 32, MINCTAS)
+template <int BPC, int NCW, int SV, int STAGES, class Src, class Acc = TermSums<BPC>>
+__global__ void __launch_bounds__((NCW + 1) * 32)
     fused_stream_tma(const __grid_constant__ Src src, int units, int warp_records,
                      int planes_ready, Partial *__restrict__ partials) {
     constexpr uint32_t kStageBytes = SV * 16;  // per plane

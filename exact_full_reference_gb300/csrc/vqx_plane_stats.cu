@@ -71,37 +71,33 @@ int variant_index(int bpc, int kind) {  // kPlanes runs the fused statistics
     return bpc == 8 ? 0 : bpc == 10 ? 1 : bpc == 12 ? 2 : 3;
 }
 
-// Kernel, CTA size and dynamic shared memory of each stage-1 variant, and
-// the TMA pipeline's consumer warps and vectors per stage.
+// Kernel, CTA size and dynamic shared memory of each stage-1 variant.
 struct Stage1Shape {
     const void *fn;
     int threads;
     size_t smem;
-    int warps;
-    int stage_vecs;
 };
 
 template <int BPC, class Src, class Acc>
 constexpr auto stream_kernel() {
-    using Sh = vqx::TmaShape<Acc>;
-    return vqx::fused_stream_tma<BPC, Sh::kWarps, Sh::kStageVecs, Sh::kStages, Sh::kMinCtas, Src, Acc>;
+    return vqx::fused_stream_tma<BPC, vqx::kTmaWarps, vqx::kTmaStageVecs, vqx::kTmaStages, Src, Acc>;
 }
 
 template <int BPC, class Acc>
 Stage1Shape stage1_shape(int path) {
-    using Sh = vqx::TmaShape<Acc>;
-    const int nt = vqx::tma_threads<Acc>();
-    const size_t sm = vqx::tma_smem<Acc>();
     switch (path) {
     case kDense:
-        return {(const void *)stream_kernel<BPC, vqx::DenseSource, Acc>(), nt, sm, Sh::kWarps, Sh::kStageVecs};
+        return {(const void *)stream_kernel<BPC, vqx::DenseSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
     case kTiles:
-        return {(const void *)stream_kernel<BPC, vqx::TileSource, Acc>(), nt, sm, Sh::kWarps, Sh::kStageVecs};
+        return {(const void *)stream_kernel<BPC, vqx::TileSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
     case kRows:
-        return {(const void *)stream_kernel<BPC, vqx::RowSource, Acc>(), nt, sm, Sh::kWarps, Sh::kStageVecs};
+        return {(const void *)stream_kernel<BPC, vqx::RowSource, Acc>(), vqx::kTmaThreads,
+                vqx::kTmaSmem};
     case kFrames:
-        return {(const void *)vqx::fused_frames<BPC, Acc>, 32 * vqx::kFrameWarps, 0, 0, 0};
-    default: return {(const void *)vqx::fused_rows<BPC, Acc>, vqx::kThreads, 0, 0, 0};
+        return {(const void *)vqx::fused_frames<BPC, Acc>, 32 * vqx::kFrameWarps, 0};
+    default: return {(const void *)vqx::fused_rows<BPC, Acc>, vqx::kThreads, 0};
     }
 }
 
@@ -420,8 +416,6 @@ int validate_plane(const vqx_plane_desc &d, int bpc, int n_frames, size_t *pitch
 // ------------------------------------------------------------------ plan
 struct Plan {
     int path = kDense;
-    int stage_vecs = 0;      // TMA pipeline of the variant: vectors per stage
-    int warps = 0;           // and consumer warps
     int bpc = 8;
     int variant = 0;         // variant_index(bpc, kind)
     int segs = 1;
@@ -443,12 +437,11 @@ struct Plan {
 // the least work per frame wins, counting the zero fill past the last column
 // and row as work, with a fixed cost per stage and per box line (a box of
 // short lines copies measurably slower than one of long lines with some fill).
-void choose_box(size_t row_bytes, int height, long long max_by, long long stage_vecs, int *elem, int *bx,
-                int *by) {
+void choose_box(size_t row_bytes, int height, long long max_by, int *elem, int *bx, int *by) {
     int eb = 8;
     while (row_bytes % (size_t)eb) eb /= 2;
     const long long row_elems = (long long)(row_bytes / (size_t)eb);
-    const long long cap = stage_vecs * 16;
+    const long long cap = (long long)vqx::kTmaStageVecs * 16;
     const long long kStageCost = 128, kLineCost = 64;  // in vectors' worth of work
     long long best = -1;
     for (int x = 16 / eb; x <= 256; x += 16 / eb) {
@@ -511,9 +504,6 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
     Plan p;
     p.bpc = bpc;
     p.variant = variant_index(bpc, kind);
-    const Stage1Shape pipe = stage1_shape(kDense, p.variant);
-    p.stage_vecs = pipe.stage_vecs;
-    p.warps = pipe.warps;
     p.width = width;
     p.height = height;
     p.stride = stride;
@@ -545,12 +535,12 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
         // rows per CTA were the batch spread over every resident CTA
         long long max_by = (long long)height * frames_per_launch / (p.resident > 0 ? p.resident : 1);
         if (max_by < 1) max_by = 1;
-        choose_box(row_bytes, height, max_by, p.stage_vecs, &p.tile_elem, &p.tile_bx, &p.tile_by);
+        choose_box(row_bytes, height, max_by, &p.tile_elem, &p.tile_bx, &p.tile_by);
     }
     // Stage counts per unit: a dense or row-piece unit is cut into stages of
     // SV vectors, a tile unit into bands of boxes (segments of whole bands), a
     // scalar row unit into rows, one per warp (8 warps).
-    const uint32_t sv = (uint32_t)p.stage_vecs;
+    const uint32_t sv = (uint32_t)vqx::kTmaStageVecs;
     const uint32_t band = p.path == kTiles ? (uint32_t)p.tile_by : 1u;
     const uint32_t tiles_x =
         p.path == kTiles ? (uint32_t)((row_bytes / (size_t)p.tile_elem + p.tile_bx - 1) / p.tile_bx) : 1u;
@@ -571,7 +561,7 @@ Plan make_plan(const DeviceCtx &c, const void *ref, const void *dist, int width,
     };
     // at least half a stage (dense), a band (tiles) or a row per unit
     long long max_segs = p.path == kDense ? (long long)(2 * (uint64_t)work / sv) : (long long)(work / band);
-    p.rec_per_unit = p.path == kRowsScalar ? 1 : p.warps;
+    p.rec_per_unit = p.path == kRowsScalar ? 1 : vqx::kTmaWarps;
     UnitShape u = choose_segs(frames_per_launch, max_segs, p.resident, unit);
     if (u.segs * p.rec_per_unit > max_records) {
         p.rec_per_unit = 1;
@@ -633,8 +623,8 @@ cudaError_t launch_stage1_bpc(const Plan &p, const unsigned char *ref, const uns
     }
     // persistent: at most the resident CTAs, each walking several units
     cfg.gridDim = dim3((unsigned)(units < p.resident ? units : p.resident));
-    cfg.blockDim = dim3(vqx::tma_threads<Acc>());
-    cfg.dynamicSmemBytes = vqx::tma_smem<Acc>();
+    cfg.blockDim = dim3(vqx::kTmaThreads);
+    cfg.dynamicSmemBytes = vqx::kTmaSmem;
     cudaLaunchAttribute attr[1];
     if (overlap) {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
