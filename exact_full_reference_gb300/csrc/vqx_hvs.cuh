@@ -67,8 +67,9 @@ constexpr int kHvsThreads = 32 * kHvsLeaves;
 constexpr int kHvsLeafVecs = kHvsLeaf / 4;
 constexpr int kHvsLeafSlots = kHvsLeafVecs + kHvsLeafVecs / 8;
 constexpr size_t kHvsTablesSmem = (size_t)kHvsLeaves * kHvsLeafSlots * sizeof(float4);
-// Windows of 32 node records the walk loads at once.
-constexpr int kHvsWalkWindows = 4;
+// Windows of 32 node records the walk holds in registers at once (and as
+// many loading behind them).
+constexpr int kHvsWalkWindows = 2;
 
 // A transfer word is K itself.  The parity after a run needs no bit of its
 // own: from a state of parity p the run ends at m + K, whose parity is that
@@ -887,13 +888,33 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
     }
 }
 
-__device__ __forceinline__ HvsRec hvs_load_rec(const HvsRec *p) {
-    HvsRec r;
-    r.k = __ldcg(reinterpret_cast<const uint4 *>(p));
-    r.b = __ldcg(&p->b);
-    r.pad[0] = __ldcg(&p->pad[0]);
-    r.pad[1] = r.pad[2] = 0;
+// A record as the walk keeps it: its four transfer words, and its binade
+// and flags in one word (binade in the low 16 bits).  Records are read
+// through the read-only path: the tables kernel wrote them before the walk
+// started.
+struct HvsWalkRec {
+    uint4 k;
+    uint32_t bf;
+};
+
+__device__ __forceinline__ HvsWalkRec hvs_walk_rec(const HvsRec *p, bool in) {
+    HvsWalkRec r;
+    if (in) {
+        r.k = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(&p->b));
+        r.bf = w.x | (w.y << 16);
+    } else {
+        r.k = make_uint4(kHvsBad, kHvsBad, kHvsBad, kHvsBad);
+        r.bf = 0u;
+    }
     return r;
+}
+
+__device__ __forceinline__ HvsFn hvs_select_w(const HvsWalkRec &r, uint32_t b) {
+    const uint32_t rb = r.bf & 0xffffu;
+    if (b == rb) return {r.k.x, r.k.y};
+    if (b == rb + 1u) return {r.k.z, r.k.w};
+    return {kHvsBad, kHvsBad};
 }
 
 // One leaf, lane by lane, from state s.
@@ -921,12 +942,56 @@ __device__ __forceinline__ void hvs_walk_leaf(const HvsArgs &a, const float *pt,
     }
 }
 
+// The terms of node `node` of a plane into L2 (the warp's lanes share the
+// lines; none past the plane's terms).
+__device__ __forceinline__ void hvs_prefetch_terms(const HvsArgs &a, const float *pt, int node, int lane) {
+    const long long t0 = (long long)node * kHvsNode;
+#pragma unroll
+    for (int i = 0; i < kHvsNode / 32 / 32; i++) {
+        const long long t = t0 + ((long long)i * 32 + lane) * 32;
+        if (t < a.n_terms) asm volatile("prefetch.global.L2 [%0];" ::"l"(pt + t));
+    }
+}
+
+// Node `node` of a plane, leaf by leaf (its leaf records read once), and a
+// leaf whose run leaves the state's binade lane by lane.
+__device__ __forceinline__ void hvs_walk_node(const HvsArgs &a, const float *pt, const HvsRec *leaves,
+                                              int node, int lane, uint32_t &s, HvsOut &o) {
+    const long long l0 = (long long)node * kHvsLeaves;
+    const int nl = (int)min((long long)kHvsLeaves, (long long)a.n_leaves - l0);
+    const HvsWalkRec lr = hvs_walk_rec(leaves + l0 + lane, lane < nl);
+    hvs_prefetch_terms(a, pt, node, lane);  // for the leaf walked lane by lane, if any
+    int lf = 0;
+    while (lf < nl) {
+        const uint32_t b = hvs_binade(s);
+        const HvsFn g = lane >= lf && lane < nl ? hvs_select_w(lr, b) : hvs_identity();
+        lf = hvs_take(hvs_scan(g, lane), nl, lane, s);
+        if (lf < nl) {
+            hvs_walk_leaf(a, pt, l0 + lf, lane, s, o.replayed_runs);
+            o.replayed_leaves++;
+            lf++;
+        }
+    }
+}
+
 // One warp per plane: the walk over nodes, leaves and terms.  Writes the
 // plane's result (into host-mapped memory).  A node whose terms were not all
 // in [0, 2^95) ends the plane's walk before any of its terms are used: the
 // plane's sum is NaN and its flags say why.
-__global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
+// The node records go through registers in blocks of kHvsWalkWindows
+// windows of 32, the next block loading while this one is walked.  A window
+// is scanned from the first node not yet taken (the nodes before it count as
+// the identity), so a node walked leaf by leaf costs no reload of its
+// window; such a node's terms are prefetched into L2 as soon as it is met.
+// At most 80 registers a thread (the launch bound): a warp's registers come
+// from one of the SM's four sub-partitions, and beside a CTA of the next
+// call's hvs_tables_tma (27 warps of 72 registers) the least loaded one has
+// 2,560 left.  A walk that needs more waits for SMs the tables kernel holds,
+// and the tables CTAs it displaces start late (measured: pipelined steps
+// 244 -> 287 us at 98 registers).
+__global__ void __launch_bounds__(32, 24) hvs_walk(HvsArgs a, HvsOut *out) {
     allow_dependent_launch();  // the next call's tables may start on free SMs
+    constexpr int W = kHvsWalkWindows;
     const int plane = blockIdx.x, lane = threadIdx.x;
     HvsOut o;
     o.flags = 0;
@@ -936,60 +1001,43 @@ __global__ void __launch_bounds__(32) hvs_walk(HvsArgs a, HvsOut *out) {
     const HvsRec *nodes = a.nodes + (size_t)plane * (size_t)a.n_nodes;
     const HvsRec *leaves = a.leaves + (size_t)plane * (size_t)a.n_leaves;
     uint32_t s = 0u;  // the running sum, as float bits
-    int nd = 0;
-    bool range = false;
-    while (nd < a.n_nodes && !range) {
-        // The records of the next kHvsWalkWindows windows of 32 nodes, loaded
-        // together (the selection waits for the state; the loads need not).
-        HvsRec r[kHvsWalkWindows];
+    bool stop = false;
+    HvsWalkRec cur[W], nxt[W];
 #pragma unroll
-        for (int j = 0; j < kHvsWalkWindows; j++) {
-            const int i = nd + 32 * j + lane;
-            if (i < a.n_nodes) r[j] = hvs_load_rec(nodes + i);
-        }
-        bool partial = false;
+    for (int j = 0; j < W; j++) {
+        const int i = 32 * j + lane, i2 = 32 * (W + j) + lane;
+        cur[j] = hvs_walk_rec(nodes + i, i < a.n_nodes);
+        nxt[j] = hvs_walk_rec(nodes + i2, i2 < a.n_nodes);
+    }
+    for (int base = 0; base < a.n_nodes && !stop; base += 32 * W) {
 #pragma unroll
-        for (int j = 0; j < kHvsWalkWindows; j++) {
-            const int cnt = min(32, a.n_nodes - nd);  // window j starts at node nd
-            if (cnt <= 0) break;
-            const uint32_t b = hvs_binade(s);
-            HvsFn f = hvs_identity();
-            uint32_t nf = 0;
-            if (lane < cnt) {
-                f = hvs_select(r[j], b);
-                nf = r[j].pad[0];
-            }
-            o.flags |= __reduce_or_sync(0xffffffffu, nf) & kHvsFlagGuess;
-            if (__any_sync(0xffffffffu, nf & (kHvsFlagRange | kHvsFlagTimeout))) {
-                o.flags |= __reduce_or_sync(0xffffffffu, nf) & (kHvsFlagRange | kHvsFlagTimeout);
-                range = true;
+        for (int j = 0; j < W; j++) {
+            const int ws = base + 32 * j;
+            if (stop || ws >= a.n_nodes) break;
+            const int cnt = min(32, a.n_nodes - ws);
+            const uint32_t fl = __reduce_or_sync(0xffffffffu, lane < cnt ? cur[j].bf >> 16 : 0u);
+            o.flags |= fl & kHvsFlagGuess;
+            if (fl & (kHvsFlagRange | kHvsFlagTimeout)) {
+                o.flags |= fl & (kHvsFlagRange | kHvsFlagTimeout);
+                stop = true;
                 break;
             }
-            const int took = hvs_take(hvs_scan(f, lane), cnt, lane, s);
-            nd += took;
-            if (took < cnt) {
-                partial = true;
-                break;
+            int off = 0;
+            while (off < cnt) {
+                const uint32_t b = hvs_binade(s);
+                const HvsFn f = lane >= off && lane < cnt ? hvs_select_w(cur[j], b) : hvs_identity();
+                const int took = hvs_take(hvs_scan(f, lane), cnt, lane, s);
+                if (took >= cnt) break;
+                hvs_walk_node(a, pt, leaves, ws + took, lane, s, o);
+                off = took + 1;
             }
         }
-        if (range || !partial) continue;
-        // node nd, leaf by leaf
-        const long long l0 = (long long)nd * kHvsLeaves;
-        const int nl = (int)min((long long)kHvsLeaves, (long long)a.n_leaves - l0);
-        int lf = 0;
-        while (lf < nl) {
-            const int c2 = nl - lf;
-            const uint32_t bb = hvs_binade(s);
-            const HvsFn g =
-                lane < c2 ? hvs_select(hvs_load_rec(leaves + l0 + lf + lane), bb) : hvs_identity();
-            lf += hvs_take(hvs_scan(g, lane), c2, lane, s);
-            if (lf < nl) {
-                hvs_walk_leaf(a, pt, l0 + lf, lane, s, o.replayed_runs);
-                o.replayed_leaves++;
-                lf++;
-            }
+#pragma unroll
+        for (int j = 0; j < W; j++) {
+            const int i = base + 32 * (2 * W + j) + lane;
+            cur[j] = nxt[j];
+            nxt[j] = hvs_walk_rec(nodes + i, i < a.n_nodes);
         }
-        nd++;
     }
     if (lane == 0) {
         o.sum_bits = (o.flags & (kHvsFlagRange | kHvsFlagTimeout)) ? 0x7FC00000u : s;
