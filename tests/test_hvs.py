@@ -176,6 +176,28 @@ def test_one_very_long_plane(lib, orc):
     assert rec["sum"].tobytes() == sums.tobytes() and rec["score"].tobytes() == scores.tobytes()
 
 
+@pytest.mark.parametrize("growth", [2.0, 1.3, "steps"])
+def test_walk_crossings_node_after_node(lib, orc, growth):
+    """Sums that cross a power of two in node after node (growth 2: every
+    node of 8192 terms, over 80 nodes; 1.3: most, over 200; "steps": bursts
+    every fifth node, over 200): windows where many nodes are walked leaf by
+    leaf in turn, each window rescanned from the node after the last one
+    walked, across the walk's register blocks of 64 nodes."""
+    rng = np.random.default_rng(41)
+    nodes, node = (80 if growth == 2.0 else 200), 8192
+    k = np.repeat(np.arange(nodes), node).astype(np.float64)
+    if growth == "steps":
+        scale = np.where(k % 5 == 0, 2.0 ** (k / 5.0), 2.0 ** (k / 5.0) / 64.0)
+    else:
+        scale = growth ** k
+    t = np.empty((3, nodes * node), np.float32)
+    for p in range(3):
+        t[p] = (scale * rng.uniform(0.25, 1.0, nodes * node) / node).astype(np.float32)
+    t[:, rng.random(t.shape[1]) < 0.3] = 0.0
+    rec = check(lib, orc, t)
+    assert (rec["replayed_leaves"] > 0).all()
+
+
 def test_many_small_planes(lib, orc):
     """3000 planes of 37 terms: one node each, 3000 walks."""
     rng = np.random.default_rng(7)
