@@ -236,6 +236,7 @@ constexpr int kSumWarps = 4;  // blocks (one per warp) per CTA of ordered_block_
 __global__ void __launch_bounds__(32 * kSumWarps, 10)
     ordered_block_sums(const OrdPlanes g, u64 *__restrict__ sums, uint32_t *__restrict__ ors,
                        uint32_t *__restrict__ ssums, int *__restrict__ n_work, int planes_ready) {
+    allow_dependent_launch();  // this batch's classification may be scheduled now
     if (!planes_ready) grid_dependency_wait();
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *n_work = 0;
     const int lane = threadIdx.x & 31;
@@ -294,6 +295,8 @@ __global__ void __launch_bounds__(kClassThreads)
     ordered_classify(const u64 *__restrict__ sums, const uint32_t *__restrict__ ors,
                      const uint32_t *__restrict__ ssums, int nb, int *__restrict__ cls,
                      OrdWork *__restrict__ work, int *__restrict__ n_work, u64 *__restrict__ out) {
+    allow_dependent_launch();
+    grid_dependency_wait();  // the block sums are complete
     constexpr int kWarps = kClassThreads / 32;
     const int f = blockIdx.x, q = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int per = (nb + kClassThreads - 1) / kClassThreads;
@@ -438,6 +441,8 @@ constexpr int kTableWarps = 2;  // warps per CTA in ordered_tables (33 KB of sta
 __global__ void __launch_bounds__(32 * kTableWarps)
     ordered_tables(const OrdPlanes g, const int *__restrict__ cls, const OrdWork *__restrict__ work,
                    const int *__restrict__ n_work, OrdTable *__restrict__ tables) {
+    allow_dependent_launch();
+    grid_dependency_wait();  // the classification is complete
     __shared__ uint32_t terms_all[kTableWarps][kOrdBlock + kOrdBlock / kOrdLane];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     uint32_t *terms = terms_all[wib];
@@ -553,6 +558,7 @@ __global__ void __launch_bounds__(32)
                  const int *__restrict__ cls, const OrdTable *__restrict__ tables,
                  u64 *__restrict__ out) {
     allow_dependent_launch();  // the next batch's block sums may start on free SMs
+    grid_dependency_wait();    // the tables are complete
     const int f = blockIdx.x, q = blockIdx.y, lane = threadIdx.x;
     __shared__ uint32_t terms[kOrdBlock];
     const int nb = g.nb;

@@ -1312,22 +1312,29 @@ extern "C" int vqx_plane_stats_ordered_submit(const void *ref, const void *dist,
     if (pd->timed) cudaEventRecord(pd->ev[0], st);
     e = cudaLaunchKernelEx(&cfg, vqx::ordered_block_sums, g, sums, ors, ssums, n_work, ready);
     if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[1], st);
+    // The kernels after it are programmatic dependents too, each waiting
+    // for the one ahead before it reads: their CTAs are in place when it
+    // ends, and the next batch's block sums start during this batch's
+    // classification, tables and walk.
     if (e == cudaSuccess) {
-        vqx::ordered_classify<<<dim3(n_frames, vqx::kOrdSeqs), vqx::kClassThreads, 0, st>>>(
-            sums, ors, ssums, nb, cls, work, n_work, (u64 *)pd->rec.dev);
-        e = cudaGetLastError();
+        cfg.gridDim = dim3(n_frames, vqx::kOrdSeqs);
+        cfg.blockDim = dim3(vqx::kClassThreads);
+        e = cudaLaunchKernelEx(&cfg, vqx::ordered_classify, (const u64 *)sums, (const uint32_t *)ors,
+                               (const uint32_t *)ssums, nb, cls, work, n_work, (u64 *)pd->rec.dev);
     }
     if (e == cudaSuccess) {
         // a fixed grid of warps takes the tabulated blocks from the list
         const size_t jobs_max = (cells + vqx::kTableWarps - 1) / vqx::kTableWarps;
-        const unsigned grid = (unsigned)(jobs_max < (size_t)ctx->sms * 6 ? jobs_max : (size_t)ctx->sms * 6);
-        vqx::ordered_tables<<<grid, 32 * vqx::kTableWarps, 0, st>>>(g, cls, work, n_work, tables);
-        e = cudaGetLastError();
+        cfg.gridDim = dim3((unsigned)(jobs_max < (size_t)ctx->sms * 6 ? jobs_max : (size_t)ctx->sms * 6));
+        cfg.blockDim = dim3(32 * vqx::kTableWarps);
+        e = cudaLaunchKernelEx(&cfg, vqx::ordered_tables, g, (const int *)cls, (const vqx::OrdWork *)work,
+                               (const int *)n_work, tables);
     }
     if (e == cudaSuccess) {
-        vqx::ordered_walk<<<dim3(n_frames, vqx::kOrdSeqs), 32, 0, st>>>(g, sums, ors, cls, tables,
-                                                                         (u64 *)pd->rec.dev);
-        e = cudaGetLastError();
+        cfg.gridDim = dim3(n_frames, vqx::kOrdSeqs);
+        cfg.blockDim = dim3(32);
+        e = cudaLaunchKernelEx(&cfg, vqx::ordered_walk, g, (const u64 *)sums, (const uint32_t *)ors,
+                               (const int *)cls, (const vqx::OrdTable *)tables, (u64 *)pd->rec.dev);
     }
     if (e == cudaSuccess && pd->timed) cudaEventRecord(pd->ev[2], st);
     if (e == cudaSuccess) e = cudaEventRecord(pd->done, st);
