@@ -345,6 +345,7 @@ __device__ __forceinline__ bool hvs_lookback(const u64 *status, int node, int la
 // touches only this call's workspace, and reads the terms after that kernel
 // has finished unless they were ready before it started.
 __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
+    allow_dependent_launch();  // the walk may be scheduled now (it waits for this kernel)
     extern __shared__ float4 s_terms[];  // kHvsLeaves leaves, kHvsLeafSlots each
     __shared__ float s_leaf_sum[kHvsLeaves];
     __shared__ float s_excl;
@@ -608,6 +609,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
 
 __global__ void __launch_bounds__(kHvsTmaThreads, 1)
     hvs_tables_tma(const __grid_constant__ CUtensorMap tm, HvsArgs a, HvsTmaArgs t) {
+    allow_dependent_launch();  // the walk may be scheduled now (it waits for this kernel)
     constexpr int S = kHvsTmaStages;
     extern __shared__ __align__(1024) unsigned char hvs_raw[];
     unsigned char *ring = hvs_raw;
@@ -890,8 +892,10 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
 
 // A record as the walk keeps it: its four transfer words, and its binade
 // and flags in one word (binade in the low 16 bits).  Records are read
-// through the read-only path: the tables kernel wrote them before the walk
-// started.
+// through L2: the walk is launched as a programmatic dependent, before the
+// tables kernel that writes them has ended, and the read-only data path
+// needs data unchanged for the reading kernel's whole run (read through it,
+// the walk saw records of an earlier call in about one test in twelve).
 struct HvsWalkRec {
     uint4 k;
     uint32_t bf;
@@ -900,8 +904,8 @@ struct HvsWalkRec {
 __device__ __forceinline__ HvsWalkRec hvs_walk_rec(const HvsRec *p, bool in) {
     HvsWalkRec r;
     if (in) {
-        r.k = __ldg(reinterpret_cast<const uint4 *>(p));
-        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(&p->b));
+        r.k = __ldcg(reinterpret_cast<const uint4 *>(p));
+        const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(&p->b));
         r.bf = w.x | (w.y << 16);
     } else {
         r.k = make_uint4(kHvsBad, kHvsBad, kHvsBad, kHvsBad);
@@ -991,6 +995,7 @@ __device__ __forceinline__ void hvs_walk_node(const HvsArgs &a, const float *pt,
 // 244 -> 287 us at 98 registers).
 __global__ void __launch_bounds__(32, 24) hvs_walk(HvsArgs a, HvsOut *out) {
     allow_dependent_launch();  // the next call's tables may start on free SMs
+    grid_dependency_wait();    // this call's tables are complete
     constexpr int W = kHvsWalkWindows;
     const int plane = blockIdx.x, lane = threadIdx.x;
     HvsOut o;

@@ -45,10 +45,12 @@ typedef unsigned long long u64;
 //                      form it
 //   v[7]               0
 // The accumulators' totals() fill the same eight words; every word but v[5]
-// is a sum, v[5] an OR.
-struct Partial {
+// is a sum, v[5] an OR.  Records are 16-byte aligned (read as pairs of
+// words).
+struct __align__(16) Partial {
     u64 v[8];
 };
+static_assert(sizeof(Partial) == 64, "a record is 64 bytes");
 constexpr int kWords = 8;
 
 constexpr int kThreads = 256;     // CTA size of the strided-layout stage-1 kernel
@@ -991,10 +993,38 @@ __global__ void __launch_bounds__(kSumThreads)
     grid_dependency_wait();
     const int f = blockIdx.x;
     u64 t[kWords] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = threadIdx.x; s < per_frame; s += kSumThreads) {
-        const Partial &p = partials[(size_t)f * per_frame + s];
+    // Records go through L2: stage 1 lets this kernel start before it ends,
+    // and the read-only data path needs data unchanged for the reader's whole
+    // run.  Two records a thread are loaded at a time; this also keeps the
+    // kernel above 40 registers, so that its CTAs do not fit beside two
+    // running stage-1 CTAs while they wait: at 32 registers they did, and
+    // pipelined steps took 1-4 % longer (the next batch's stage-1 CTAs
+    // found the SMs they sat on short of registers).
+    const Partial *base = partials + (size_t)f * per_frame;
+    int s = threadIdx.x;
+    for (; s + kSumThreads < per_frame; s += 2 * kSumThreads) {
+        ulonglong2 v[2][kWords / 2];
 #pragma unroll
-        for (int k = 0; k < kWords; k++) t[k] = combine(k, t[k], p.v[k]);
+        for (int r = 0; r < 2; r++)
+#pragma unroll
+            for (int k = 0; k < kWords / 2; k++)
+                v[r][k] = __ldcg(reinterpret_cast<const ulonglong2 *>(base + s + r * kSumThreads) + k);
+#pragma unroll
+        for (int r = 0; r < 2; r++)
+#pragma unroll
+            for (int k = 0; k < kWords / 2; k++) {
+                t[2 * k] = combine(2 * k, t[2 * k], v[r][k].x);
+                t[2 * k + 1] = combine(2 * k + 1, t[2 * k + 1], v[r][k].y);
+            }
+    }
+    for (; s < per_frame; s += kSumThreads) {
+        const ulonglong2 *p = reinterpret_cast<const ulonglong2 *>(base + s);
+#pragma unroll
+        for (int k = 0; k < kWords / 2; k++) {
+            const ulonglong2 v = __ldcg(p + k);
+            t[2 * k] = combine(2 * k, t[2 * k], v.x);
+            t[2 * k + 1] = combine(2 * k + 1, t[2 * k + 1], v.y);
+        }
     }
     block_reduce_store<kSumThreads>(t, out[f].v);
 }

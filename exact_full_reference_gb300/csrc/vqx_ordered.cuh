@@ -278,6 +278,23 @@ struct OrdWork {
     int f, q, b;
 };
 
+// Loads of what a kernel ahead on the stream wrote.  The classification,
+// tables and walk are launched as programmatic dependents, before the kernels
+// ahead have ended; the read-only data path needs data unchanged for the
+// reading kernel's whole run, so these loads go through L2 instead.
+__device__ __forceinline__ OrdWork ld_work(const OrdWork *p) {
+    return OrdWork{__ldcg(&p->f), __ldcg(&p->q), __ldcg(&p->b)};
+}
+__device__ __forceinline__ OrdTable ld_table(const OrdTable *p) {
+    OrdTable t;
+    t.e[0] = __ldcg(&p->e[0]);
+    t.e[1] = __ldcg(&p->e[1]);
+    const int2 v = __ldcg(reinterpret_cast<const int2 *>(p->p));
+    t.p[0] = v.x;
+    t.p[1] = v.y;
+    return t;
+}
+
 constexpr int kOrdBatch = 8;  // chunks of 32 blocks loaded at once by the one-warp kernels
 constexpr int kOrdOut = 8;    // words per frame of the ordered kernels' output
 
@@ -304,10 +321,10 @@ __global__ void __launch_bounds__(kClassThreads)
     const size_t row = (size_t)f * nb;
     u64 mine = 0, sr = 0, sd = 0;
     for (int b = b0; b < b1; b++) {
-        mine += sums[(row + b) * kOrdSeqs + q];
+        mine += __ldcg(sums + (row + b) * kOrdSeqs + q);
         if (q == 0) {
-            sr += ssums[(row + b) * 2];
-            sd += ssums[(row + b) * 2 + 1];
+            sr += __ldcg(ssums + (row + b) * 2);
+            sd += __ldcg(ssums + (row + b) * 2 + 1);
         }
     }
     // exclusive prefix of this thread's run
@@ -330,14 +347,14 @@ __global__ void __launch_bounds__(kClassThreads)
     int ntab = 0;
     for (int b = b0; b < b1; b++) {
         const size_t in = (row + b) * kOrdSeqs + q;
-        const u64 T = sums[in], P1 = P + T;
+        const u64 T = __ldcg(sums + in), P1 = P + T;
         int c = kOrdReplay;
         if (P1 < kTwo53) {
             c = kOrdExact;
         } else if (P >= kTwo53 + kOrdMargin && binade_of(P - kOrdMargin) == binade_of(P1 + kOrdMargin)) {
             c = binade_of(P) - 52;
             // the running sum is a multiple of 2^c here; so are the terms?
-            if ((ors[in] & ((1u << c) - 1)) == 0) c = kOrdExact;
+            if ((__ldcg(ors + in) & ((1u << c) - 1)) == 0) c = kOrdExact;
         }
         cls[((size_t)f * kOrdSeqs + q) * nb + b] = c;
         ntab += c != kOrdExact && c != kOrdReplay;
@@ -446,11 +463,11 @@ __global__ void __launch_bounds__(32 * kTableWarps)
     __shared__ uint32_t terms_all[kTableWarps][kOrdBlock + kOrdBlock / kOrdLane];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     uint32_t *terms = terms_all[wib];
-    const int n = *n_work;
+    const int n = __ldcg(n_work);
     for (int w = blockIdx.x * kTableWarps + wib; w < n; w += gridDim.x * kTableWarps) {
-        const OrdWork job = work[w];
+        const OrdWork job = ld_work(work + w);
         const size_t slot = ((size_t)job.f * kOrdSeqs + job.q) * g.nb + job.b;
-        const int k = cls[slot];
+        const int k = __ldcg(cls + slot);
         const uint32_t len = ord_len(g, job.b);
         ord_block_pixels(g, job.f, job.b, lane, 32, [&](uint32_t j, uint32_t r, uint32_t d) {
             terms[j + j / kOrdLane] = ord_term(job.q, r, d);
@@ -574,11 +591,11 @@ __global__ void __launch_bounds__(32)
             const bool valid = b < nb;
             const size_t slot = ((size_t)f * kOrdSeqs + q) * nb + b;
             const size_t in = ((size_t)f * nb + b) * kOrdSeqs + q;
-            cB[u] = valid ? cls[slot] : kOrdExact;
-            TB[u] = valid ? sums[in] : 0;
-            oB[u] = valid ? ors[in] : 0;
+            cB[u] = valid ? __ldcg(cls + slot) : kOrdExact;
+            TB[u] = valid ? __ldcg(sums + in) : 0;
+            oB[u] = valid ? __ldcg(ors + in) : 0;
             tbB[u] = OrdTable{{0, 0}, {0, 1}};
-            if (valid && cB[u] != kOrdExact && cB[u] != kOrdReplay) tbB[u] = tables[slot];
+            if (valid && cB[u] != kOrdExact && cB[u] != kOrdReplay) tbB[u] = ld_table(tables + slot);
         }
 #pragma unroll
         for (int u = 0; u < kOrdBatch; u++) {

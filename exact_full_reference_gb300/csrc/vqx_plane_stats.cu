@@ -1552,8 +1552,12 @@ extern "C" int vqx_psnr_hvs_sum_submit(const float *terms, int64_t n_terms, int6
                 : cudaLaunchKernelEx(&cfg, vqx::hvs_tables, a);
     if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[1], st);
     if (e == cudaSuccess) {
-        vqx::hvs_walk<<<(unsigned)n_planes, 32, 0, st>>>(a, (vqx::HvsOut *)pd->rec.dev);
-        e = cudaGetLastError();
+        // a programmatic dependent of the tables: its warps are in place when
+        // they end (a walk warp fits beside a tables CTA)
+        cfg.gridDim = dim3((unsigned)n_planes);
+        cfg.blockDim = dim3(32);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, vqx::hvs_walk, a, (vqx::HvsOut *)pd->rec.dev);
     }
     if (e == cudaSuccess && pd->timed) e = cudaEventRecord(pd->ev[2], st);
     if (e == cudaSuccess) e = cudaEventRecord(pd->done, st);
