@@ -270,14 +270,18 @@ __device__ __forceinline__ int hvs_take(HvsFn scanned, int valid, int lane, uint
 }
 
 // The lane's kHvsLane terms starting at p, with `avail` of them inside the
-// plane; the rest read as +0, which adds nothing.
+// plane; the rest read as +0, which adds nothing.  Terms are read through
+// L2 (ld.global.cg) everywhere in these kernels, never through the read-only
+// data path: the kernels are programmatic dependents of the kernel ahead and
+// may start while a kernel that wrote the terms (the caller's, when it lets
+// its dependents start early) is still running.
 __device__ __forceinline__ void hvs_load(const float *p, long long avail, bool vec,
                                          float (&t)[kHvsLane]) {
     if (vec && avail >= kHvsLane) {
         const float4 *q = reinterpret_cast<const float4 *>(p);
 #pragma unroll
         for (int i = 0; i < kHvsLane / 4; i++) {
-            const float4 v = __ldg(q + i);
+            const float4 v = __ldcg(q + i);
             t[4 * i] = v.x;
             t[4 * i + 1] = v.y;
             t[4 * i + 2] = v.z;
@@ -285,7 +289,7 @@ __device__ __forceinline__ void hvs_load(const float *p, long long avail, bool v
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kHvsLane; i++) t[i] = i < avail ? __ldg(p + i) : 0.0f;
+        for (int i = 0; i < kHvsLane; i++) t[i] = i < avail ? __ldcg(p + i) : 0.0f;
     }
 }
 
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
 #pragma unroll
         for (int k = 0; k < kHvsLeafVecs / 32; k++) {
             const int q = lane + 32 * k;
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(lb) + q);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(lb) + q);
             sl[q + (q >> 3)] = v;
             const uint32_t ux = __float_as_uint(v.x), uy = __float_as_uint(v.y);
             const uint32_t uz = __float_as_uint(v.z), uw = __float_as_uint(v.w);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kHvsThreads, 6) hvs_tables(HvsArgs a) {
         float *sf = reinterpret_cast<float *>(sl);
         for (int k = 0; k < kHvsLeaf / 32; k++) {
             const int i = lane + 32 * k;
-            const float v = i < avail ? __ldg(lb + i) : 0.0f;
+            const float v = i < avail ? __ldcg(lb + i) : 0.0f;
             const int q = i >> 2;
             sf[4 * (q + (q >> 3)) + (i & 3)] = v;
             ls = __fadd_rn(ls, v);
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
                 // the partial row, if it is one of this leaf's rows
                 const long long row0 = (long long)node * kHvsNodeRows + (long long)leafw * 32;
                 if (t.tail && t.rows_full >= row0 && t.rows_full < row0 + 32 && lane < t.tail) {
-                    const float v = __ldg(planes + (size_t)plane * (size_t)a.pitch +
+                    const float v = __ldcg(planes + (size_t)plane * (size_t)a.pitch +
                                           (size_t)t.rows_full * 32 + lane);
                     ls = __fadd_rn(ls, v);
                     bad |= hvs_bad_term(v);
@@ -817,7 +821,7 @@ __global__ void __launch_bounds__(kHvsTmaThreads, 1)
                 // the partial row: its terms from the plane, zeros past its end
                 const float *src = planes + (size_t)plane * (size_t)a.pitch + (size_t)row * 32;
 #pragma unroll
-                for (int i = 0; i < kHvsLane; i++) tv[i] = i < t.tail ? __ldg(src + i) : 0.0f;
+                for (int i = 0; i < kHvsLane; i++) tv[i] = i < t.tail ? __ldcg(src + i) : 0.0f;
             } else {
                 const float4 *rw = reinterpret_cast<const float4 *>(
                     ring + (size_t)st * kHvsNodeBytes + (size_t)(lw * 32 + lane) * 128);

@@ -95,8 +95,13 @@ __device__ __forceinline__ uint32_t ord_term(int q, uint32_t r, uint32_t d) {
     return t[q];
 }
 
+// Plane loads go through L2 (ld.global.cg), not the read-only data path:
+// these kernels are programmatic dependents of the kernel ahead, so they
+// may start while a kernel that writes the planes is still running (the
+// caller's, when it lets its dependents start early), and the read-only path
+// needs data unchanged for the reading kernel's whole run.
 __device__ __forceinline__ uint4 ord_ld16(const unsigned char *p) {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+    return __ldcg(reinterpret_cast<const uint4 *>(p));
 }
 
 // Calls fn(j, r, d) for every pixel j of block b of frame f, the lanes
@@ -127,7 +132,8 @@ __device__ __forceinline__ void ord_block_pixels(const OrdPlanes &g, int f, int 
         const uint32_t n = min((uint32_t)g.width - x, len - j0);
         const unsigned short *rr = reinterpret_cast<const unsigned short *>(rf + (size_t)y * g.stride) + x;
         const unsigned short *dr = reinterpret_cast<const unsigned short *>(df + (size_t)y * g.stride) + x;
-        for (uint32_t k = tid; k < n; k += nthreads) fn(j0 + k, (uint32_t)rr[k], (uint32_t)dr[k]);
+        for (uint32_t k = tid; k < n; k += nthreads)
+            fn(j0 + k, (uint32_t)__ldcg(rr + k), (uint32_t)__ldcg(dr + k));
         j0 += n;
         y++;
         x = 0;
