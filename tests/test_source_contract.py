@@ -4,7 +4,7 @@ The pages guard their exact twins with source-level contract tests: each
 names a regression that would silently change a result and fails on a copy
 of the code with that regression planted ("ADR-1447: float_moment_hip adds
 the float squares the CPU adds, ...", Consequences: four planted regressions
-in the contract test).  These do the same for the three things here that the
+in the contract test).  These do the same for the four things here that the
 GPU parity tests could only catch on a GPU, and only for inputs that happen
 to exercise them:
 
@@ -14,7 +14,10 @@ to exercise them:
   reorder its double running sums);
 - every 32-bit accumulator run must hold its worst-case terms;
 - the packed fp32 square must stay one fused multiply-add with a +0 addend
-  (a plain packed multiply was found fused into the add that consumes it).
+  (a plain packed multiply was found fused into the add that consumes it);
+- kernels launched as programmatic dependents must not read through the
+  read-only data path (a walk that did returned an earlier call's records),
+  and the psnr_hvs walk must keep its register bound.
 
 Each check returns the problems it finds; every test also plants the
 regression in a copy of the text and asserts that the check reports it.
@@ -217,3 +220,69 @@ def test_planted_square_regressions_are_caught(old, new):
         src = f.read()
     planted = src.replace(old, new, 1)
     assert planted != src and check_square_form(planted)
+
+
+# ---------------------------------------------------------------- dependent launches
+# Kernels launched as programmatic dependents start before the kernel ahead
+# has ended; the read-only data path (__ldg, ld.global.nc) needs data
+# unchanged for the reading kernel's whole run, and a psnr_hvs walk that read
+# the tables' records through it returned records of an earlier call.  Every
+# kernel of the replay and psnr_hvs files is such a dependent, and so is
+# stage 2 (frame_sums) in the fused file.
+DEPENDENT_FILES = ("vqx_ordered.cuh", "vqx_hvs.cuh")
+
+
+def function_body(text, signature):
+    """The text of the function whose definition starts with ``signature``
+    (from its opening brace to the matching closing brace)."""
+    start = text.index(signature)
+    i = text.index("{", start)
+    depth = 0
+    for j in range(i, len(text)):
+        depth += {"{": 1, "}": -1}.get(text[j], 0)
+        if depth == 0:
+            return text[i : j + 1]
+    raise ValueError("unbalanced braces after %r" % signature)
+
+
+def check_dependent_loads(texts):
+    """texts: file name -> source.  Returns the problems found."""
+    problems = []
+    for name in DEPENDENT_FILES:
+        for m in re.finditer(r"__ldg\s*\(|ld\.global\.nc", texts[name]):
+            line = texts[name].count("\n", 0, m.start()) + 1
+            problems.append("%s:%d reads through the read-only data path" % (name, line))
+    body = function_body(texts["vqx_kernels.cuh"], "frame_sums(const Partial")
+    if re.search(r"__ldg\s*\(|ld\.global\.nc", body) or "__ldcg" not in body:
+        problems.append("frame_sums does not read the records through L2")
+    if not re.search(r"__launch_bounds__\(32,\s*24\)\s*hvs_walk", texts["vqx_hvs.cuh"]):
+        problems.append("hvs_walk lost its bound of 80 registers (it must fit beside a tables CTA)")
+    return problems
+
+
+def dependent_sources():
+    names = DEPENDENT_FILES + ("vqx_kernels.cuh",)
+    return {n: open(os.path.join(CSRC, n)).read() for n in names}
+
+
+def test_dependent_kernels_read_through_l2():
+    assert check_dependent_loads(dependent_sources()) == []
+
+
+@pytest.mark.parametrize("plant", ["walk_ldg", "ordered_ldg", "frame_sums_plain", "walk_bound"])
+def test_planted_dependent_load_regressions_are_caught(plant):
+    texts = dependent_sources()
+    if plant == "walk_ldg":
+        texts["vqx_hvs.cuh"] = texts["vqx_hvs.cuh"].replace("r.k = __ldcg(", "r.k = __ldg(", 1)
+    elif plant == "ordered_ldg":
+        texts["vqx_ordered.cuh"] = texts["vqx_ordered.cuh"].replace(
+            "return __ldcg(reinterpret_cast<const uint4 *>(p));",
+            "return __ldg(reinterpret_cast<const uint4 *>(p));", 1)
+    elif plant == "frame_sums_plain":
+        body = function_body(texts["vqx_kernels.cuh"], "frame_sums(const Partial")
+        texts["vqx_kernels.cuh"] = texts["vqx_kernels.cuh"].replace(body, body.replace("__ldcg", "__ldg"))
+    else:
+        texts["vqx_hvs.cuh"] = texts["vqx_hvs.cuh"].replace("__launch_bounds__(32, 24) hvs_walk",
+                                                            "__launch_bounds__(32) hvs_walk", 1)
+    assert texts != dependent_sources(), "the plant did not apply"
+    assert check_dependent_loads(texts), plant
